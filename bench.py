@@ -1,0 +1,383 @@
+#!/usr/bin/env python
+"""Benchmark of the gpt-oss MoE MLP block (libmoe_b300) on B300 GPUs.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one moe_forward over one batch of T synthetic tokens: router, top-4,
+selected softmax, permutation, grouped gate_up GEMM with clamped SwiGLU, grouped
+down GEMM, weighted combine.  The default workload is the gpt-oss-20b MoE layer
+at decode (T = 32, d = W = 2880, E = 32, top-4).  Inputs are resident in HBM
+when the timed region starts; L2 is flushed (a 256 MB write) before every timed
+step.  Prints ONE JSON line (rank 0).
+
+Under torchrun (N > 1) every rank runs an independent replica of the layer on
+its own GPU (the layer needs no exchange between GPUs); `value` is the tokens
+of all ranks over the slowest rank's time.
+
+--impl reference times the CPU oracle (fp64 numpy, the checker of this
+library) on a bounded token sample of the same workload; only rank 0 works.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from sparse_moe_transformer_selected_b300 import inputs as gen  # noqa: E402
+
+METRIC = "MoE-layer tokens/s at 20b/120b shapes; % of HBM or tensor-pipe roofline"
+STAGES = ["router_topk", "route_scan", "route_scatter", "gate_up", "down", "combine"]
+KERNEL_SOURCES = {
+    "router_topk": "router_topk.cu", "route_scan": "permute.cu", "route_scatter": "permute.cu",
+    "gate_up": "grouped_gemm_simt.cu", "down": "grouped_gemm_simt.cu", "combine": "combine.cu",
+}
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+def env_rank():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)),
+            int(os.environ.get("WORLD_SIZE", 1)))
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------ clocks --
+
+class ClockSampler:
+    """nvidia-smi SM clock / throttle-reason samples while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"moe_bench_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------- algorithmic work --
+
+def stage_work(wl: gen.Workload, counts: np.ndarray):
+    """Algorithmic bytes and flops of each kernel for one step (ideal traffic:
+    every operand read once, every result written once)."""
+    T, d, W, E, k = wl.T, wl.d, wl.W, wl.E, wl.k
+    R = T * k
+    active = int((counts > 0).sum())
+    gu_bytes_expert = 2 * W * d // 2 + 2 * W * d // 32 + 2 * W * 2          # codes, scales, bias
+    dn_bytes_expert = d * W // 2 + d * W // 32 + d * 2
+    return {
+        "router_topk": {"flops": 2 * T * d * E, "bytes": T * d * 2 + E * d * 4 + E * 4 + R * 12},
+        "route_scan": {"flops": 0, "bytes": 8 * E * ((T + 31) // 32) + 8 * (E + 1)},
+        "route_scatter": {"flops": 0, "bytes": R * d * 2 + T * d * 2 + R * 20},
+        "gate_up": {"flops": 2 * R * d * 2 * W,
+                    "bytes": active * gu_bytes_expert + R * d * 2 + R * W * 4,
+                    "unit": f"{active} active experts x {gu_bytes_expert} B + x_perm + h"},
+        "down": {"flops": 2 * R * W * d,
+                 "bytes": active * dn_bytes_expert + R * W * 4 + R * d * 4,
+                 "unit": f"{active} active experts x {dn_bytes_expert} B + h + y"},
+        "combine": {"flops": 2 * R * d, "bytes": R * d * 4 + T * d * 2 + R * 8},
+        "_active": active,
+    }
+
+
+def kernel_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu capture, if the kernel's source
+    is unchanged since (profiles/dram_traffic.txt: kernel workload sha bytes)."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    src = os.path.join(ROOT, "sparse_moe_transformer_selected_b300", "csrc", KERNEL_SOURCES[kernel])
+    if not os.path.exists(path) or not os.path.exists(src):
+        return None
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    with open(path) as f:
+        for line in f:
+            p = line.split()
+            if len(p) == 4 and not line.startswith("#") and p[0] == kernel and p[1] == workload \
+                    and p[2] == sha:
+                return float(p[3])
+    return None
+
+
+# ------------------------------------------------------------- CPU arm --
+
+def oracle_sample(inp, n_tokens: int, seed: int = 99):
+    from oracle import moe_oracle as O
+    rng = np.random.Generator(np.random.PCG64(seed))
+    tokens = np.sort(rng.choice(inp.wl.T, size=min(n_tokens, inp.wl.T), replace=False))
+    t0 = time.perf_counter()
+    O.moe_forward_inputs(inp, tokens=tokens)
+    return len(tokens), time.perf_counter() - t0
+
+
+def blas_threads() -> int:
+    try:
+        import threadpoolctl
+        info = threadpoolctl.threadpool_info()
+        return max([i.get("num_threads", 1) for i in info] or [1])
+    except Exception:
+        return 1
+
+
+def default_sample(wl: gen.Workload) -> int:
+    # the oracle dequantises each touched expert (~1.7 s at d = W = 2880), so a
+    # few tokens already take 10-30 s; small layers run whole
+    return wl.T if wl.d * wl.W <= 512 * 512 else 3
+
+
+def run_reference(args, wl):
+    rank, _, world = env_rank()
+    if rank != 0:
+        return
+    inp = gen.make_inputs(wl)
+    # size each step so the whole run stays within about 150 s of CPU time
+    _, t1 = oracle_sample(inp, 1, seed=7)
+    budget = 150.0 / (args.steps + args.warmup)
+    n = args.cpu_sample or max(1, min(default_sample(wl), int(budget / max(t1, 1e-3))))
+    for _ in range(max(0, args.warmup - 1)):
+        oracle_sample(inp, n, seed=7)
+    times, toks = [], 0
+    for s in range(args.steps):
+        nt, dt = oracle_sample(inp, n, seed=100 + s)
+        times.append(dt)
+        toks += nt
+    total = sum(times)
+    value = toks / total
+    cores = blas_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_block(wl, world),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{n} seeded tokens per step of the {wl.name} layer "
+                                   f"(routing of all {wl.T} tokens + expert FFN of the sample)"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_block(wl, world):
+    return {"workload": wl.name, "T": wl.T, "d_model": wl.d, "expert_width": wl.W,
+            "experts": wl.E, "top_k": wl.k, "weights": "MXFP4 (E2M1 x 32 + E8M0)",
+            "router_bias": wl.router_bias,
+            "l2": "flushed before every timed step (256 MB write)",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+
+
+# ------------------------------------------------------------- GPU arm --
+
+def run_ours(args, wl):
+    import torch
+    import torch.distributed as dist
+    from sparse_moe_transformer_selected_b300 import moe
+    from sparse_moe_transformer_selected_b300.device import DeviceMoE
+
+    rank, local_rank, world = env_rank()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (B300)")
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    moe.load()                                     # fails loudly if the library is missing
+
+    inp = gen.make_inputs(wl)
+    dev = DeviceMoE.upload(inp)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+
+    def flush_l2():
+        flush.fill_(1)
+
+    for _ in range(args.warmup):
+        dev.forward()
+    torch.cuda.synchronize()
+    counts = np.diff(dev.region("offsets").cpu().numpy())
+
+    # device-timed steps, each preceded by an L2 flush; stage events per step
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(args.steps)]
+    for row in ev:                                  # materialise the event handles
+        for e in row:
+            e.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        for s in range(args.steps):
+            flush_l2()
+            moe.moe_set_trace_events(ev[s])
+            dev.forward()
+        moe.moe_set_trace_events(None)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    step_ms = [r[0].elapsed_time(r[6]) for r in ev]
+    stage_ms = {name: [r[i].elapsed_time(r[i + 1]) for r in ev] for i, name in enumerate(STAGES)}
+    ms = statistics.fmean(step_ms)
+
+    # end to end through the public call: pinned host x in, pinned host out back
+    x_host = dev.x.cpu().pin_memory()
+    out_host = torch.empty_like(dev.out, device="cpu").pin_memory()
+    x_in = torch.empty_like(dev.x)
+    e2e_ms = []
+    for s in range(args.warmup + args.steps):
+        flush_l2()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        x_in.copy_(x_host, non_blocking=True)
+        dev.forward(x=x_in)
+        out_host.copy_(dev.out, non_blocking=True)
+        b.record(stream)
+        b.synchronize()
+        if s >= args.warmup:
+            e2e_ms.append(a.elapsed_time(b))
+    moe.moe_poll_status(dev.workspace)
+    e2e = statistics.fmean(e2e_ms)
+
+    if world > 1:
+        t = torch.tensor([ms, e2e], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, e2e = float(t[0]), float(t[1])
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    peaks, peak_src = load_peaks()
+    work = stage_work(wl, counts)
+    mean_stage = {k_: statistics.fmean(v) for k_, v in stage_ms.items()}
+    top = max(STAGES, key=lambda s_: mean_stage[s_])
+    wk = work[top]
+    intensity = wk["flops"] / max(1, wk["bytes"])
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    sec = mean_stage[top] * 1e-3
+    if intensity < ridge or wk["flops"] == 0:
+        roof = {"bound": "hbm", "achieved": wk["bytes"] / sec / 1e9, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s"}
+        peak_note = f"HBM copy bandwidth ({peak_src})"
+    else:
+        long_step = ms > 5.0
+        pk = peaks["bf16_tflops_sustained" if long_step else "bf16_tflops"]
+        roof = {"bound": "tensor", "achieved": wk["flops"] / sec / 1e12, "peak": pk,
+                "unit": "TFLOP/s"}
+        peak_note = (f"bf16 dense {'sustained' if long_step else 'burst'} ({peak_src})")
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = kernel_traffic(top, wl.name)
+    roof["kernel"] = top
+    roof["peak_source"] = peak_note
+    roof["algorithmic"] = {"bytes": wk["bytes"], "flops": wk["flops"], "per": wk.get("unit", "")}
+
+    tokens = wl.T * world
+    line = {
+        "metric": METRIC, "value": tokens / (ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded PCG64: x~N(0,1) bf16, random MXFP4 experts)",
+        "config": config_block(wl, world),
+        "clocks": clk.summary(),
+        "e2e": {"value": tokens / (e2e * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": int(dev.x.numel() * 2),
+                "d2h_bytes_per_step": int(dev.out.numel() * 2)},
+        "gpu_launches": len(STAGES) * args.steps,
+        "roofline": roof,
+        "stages_ms": {k_: round(v, 5) for k_, v in mean_stage.items()},
+        "active_experts": work["_active"],
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        n = args.cpu_sample or default_sample(wl)
+        nt, dt = oracle_sample(inp, n)
+        line["cpu_baseline"] = {
+            "value": nt / dt, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+            "sample": f"{nt} seeded tokens of the {wl.name} layer (routing of all {wl.T} "
+                      f"tokens + expert FFN of the sample), {dt:.1f} s"}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="gptoss20b_decode", choices=sorted(gen.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-sample", type=int, default=0, help="oracle tokens per CPU sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)      # at least 3 untimed warm-up steps
+    wl = gen.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, wl)
+    else:
+        run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    main()

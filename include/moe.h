@@ -1,0 +1,172 @@
+/*
+ * moe.h — C ABI of libmoe_b300.so, the gpt-oss Mixture-of-Experts MLP block on
+ * one NVIDIA B300 (sm_103a).
+ *
+ * What is computed (pages about the gpt-oss architecture, cited by title and
+ * section):
+ *   "OpenAI 最新开源模型 gpt-oss 架构与训练解析", section 模型架构, MoE bullet:
+ *     a router over E experts (32 for 20b, 128 for 120b), top-4 routing, softmax
+ *     weighting over the selected experts only, and experts that are gated
+ *     SwiGLU FFNs with clamping and a residual-style term;
+ *   same page, weight-quantisation bullet: expert weights in MXFP4 (4.25 bits);
+ *   same page, section 更深对比更宽: d_model = expert width = 2880;
+ *   "【LLM】GPT-OSS架构变化详解", section 2.4: the MoE replaces the single FFN
+ *     and a router picks the experts of each token.
+ *
+ * For token t with input x[t] (already normalised; the RMSNorm before the block
+ * is not part of this library):
+ *   logits[e] = x[t]·router_w[e] + router_b[e]                    (fp32)
+ *   S         = the k largest logits, ordered by (logit desc, index asc)
+ *   w_j       = exp(l_j - l_max) / Σ_{j'∈S} exp(l_j' - l_max)
+ *   z         = W_gu[e_j]·x[t] + b_gu[e_j]        (rows [0,W) gate, [W,2W) up)
+ *   g = min(z_gate, limit);  u = clamp(z_up, -limit, limit)
+ *   h         = g·σ(alpha·g)·(u + 1)
+ *   y_j       = W_dn[e_j]·h + b_dn[e_j]
+ *   out[t]    = bf16( Σ_j w_j·y_j )          (fp32 sum in slot order j = 0..k-1)
+ * No shared expert is added.  Plain SwiGLU is limit = +inf, alpha = 1 with the
+ * +1 absorbed into the up bias.
+ *
+ * MXFP4 weights: each row of a weight matrix is split along K (the reduction
+ * axis) into blocks of 32 elements; a block holds 32 E2M1 codes (sign bit 3,
+ * magnitude {0,0.5,1,1.5,2,3,4,6}[code&7]) and one E8M0 scale byte s meaning
+ * 2^(s-127) (s = 255 is NaN and must not occur).  Codes are packed two per byte,
+ * the even K index in the low nibble.
+ *
+ * Conventions common to every entry point
+ *   - Every data pointer is DEVICE memory owned by the caller; the library
+ *     allocates nothing and frees nothing.  Scratch comes from the caller's
+ *     `workspace` of at least moe_workspace_bytes(...) bytes.
+ *   - All work is enqueued on `stream` (a cudaStream_t passed as void*; NULL is
+ *     the legacy default stream).  No entry point synchronises, except
+ *     moe_poll_status.
+ *   - Pointers must be 16-byte aligned (the kernels move tiles with TMA and
+ *     16-byte vector loads); violations return MOE_ERR_ALIGN.
+ *   - Argument errors are detected on the host before anything is enqueued
+ *     and leave every output untouched.  A failed launch returns MOE_ERR_CUDA.
+ *     The message of the last failure on the calling thread is returned by
+ *     moe_last_error().
+ *   - Device-side failures (a bounded wait that ran out, an index out of range)
+ *     do not trap: the kernel records a code in the workspace status word and
+ *     returns; read it with moe_poll_status.
+ *   - T = 0 returns MOE_OK and enqueues nothing.
+ *   - Shape limits: d % 32 == 0, W % 32 == 0 (whole MX blocks), 1 <= E <= 256,
+ *     1 <= k <= min(E, 8), 1 <= T, T·k < 2^31.
+ *   - Determinism: for fixed inputs every output is bitwise reproducible run to
+ *     run (no floating-point atomics; fixed reduction orders).
+ */
+#ifndef MOE_B300_H
+#define MOE_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_NULL = 1,        /* a required pointer is NULL */
+  MOE_ERR_SHAPE = 2,       /* a size violates the limits above */
+  MOE_ERR_ALIGN = 3,       /* a pointer is not 16-byte aligned */
+  MOE_ERR_WORKSPACE = 4,   /* workspace smaller than moe_workspace_bytes() */
+  MOE_ERR_UNSUPPORTED = 5, /* no sm_103a device, or a feature this build lacks */
+  MOE_ERR_CUDA = 6,        /* a CUDA runtime/driver call failed */
+  MOE_ERR_TIMEOUT = 7,     /* device: a bounded wait ran out (status word) */
+  MOE_ERR_DEVICE_BOUNDS = 8 /* device: an index was out of range (status word) */
+} moe_status;
+
+/*
+ * Bytes of scratch moe_forward / moe_route need for this shape (0 for T = 0).
+ * The workspace holds the routing tables, the permuted activations, the hidden
+ * activations h and the per-row expert outputs y; its first 256 bytes are the
+ * device status word.  Returns 0 and sets moe_last_error() for invalid shapes.
+ */
+size_t moe_workspace_bytes(int64_t T, int d, int W, int E, int k);
+
+/*
+ * The whole MoE block: router, top-k, selected softmax, permutation, grouped
+ * gate_up GEMM with the clamped SwiGLU, grouped down GEMM, weighted combine.
+ *
+ *   x_bf16      [T, d]        bf16, row-major
+ *   router_w    [E, d]        fp32
+ *   router_b    [E]           fp32
+ *   w_gu_fp4    [E, 2W, d/2]  packed E2M1 (gate rows then up rows)
+ *   w_gu_scale  [E, 2W, d/32] E8M0
+ *   b_gu_bf16   [E, 2W]       bf16
+ *   w_dn_fp4    [E, d, W/2]   packed E2M1
+ *   w_dn_scale  [E, d, W/32]  E8M0
+ *   b_dn_bf16   [E, d]        bf16
+ *   limit       clamp bound (7.0 for gpt-oss; +inf disables the clamp)
+ *   alpha       sigmoid slope (1.702 for gpt-oss)
+ *   out_bf16    [T, d]        bf16, written completely
+ * Precision: router logits, softmax and all accumulation in fp32; h is carried
+ * between the two GEMMs as a pair of bf16 terms (hi + lo, about 16 significant
+ * bits); y is fp32; out is rounded once, to nearest even.
+ */
+moe_status moe_forward(const void* x_bf16, int64_t T, int d, int W,
+                       const float* router_w, const float* router_b,
+                       const uint8_t* w_gu_fp4, const uint8_t* w_gu_scale, const void* b_gu_bf16,
+                       const uint8_t* w_dn_fp4, const uint8_t* w_dn_scale, const void* b_dn_bf16,
+                       int E, int k, float limit, float alpha,
+                       void* out_bf16, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Routing only (the first two stages of moe_forward), with its tables returned:
+ *   topk_idx  [T, k]  int32   selected experts, slot order (logit desc, index asc)
+ *   topk_w    [T, k]  fp32    softmax over the selected logits
+ *   offsets   [E + 1] int32   offsets[e] = first permuted row of expert e,
+ *                             offsets[E] = T·k
+ *   perm      [T·k]   int32   permuted row -> t·k + j; rows sorted by
+ *                             (expert, token, slot)
+ *   inv       [T, k]  int32   (t, j) -> permuted row
+ * Any of the five output pointers may be NULL to skip that table.  The
+ * workspace is the same as moe_forward's.
+ */
+moe_status moe_route(const void* x_bf16, int64_t T, int d,
+                     const float* router_w, const float* router_b, int E, int k,
+                     int32_t* topk_idx, float* topk_w, int32_t* offsets,
+                     int32_t* perm, int32_t* inv,
+                     void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Synchronises `stream`, then reads and returns the device status word of
+ * `workspace` (MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_DEVICE_BOUNDS) left by the
+ * last call that used this workspace.  Returns MOE_ERR_CUDA if the stream
+ * itself reports an error.
+ */
+moe_status moe_poll_status(const void* workspace, void* stream);
+
+/* Message describing the last failure on the calling thread ("" if none). */
+const char* moe_last_error(void);
+
+/*
+ * Where an intermediate table lives inside the workspace, for inspection in
+ * tests: writes its byte offset and size.  Contents are valid after a
+ * moe_forward (or, for the routing tables, moe_route) on that workspace.
+ *   which: 0 topk_idx int32[T,k]   1 topk_w fp32[T,k]     2 offsets int32[E+1]
+ *          3 perm int32[T·k]       4 inv int32[T,k]       5 x_perm bf16[T·k,d]
+ *          6 h_hi bf16[T·k,W]      7 h_lo bf16[T·k,W]     8 y fp32[T·k,d]
+ * Returns MOE_ERR_SHAPE for an invalid shape or `which`.
+ */
+moe_status moe_workspace_region(int64_t T, int d, int W, int E, int k, int which,
+                                size_t* offset, size_t* bytes);
+
+/*
+ * Tracing aid: make moe_forward calls from the calling thread record CUDA
+ * events at its stage boundaries, on the call's stream.  `events` holds n = 7
+ * cudaEvent_t handles (as void*) created by the caller:
+ *   [0] before the router   [1] after router/top-k   [2] after the scan
+ *   [3] after the permute   [4] after gate_up        [5] after down
+ *   [6] after the combine
+ * n = 0 (or events = NULL) turns tracing off.  The handles are used by every
+ * later moe_forward on this thread until replaced; the caller keeps them alive.
+ * Returns MOE_ERR_SHAPE for any other n.
+ */
+moe_status moe_set_trace_events(void* const* events, int n);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_B300_H */

@@ -1,0 +1,53 @@
+// K5 — weighted unpermute-combine.
+//
+// out[t] = bf16( Σ_j w[t,j] · y[inv[t,j]] ): the softmax-weighted sum of the
+// selected experts' outputs ("OpenAI 最新开源模型 gpt-oss 架构与训练解析", 模型架构,
+// MoE bullet; no shared expert is added, section 更少的大专家 vs 更多的小专家).
+// fp32 accumulation in slot order j = 0..k-1, one rounding to bf16 (nearest
+// even).  Bandwidth-bound: k rows of fp32 read, one bf16 row written.
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 128;
+
+__global__ void __launch_bounds__(kThreads)
+combine_kernel(const float* __restrict__ y, const float* __restrict__ topk_w,
+               const int32_t* __restrict__ inv, int d, int k,
+               __nv_bfloat16* __restrict__ out) {
+  const int t = blockIdx.x;
+  int32_t rows[8];
+  float w[8];
+  for (int j = 0; j < k; ++j) {
+    rows[j] = inv[(size_t)t * k + j];
+    w[j] = topk_w[(size_t)t * k + j];
+  }
+  const int n4 = d / 4;
+  for (int i = threadIdx.x; i < n4; i += kThreads) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < k; ++j) {
+      const float4 v = *reinterpret_cast<const float4*>(y + (size_t)rows[j] * d + 4 * i);
+      acc.x = fmaf(w[j], v.x, acc.x);
+      acc.y = fmaf(w[j], v.y, acc.y);
+      acc.z = fmaf(w[j], v.z, acc.z);
+      acc.w = fmaf(w[j], v.w, acc.w);
+    }
+    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+    uint2 pk;
+    pk.x = *reinterpret_cast<uint32_t*>(&lo);
+    pk.y = *reinterpret_cast<uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(out + (size_t)t * d + 4 * i) = pk;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const float* y, const float* topk_w, const int32_t* inv, int T,
+                           int d, int k, __nv_bfloat16* out, cudaStream_t s) {
+  combine_kernel<<<T, kThreads, 0, s>>>(y, topk_w, inv, d, k, out);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

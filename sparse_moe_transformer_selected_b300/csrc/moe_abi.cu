@@ -1,0 +1,288 @@
+// C ABI of libmoe_b300 (declared in include/moe.h): argument checking, the
+// workspace layout and the launch sequence K1 -> K5 on the caller's stream.
+#include "moe.h"
+#include "common.cuh"
+
+#include <stdarg.h>
+#include <stdio.h>
+
+#include <mutex>
+#include <string>
+
+namespace {
+
+thread_local std::string g_last_error;
+constexpr int kTraceEvents = 7;
+thread_local cudaEvent_t g_trace[kTraceEvents];
+thread_local bool g_trace_on = false;
+
+cudaError_t trace(int i, cudaStream_t s) {
+  return g_trace_on ? cudaEventRecord(g_trace[i], s) : cudaSuccess;
+}
+
+moe_status fail(moe_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+moe_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(MOE_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+moe_status check_shape(int64_t T, int d, int W, int E, int k) {
+  if (T < 0) return fail(MOE_ERR_SHAPE, "T = %lld < 0", (long long)T);
+  if (d <= 0 || d % 32) return fail(MOE_ERR_SHAPE, "d = %d must be a positive multiple of 32", d);
+  if (W <= 0 || W % 32) return fail(MOE_ERR_SHAPE, "W = %d must be a positive multiple of 32", W);
+  if (E < 1 || E > 256) return fail(MOE_ERR_SHAPE, "E = %d outside [1, 256]", E);
+  if (k < 1 || k > 8 || k > E) return fail(MOE_ERR_SHAPE, "k = %d outside [1, min(E, 8)]", k);
+  if (T * k >= (int64_t(1) << 31)) return fail(MOE_ERR_SHAPE, "T*k = %lld too large", (long long)(T * k));
+  return MOE_OK;
+}
+
+bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
+
+// sm_103 check, once per device.
+moe_status check_device() {
+  static std::mutex mu;
+  static int verdict[64];  // 0 unknown, 1 ok, 2 unsupported
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(MOE_ERR_UNSUPPORTED, "device ordinal %d", dev);
+  std::lock_guard<std::mutex> lock(mu);
+  if (verdict[dev] == 0) {
+    int major = 0, minor = 0;
+    e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    verdict[dev] = (major == 10 && minor == 3) ? 1 : 2;
+    if (verdict[dev] == 2) {
+      g_last_error = "device is sm_" + std::to_string(major) + std::to_string(minor) +
+                     "; this library is built for sm_103a only";
+    }
+  }
+  if (verdict[dev] != 1) return fail(MOE_ERR_UNSUPPORTED, "device is not sm_103 (B300)");
+  return MOE_OK;
+}
+
+template <class T>
+T* at(void* base, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(base) + off);
+}
+
+struct RouteOut {
+  int32_t* topk_idx;
+  float* topk_w;
+  int32_t* rank;
+  int32_t* tile_counts;
+  int32_t* tile_base;
+  int32_t* offsets;
+  int32_t* mtile_off;
+  int32_t* perm;
+  int32_t* inv;
+  __nv_bfloat16* x_perm;
+  int32_t* status;
+};
+
+RouteOut route_tables(void* ws, const moe::Workspace& L, bool gather) {
+  RouteOut r;
+  r.topk_idx = at<int32_t>(ws, L.topk_idx);
+  r.topk_w = at<float>(ws, L.topk_w);
+  r.rank = at<int32_t>(ws, L.rank);
+  r.tile_counts = at<int32_t>(ws, L.tile_counts);
+  r.tile_base = at<int32_t>(ws, L.tile_base);
+  r.offsets = at<int32_t>(ws, L.offsets);
+  r.mtile_off = at<int32_t>(ws, L.mtile_off);
+  r.perm = at<int32_t>(ws, L.perm);
+  r.inv = at<int32_t>(ws, L.inv);
+  r.x_perm = gather ? at<__nv_bfloat16>(ws, L.x_perm) : nullptr;
+  r.status = at<int32_t>(ws, L.status);
+  return r;
+}
+
+moe_status run_route(const void* x, int64_t T, int d, const float* rw, const float* rb, int E,
+                     int k, const RouteOut& r, cudaStream_t s) {
+  const auto* xb = static_cast<const __nv_bfloat16*>(x);
+  const int ntiles = int((T + moe::kRouterTile - 1) / moe::kRouterTile);
+  cudaError_t e = moe::launch_router_topk(xb, rw, rb, int(T), d, E, k, r.topk_idx, r.topk_w,
+                                          r.rank, r.tile_counts, r.status, s);
+  if (e != cudaSuccess) return cuda_fail(e, "router_topk launch");
+  if ((e = trace(1, s)) != cudaSuccess) return cuda_fail(e, "trace event");
+  e = moe::launch_route_scan(r.tile_counts, ntiles, E, r.tile_base, r.offsets, r.mtile_off, s);
+  if (e != cudaSuccess) return cuda_fail(e, "route_scan launch");
+  if ((e = trace(2, s)) != cudaSuccess) return cuda_fail(e, "trace event");
+  e = moe::launch_route_scatter(xb, int(T), d, E, k, r.topk_idx, r.rank, r.tile_base, r.perm,
+                                r.inv, r.x_perm, r.status, s);
+  if (e != cudaSuccess) return cuda_fail(e, "route_scatter launch");
+  if ((e = trace(3, s)) != cudaSuccess) return cuda_fail(e, "trace event");
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t moe_workspace_bytes(int64_t T, int d, int W, int E, int k) {
+  if (check_shape(T, d, W, E, k) != MOE_OK) return 0;
+  if (T == 0) return 0;
+  return moe::workspace_layout(T, d, W, E, k).total;
+}
+
+moe_status moe_workspace_region(int64_t T, int d, int W, int E, int k, int which,
+                                size_t* offset, size_t* bytes) {
+  moe_status st = check_shape(T, d, W, E, k);
+  if (st != MOE_OK) return st;
+  if (!offset || !bytes) return fail(MOE_ERR_NULL, "offset/bytes pointer is NULL");
+  const moe::Workspace L = moe::workspace_layout(T, d, W, E, k);
+  const size_t R = size_t(T) * k;
+  switch (which) {
+    case 0: *offset = L.topk_idx; *bytes = R * 4; break;
+    case 1: *offset = L.topk_w; *bytes = R * 4; break;
+    case 2: *offset = L.offsets; *bytes = size_t(E + 1) * 4; break;
+    case 3: *offset = L.perm; *bytes = R * 4; break;
+    case 4: *offset = L.inv; *bytes = R * 4; break;
+    case 5: *offset = L.x_perm; *bytes = R * d * 2; break;
+    case 6: *offset = L.h_hi; *bytes = R * W * 2; break;
+    case 7: *offset = L.h_lo; *bytes = R * W * 2; break;
+    case 8: *offset = L.y; *bytes = R * d * 4; break;
+    default: return fail(MOE_ERR_SHAPE, "unknown workspace region %d", which);
+  }
+  return MOE_OK;
+}
+
+moe_status moe_forward(const void* x_bf16, int64_t T, int d, int W, const float* router_w,
+                       const float* router_b, const uint8_t* w_gu_fp4, const uint8_t* w_gu_scale,
+                       const void* b_gu_bf16, const uint8_t* w_dn_fp4, const uint8_t* w_dn_scale,
+                       const void* b_dn_bf16, int E, int k, float limit, float alpha,
+                       void* out_bf16, void* workspace, size_t workspace_bytes, void* stream) {
+  moe_status st = check_shape(T, d, W, E, k);
+  if (st != MOE_OK) return st;
+  const void* ptrs[] = {x_bf16, router_w, router_b, w_gu_fp4, w_gu_scale, b_gu_bf16,
+                        w_dn_fp4, w_dn_scale, b_dn_bf16, out_bf16, workspace};
+  const char* names[] = {"x", "router_w", "router_b", "w_gu", "w_gu_scale", "b_gu",
+                         "w_dn", "w_dn_scale", "b_dn", "out", "workspace"};
+  for (int i = 0; i < 11; ++i) {
+    if (T > 0 && !ptrs[i]) return fail(MOE_ERR_NULL, "%s is NULL", names[i]);
+    if (misaligned(ptrs[i])) return fail(MOE_ERR_ALIGN, "%s is not 16-byte aligned", names[i]);
+  }
+  if (alpha != alpha || limit != limit) return fail(MOE_ERR_SHAPE, "limit/alpha is NaN");
+  if (T == 0) return MOE_OK;
+  const moe::Workspace L = moe::workspace_layout(T, d, W, E, k);
+  if (workspace_bytes < L.total)
+    return fail(MOE_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", workspace_bytes, L.total);
+  st = check_device();
+  if (st != MOE_OK) return st;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const RouteOut r = route_tables(workspace, L, true);
+  cudaError_t e = trace(0, s);
+  if (e != cudaSuccess) return cuda_fail(e, "trace event");
+  st = run_route(x_bf16, T, d, router_w, router_b, E, k, r, s);
+  if (st != MOE_OK) return st;
+
+  moe::GemmArgs a;
+  a.R = int(T * k);
+  a.d = d;
+  a.W = W;
+  a.E = E;
+  a.offsets = r.offsets;
+  a.mtile_off = r.mtile_off;
+  a.x_perm = r.x_perm;
+  a.w_gu = w_gu_fp4;
+  a.w_gu_scale = w_gu_scale;
+  a.b_gu = static_cast<const __nv_bfloat16*>(b_gu_bf16);
+  a.w_dn = w_dn_fp4;
+  a.w_dn_scale = w_dn_scale;
+  a.b_dn = static_cast<const __nv_bfloat16*>(b_dn_bf16);
+  a.limit = limit;
+  a.alpha = alpha;
+  a.h_hi = at<__nv_bfloat16>(workspace, L.h_hi);
+  a.h_lo = at<__nv_bfloat16>(workspace, L.h_lo);
+  a.y = at<float>(workspace, L.y);
+  a.status = r.status;
+  e = moe::launch_gateup(a, s);
+  if (e != cudaSuccess) return cuda_fail(e, "gate_up launch");
+  if ((e = trace(4, s)) != cudaSuccess) return cuda_fail(e, "trace event");
+  e = moe::launch_down(a, s);
+  if (e != cudaSuccess) return cuda_fail(e, "down launch");
+  if ((e = trace(5, s)) != cudaSuccess) return cuda_fail(e, "trace event");
+  e = moe::launch_combine(a.y, r.topk_w, r.inv, int(T), d, k,
+                          static_cast<__nv_bfloat16*>(out_bf16), s);
+  if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+  if ((e = trace(6, s)) != cudaSuccess) return cuda_fail(e, "trace event");
+  return MOE_OK;
+}
+
+moe_status moe_route(const void* x_bf16, int64_t T, int d, const float* router_w,
+                     const float* router_b, int E, int k, int32_t* topk_idx, float* topk_w,
+                     int32_t* offsets, int32_t* perm, int32_t* inv, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+  // The route tables do not depend on W; use the smallest legal width for sizing.
+  moe_status st = check_shape(T, d, 32, E, k);
+  if (st != MOE_OK) return st;
+  const void* ptrs[] = {x_bf16, router_w, router_b, workspace, topk_idx, topk_w, offsets, perm, inv};
+  const char* names[] = {"x", "router_w", "router_b", "workspace", "topk_idx", "topk_w",
+                         "offsets", "perm", "inv"};
+  for (int i = 0; i < 9; ++i) {
+    if (i < 4 && T > 0 && !ptrs[i]) return fail(MOE_ERR_NULL, "%s is NULL", names[i]);
+    if (misaligned(ptrs[i])) return fail(MOE_ERR_ALIGN, "%s is not 16-byte aligned", names[i]);
+  }
+  if (T == 0) return MOE_OK;
+  const moe::Workspace L = moe::workspace_layout(T, d, 32, E, k);
+  // Only the routing prefix of the layout is touched: everything before x_perm.
+  if (workspace_bytes < L.x_perm)
+    return fail(MOE_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", workspace_bytes, L.x_perm);
+  st = check_device();
+  if (st != MOE_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const RouteOut r = route_tables(workspace, L, false);
+  st = run_route(x_bf16, T, d, router_w, router_b, E, k, r, s);
+  if (st != MOE_OK) return st;
+  const size_t R = size_t(T) * k;
+  struct { void* dst; const void* src; size_t n; } copies[] = {
+      {topk_idx, r.topk_idx, R * 4}, {topk_w, r.topk_w, R * 4},
+      {offsets, r.offsets, size_t(E + 1) * 4}, {perm, r.perm, R * 4}, {inv, r.inv, R * 4}};
+  for (auto& c : copies) {
+    if (!c.dst) continue;
+    cudaError_t e = cudaMemcpyAsync(c.dst, c.src, c.n, cudaMemcpyDeviceToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync of a route table");
+  }
+  return MOE_OK;
+}
+
+moe_status moe_poll_status(const void* workspace, void* stream) {
+  if (!workspace) return fail(MOE_ERR_NULL, "workspace is NULL");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  int32_t word = 0;
+  e = cudaMemcpy(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy of the status word");
+  if (word == MOE_ERR_TIMEOUT) return fail(MOE_ERR_TIMEOUT, "a device-side wait ran out");
+  if (word == MOE_ERR_DEVICE_BOUNDS) return fail(MOE_ERR_DEVICE_BOUNDS, "a device index was out of range");
+  if (word != 0) return fail(MOE_ERR_CUDA, "unexpected device status %d", word);
+  return MOE_OK;
+}
+
+const char* moe_last_error(void) { return g_last_error.c_str(); }
+
+moe_status moe_set_trace_events(void* const* events, int n) {
+  if (n == 0 || events == nullptr) {
+    g_trace_on = false;
+    return MOE_OK;
+  }
+  if (n != kTraceEvents) return fail(MOE_ERR_SHAPE, "need %d trace events, got %d", kTraceEvents, n);
+  for (int i = 0; i < kTraceEvents; ++i) {
+    if (!events[i]) return fail(MOE_ERR_NULL, "trace event %d is NULL", i);
+    g_trace[i] = static_cast<cudaEvent_t>(events[i]);
+  }
+  g_trace_on = true;
+  return MOE_OK;
+}
+
+}  // extern "C"

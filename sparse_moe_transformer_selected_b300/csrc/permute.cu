@@ -1,0 +1,125 @@
+// K2 — expert histogram scan and token permutation.
+//
+// The pages fix only that each token is processed by its selected experts
+// ("OpenAI 最新开源模型 gpt-oss 架构与训练解析", 模型架构, MoE bullet); grouping the
+// routed rows by expert is what lets each expert run as one dense GEMM.  Rows
+// are ordered by (expert, token, slot).  Since a token never picks an expert
+// twice, a row's place is offsets[e] + (rows of e in earlier router tiles) +
+// (rank inside its tile), all integer and order-free, so the permutation is
+// deterministic without atomics.
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kScanThreads = 1024;
+
+// One CTA.  Thread (g, e) sums expert e over a contiguous range of tiles,
+// then the partial sums are scanned in tile order and in expert order.
+__global__ void __launch_bounds__(kScanThreads)
+route_scan_kernel(const int32_t* __restrict__ tile_counts, int ntiles, int E,
+                  int32_t* __restrict__ tile_base, int32_t* __restrict__ offsets,
+                  int32_t* __restrict__ mtile_off) {
+  __shared__ int32_t part[kScanThreads];
+  __shared__ int32_t total[257];
+  __shared__ int32_t off[257];
+  const int tid = threadIdx.x;
+  const int G = kScanThreads / E;           // E <= 256 -> G >= 4
+  const int g = tid / E, e = tid - g * E;
+  const bool active = g < G;
+  const int chunk = (ntiles + G - 1) / G;
+  const int ta = min(ntiles, g * chunk), tb = min(ntiles, ta + chunk);
+  int32_t sum = 0;
+  if (active)
+    for (int t = ta; t < tb; ++t) sum += tile_counts[(size_t)t * E + e];
+  part[tid] = sum;
+  __syncthreads();
+  if (tid < E) {
+    int32_t run = 0;
+    for (int q = 0; q < G; ++q) {
+      const int32_t v = part[q * E + tid];
+      part[q * E + tid] = run;
+      run += v;
+    }
+    total[tid] = run;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int32_t run = 0, mrun = 0;
+    for (int q = 0; q < E; ++q) {
+      off[q] = run;
+      offsets[q] = run;
+      mtile_off[q] = mrun;
+      run += total[q];
+      mrun += (total[q] + kGemmBM - 1) / kGemmBM;
+    }
+    offsets[E] = run;
+    mtile_off[E] = mrun;
+  }
+  __syncthreads();
+  if (active) {
+    int32_t base = off[e] + part[tid];
+    for (int t = ta; t < tb; ++t) {
+      tile_base[(size_t)t * E + e] = base;
+      base += tile_counts[(size_t)t * E + e];
+    }
+  }
+}
+
+// One warp per routed row (t, j): write perm / inv and copy x[t] to its row.
+__global__ void __launch_bounds__(256)
+route_scatter_kernel(const __nv_bfloat16* __restrict__ x, int T, int d, int E, int k,
+                     const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ rank,
+                     const int32_t* __restrict__ tile_base, int32_t* __restrict__ perm,
+                     int32_t* __restrict__ inv, __nv_bfloat16* __restrict__ x_perm,
+                     int32_t* __restrict__ status) {
+  const int64_t R = (int64_t)T * k;
+  const int64_t q = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (q >= R) return;
+  const int t = (int)(q / k);
+  const int e = topk_idx[q];
+  if (e < 0 || e >= E) {
+    if (lane == 0) atomicMax(status, kStatusBounds);
+    return;
+  }
+  const int64_t row = (int64_t)tile_base[(size_t)(t / kRouterTile) * E + e] + rank[q];
+  if (row < 0 || row >= R) {
+    if (lane == 0) atomicMax(status, kStatusBounds);
+    return;
+  }
+  if (lane == 0) {
+    if (perm) perm[row] = (int32_t)q;
+    if (inv) inv[q] = (int32_t)row;
+  }
+  if (x_perm) {
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * d);
+    uint4* dst = reinterpret_cast<uint4*>(x_perm + (size_t)row * d);
+    const int n16 = d / 8;
+    for (int i = lane; i < n16; i += 32) dst[i] = src[i];
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_route_scan(const int32_t* tile_counts, int ntiles, int E,
+                              int32_t* tile_base, int32_t* offsets, int32_t* mtile_off,
+                              cudaStream_t s) {
+  route_scan_kernel<<<1, kScanThreads, 0, s>>>(tile_counts, ntiles, E, tile_base, offsets,
+                                               mtile_off);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route_scatter(const __nv_bfloat16* x, int T, int d, int E, int k,
+                                 const int32_t* topk_idx, const int32_t* rank,
+                                 const int32_t* tile_base, int32_t* perm, int32_t* inv,
+                                 __nv_bfloat16* x_perm, int32_t* status, cudaStream_t s) {
+  const int64_t R = (int64_t)T * k;
+  const int warps_per_block = 8;
+  const int64_t grid = (R + warps_per_block - 1) / warps_per_block;
+  route_scatter_kernel<<<(unsigned)grid, warps_per_block * 32, 0, s>>>(
+      x, T, d, E, k, topk_idx, rank, tile_base, perm, inv, x_perm, status);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,102 @@
+"""Device-side buffers for one MoE layer, and a call of moe_forward on them.
+
+PyTorch provides the device memory and the stream; the arithmetic is all in
+libmoe_b300.so.  Used by the tests, the benchmark and the smoke entry point.
+"""
+from __future__ import annotations
+
+import dataclasses
+
+import numpy as np
+import torch
+
+from . import moe
+from .inputs import MoEInputs
+
+
+def _bf16(a: np.ndarray, device) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(device).view(torch.bfloat16)
+
+
+def _u8(a: np.ndarray, device) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+
+@dataclasses.dataclass
+class DeviceMoE:
+    """All arguments of moe_forward resident on one device."""
+
+    T: int
+    d: int
+    W: int
+    E: int
+    k: int
+    limit: float
+    alpha: float
+    x: torch.Tensor
+    router_w: torch.Tensor
+    router_b: torch.Tensor
+    w_gu: torch.Tensor
+    w_gu_scale: torch.Tensor
+    b_gu: torch.Tensor
+    w_dn: torch.Tensor
+    w_dn_scale: torch.Tensor
+    b_dn: torch.Tensor
+    out: torch.Tensor
+    workspace: torch.Tensor
+
+    @classmethod
+    def upload(cls, inp: MoEInputs, device="cuda") -> "DeviceMoE":
+        wl = inp.wl
+        ws_bytes = moe.moe_workspace_bytes(wl.T, wl.d, wl.W, wl.E, wl.k)
+        return cls(
+            T=wl.T, d=wl.d, W=wl.W, E=wl.E, k=wl.k, limit=inp.limit, alpha=inp.alpha,
+            x=_bf16(inp.x, device),
+            router_w=torch.from_numpy(inp.router_w).to(device),
+            router_b=torch.from_numpy(inp.router_b).to(device),
+            w_gu=_u8(inp.w_gu, device), w_gu_scale=_u8(inp.w_gu_scale, device),
+            b_gu=_bf16(inp.b_gu, device),
+            w_dn=_u8(inp.w_dn, device), w_dn_scale=_u8(inp.w_dn_scale, device),
+            b_dn=_bf16(inp.b_dn, device),
+            out=torch.empty((wl.T, wl.d), dtype=torch.bfloat16, device=device),
+            workspace=torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=device),
+        )
+
+    def forward(self, x=None, out=None, stream=None) -> torch.Tensor:
+        x = self.x if x is None else x
+        out = self.out if out is None else out
+        moe.moe_forward(x, self.T, self.d, self.W, self.router_w, self.router_b,
+                        self.w_gu, self.w_gu_scale, self.b_gu, self.w_dn, self.w_dn_scale,
+                        self.b_dn, self.E, self.k, self.limit, self.alpha, out,
+                        self.workspace, self.workspace.numel(), stream)
+        return out
+
+    def route(self, stream=None):
+        T, k, E = self.T, self.k, self.E
+        dev = self.x.device
+        idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+        w = torch.empty((T, k), dtype=torch.float32, device=dev)
+        off = torch.empty(E + 1, dtype=torch.int32, device=dev)
+        perm = torch.empty(T * k, dtype=torch.int32, device=dev)
+        inv = torch.empty((T, k), dtype=torch.int32, device=dev)
+        moe.moe_route(self.x, T, self.d, self.router_w, self.router_b, E, k, idx, w, off, perm,
+                      inv, self.workspace, self.workspace.numel(), stream)
+        return idx, w, off, perm, inv
+
+    def region(self, which: str) -> torch.Tensor:
+        """A view of an intermediate table inside the workspace (after forward)."""
+        off, nb = moe.moe_workspace_region(self.T, self.d, self.W, self.E, self.k, which)
+        raw = self.workspace[off:off + nb]
+        R = self.T * self.k
+        dtype, shape = {
+            "topk_idx": (torch.int32, (self.T, self.k)), "topk_w": (torch.float32, (self.T, self.k)),
+            "offsets": (torch.int32, (self.E + 1,)), "perm": (torch.int32, (R,)),
+            "inv": (torch.int32, (self.T, self.k)), "x_perm": (torch.bfloat16, (R, self.d)),
+            "h_hi": (torch.bfloat16, (R, self.W)), "h_lo": (torch.bfloat16, (R, self.W)),
+            "y": (torch.float32, (R, self.d)),
+        }[which]
+        return raw.view(dtype).view(shape)
+
+
+def bf16_to_f64(t: torch.Tensor) -> np.ndarray:
+    return t.float().cpu().numpy().astype(np.float64)

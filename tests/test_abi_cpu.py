@@ -1,0 +1,118 @@
+"""The C ABI on the host: the library loads, exports what include/moe.h declares,
+and rejects bad arguments before touching the GPU.  No kernel runs here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from sparse_moe_transformer_selected_b300 import build, moe
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return moe.load()
+
+
+def declared_functions():
+    src = open(HEADER, encoding="utf-8").read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_]+)\s*\(", src)))
+
+
+def test_header_declares_the_binding_names():
+    assert declared_functions() == sorted(moe.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    # exported with C linkage: the plain name resolves through dlsym
+    for name in declared_functions():
+        ctypes.CDLL(moe.LIB_PATH)[name]
+
+
+def test_workspace_bytes(lib):
+    assert moe.moe_workspace_bytes(0, 256, 256, 8, 4) == 0
+    n = moe.moe_workspace_bytes(64, 256, 256, 8, 4)
+    R = 256
+    assert n >= R * 256 * 2 + 2 * R * 256 * 2 + R * 256 * 4  # x_perm + h pair + y
+    assert moe.moe_workspace_bytes(64, 250, 256, 8, 4) == 0       # d % 32
+    assert moe.moe_workspace_bytes(64, 256, 250, 8, 4) == 0       # W % 32
+    assert moe.moe_workspace_bytes(64, 256, 256, 257, 4) == 0     # E > 256
+    assert moe.moe_workspace_bytes(64, 256, 256, 8, 9) == 0       # k > 8
+    assert moe.moe_workspace_bytes(64, 256, 256, 3, 4) == 0       # k > E
+    assert "k = 4" in moe.moe_last_error()
+
+
+def test_workspace_regions_disjoint_and_aligned(lib):
+    T, d, W, E, k = 77, 96, 160, 5, 3
+    total = moe.moe_workspace_bytes(T, d, W, E, k)
+    spans = []
+    for name in moe.REGIONS:
+        off, nb = moe.moe_workspace_region(T, d, W, E, k, name)
+        assert off % 256 == 0 and off >= 256 and off + nb <= total, name
+        spans.append((off, off + nb))
+    spans.sort()
+    for (a0, a1), (b0, b1) in zip(spans, spans[1:]):
+        assert a1 <= b0
+    with pytest.raises(moe.MoEError):
+        moe.moe_workspace_region(T, d, W, E, k, 99)
+
+
+def _forward(lib, T=64, d=256, W=256, E=8, k=4, ws_bytes=None, **ptrs):
+    good = dict(x=16, rw=16, rb=16, wgu=16, wgus=16, bgu=16, wdn=16, wdns=16, bdn=16,
+                out=16, ws=16)
+    good.update(ptrs)
+    if ws_bytes is None:
+        ws_bytes = max(1, moe.moe_workspace_bytes(T, d, W, E, k))
+    p = {k_: ctypes.c_void_p(v) for k_, v in good.items()}
+    return lib.moe_forward(p["x"], T, d, W, p["rw"], p["rb"], p["wgu"], p["wgus"], p["bgu"],
+                           p["wdn"], p["wdns"], p["bdn"], E, k, 7.0, 1.702, p["out"], p["ws"],
+                           ws_bytes, None)
+
+
+def test_argument_errors_return_before_any_launch(lib):
+    # every case below is rejected on the host; the fake addresses are never used
+    assert _forward(lib, d=100) == 2                              # MOE_ERR_SHAPE
+    assert _forward(lib, W=48) == 2
+    assert _forward(lib, E=0) == 2
+    assert _forward(lib, k=0) == 2
+    assert _forward(lib, T=-1) == 2
+    assert _forward(lib, x=0) == 1                                # MOE_ERR_NULL
+    assert "x is NULL" in moe.moe_last_error()
+    assert _forward(lib, ws=0) == 1
+    assert _forward(lib, wgu=24) == 3                             # MOE_ERR_ALIGN
+    assert "w_gu" in moe.moe_last_error()
+    assert _forward(lib, ws_bytes=1024) == 4                      # MOE_ERR_WORKSPACE
+    assert _forward(lib, T=0) == 0                                # nothing to do
+
+
+def test_nan_limit_rejected(lib):
+    p = [ctypes.c_void_p(16)] * 11
+    st = lib.moe_forward(p[0], 64, 256, 256, p[1], p[2], p[3], p[4], p[5], p[6], p[7], p[8],
+                         8, 4, float("nan"), 1.0, p[9], p[10], 1 << 30, None)
+    assert st == 2
+
+
+def test_route_argument_errors(lib):
+    v = ctypes.c_void_p
+    assert lib.moe_route(v(16), 64, 100, v(16), v(16), 8, 4, None, None, None, None, None,
+                         v(16), 1 << 20, None) == 2
+    assert lib.moe_route(None, 64, 256, v(16), v(16), 8, 4, None, None, None, None, None,
+                         v(16), 1 << 20, None) == 1
+    assert lib.moe_route(v(16), 64, 256, v(16), v(16), 8, 4, v(20), None, None, None, None,
+                         v(16), 1 << 20, None) == 3
+    assert lib.moe_route(v(16), 0, 256, v(16), v(16), 8, 4, None, None, None, None, None,
+                         v(16), 0, None) == 0
+
+
+def test_binding_raises_on_error(lib):
+    with pytest.raises(moe.MoEError) as ei:
+        moe.moe_forward(0, 64, 256, 256, 16, 16, 16, 16, 16, 16, 16, 16, 8, 4, 7.0, 1.702,
+                        16, 16, 1 << 30, stream=0)
+    assert ei.value.status == 1
