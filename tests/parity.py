@@ -22,13 +22,22 @@ W_ABS = 2e-5
 
 
 def check_routing(ref, idx_gpu: np.ndarray, w_gpu: np.ndarray, k: int):
-    """Compare top-k indices and weights.  Returns the tokens whose selection
-    legitimately differs (flagged near-ties with another valid choice)."""
+    """Compare top-k selections and weights.
+
+    The selected SET is what is unique: it must equal the oracle's, except for
+    a token whose k-th and (k+1)-th exact logits are within GAP (a flagged
+    near-tie), where any valid top-k within that margin is accepted.  The slot
+    ORDER is only unique up to near-equal logits, so it is checked for being
+    non-increasing in the exact logits (within GAP).  Weights are compared per
+    expert.  Returns the tokens whose selection legitimately differs.
+    """
     idx_ref = ref["topk_idx"]
     logits = ref["logits"]
     T = idx_ref.shape[0]
     assert idx_gpu.shape == idx_ref.shape
-    differ = np.nonzero(np.any(idx_gpu != idx_ref, axis=1))[0]
+    set_gpu = np.sort(idx_gpu, axis=1)
+    set_ref = np.sort(idx_ref, axis=1)
+    differ = np.nonzero(np.any(set_gpu != set_ref, axis=1))[0]
     excused = []
     for t in differ:
         assert ref["gap"][t] < GAP, (
@@ -39,9 +48,17 @@ def check_routing(ref, idx_gpu: np.ndarray, w_gpu: np.ndarray, k: int):
         kth = np.sort(logits[t])[::-1][k - 1]
         assert np.all(logits[t, sel] >= kth - GAP), f"token {t}: invalid near-tie choice"
         excused.append(int(t))
+    # slot order: non-increasing exact logits, up to near-ties
+    lg = np.take_along_axis(logits, idx_gpu.astype(np.int64), axis=1)
+    bad = np.nonzero(np.any(lg[:, 1:] > lg[:, :-1] + GAP, axis=1))[0]
+    assert bad.size == 0, f"token {bad[0]}: slots not in descending logit order {idx_gpu[bad[0]]}"
     same = np.setdiff1d(np.arange(T), differ)
     if same.size:
-        err = np.abs(w_gpu[same] - ref["topk_w"][same])
+        og = np.argsort(idx_gpu[same], axis=1)
+        orf = np.argsort(idx_ref[same], axis=1)
+        wg = np.take_along_axis(w_gpu[same], og, axis=1)
+        wr = np.take_along_axis(ref["topk_w"][same], orf, axis=1)
+        err = np.abs(wg - wr)
         assert err.max() <= W_ABS, f"routing weight error {err.max():.3g} > {W_ABS}"
     return excused
 
