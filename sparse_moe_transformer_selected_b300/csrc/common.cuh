@@ -30,7 +30,9 @@ struct Workspace {
   size_t mtile_off;    // int32[E+1]   prefix of ceil(count/kGemmBM)
   size_t perm;         // int32[R]
   size_t inv;          // int32[R]
-  size_t x_perm;       // bf16[R, d]
+  size_t xexp;         // int32[T]   per-token exponent e_t of the f16 scaling
+  size_t rowexp;       // int32[R]   e_t of the token of each permuted row
+  size_t x_perm;       // f16[R, d]  x[t] * 2^e_t
   size_t h_hi;         // bf16[R, W]
   size_t h_lo;         // bf16[R, W]
   size_t y;            // float[R, d]
@@ -59,6 +61,8 @@ inline Workspace workspace_layout(int64_t T, int d, int W, int E, int k) {
   ws.mtile_off = take(size_t(E + 1) * 4);
   ws.perm = take(size_t(R) * 4);
   ws.inv = take(size_t(R) * 4);
+  ws.xexp = take(size_t(T) * 4);
+  ws.rowexp = take(size_t(R) * 4);
   ws.x_perm = take(size_t(R) * d * 2);
   ws.h_hi = take(size_t(R) * W * 2);
   ws.h_lo = take(size_t(R) * W * 2);
@@ -70,29 +74,34 @@ inline Workspace workspace_layout(int64_t T, int d, int W, int E, int k) {
 // ---------------------------------------------------------------- kernels --
 // Host-side launchers, one per stage.  All return the launch's cudaError_t.
 
-// K1: logits, top-k, selected softmax, per-tile histogram and in-tile ranks.
-// Also clears the status word (the first kernel of every call).
+// K1: logits, top-k, selected softmax, per-tile histogram and in-tile ranks,
+// and the per-token exponent e_t = 14 - floor(log2 max|x_t|) used to hold x in
+// f16 exactly.  Also clears the status word (the first kernel of every call).
 cudaError_t launch_router_topk(const __nv_bfloat16* x, const float* router_w,
                                const float* router_b, int T, int d, int E, int k,
                                int32_t* topk_idx, float* topk_w, int32_t* rank,
-                               int32_t* tile_counts, int32_t* status, cudaStream_t s);
+                               int32_t* tile_counts, int32_t* xexp, int32_t* status,
+                               cudaStream_t s);
 
 // K2a: expert offsets, per-(tile, expert) bases, row-tile prefix.
 cudaError_t launch_route_scan(const int32_t* tile_counts, int ntiles, int E,
                               int32_t* tile_base, int32_t* offsets, int32_t* mtile_off,
                               cudaStream_t s);
 
-// K2b: perm / inv tables and (optionally) the gathered activations.
+// K2b: perm / inv tables and (optionally) the gathered activations in f16,
+// x_perm[row] = x[t] * 2^e_t, rowexp[row] = e_t.
 cudaError_t launch_route_scatter(const __nv_bfloat16* x, int T, int d, int E, int k,
                                  const int32_t* topk_idx, const int32_t* rank,
-                                 const int32_t* tile_base, int32_t* perm, int32_t* inv,
-                                 __nv_bfloat16* x_perm, int32_t* status, cudaStream_t s);
+                                 const int32_t* tile_base, const int32_t* xexp, int32_t* perm,
+                                 int32_t* inv, void* x_perm, int32_t* rowexp, int32_t* status,
+                                 cudaStream_t s);
 
 struct GemmArgs {
   int R, d, W, E;
   const int32_t* offsets;     // [E+1]
   const int32_t* mtile_off;   // [E+1]
-  const __nv_bfloat16* x_perm;
+  const void* x_perm;         // f16 [R, d], each row scaled by 2^rowexp[row]
+  const int32_t* rowexp;      // [R]
   const uint8_t* w_gu; const uint8_t* w_gu_scale; const __nv_bfloat16* b_gu;
   const uint8_t* w_dn; const uint8_t* w_dn_scale; const __nv_bfloat16* b_dn;
   float limit, alpha;

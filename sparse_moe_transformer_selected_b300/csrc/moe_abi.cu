@@ -85,7 +85,9 @@ struct RouteOut {
   int32_t* mtile_off;
   int32_t* perm;
   int32_t* inv;
-  __nv_bfloat16* x_perm;
+  int32_t* xexp;
+  int32_t* rowexp;
+  void* x_perm;
   int32_t* status;
 };
 
@@ -100,7 +102,9 @@ RouteOut route_tables(void* ws, const moe::Workspace& L, bool gather) {
   r.mtile_off = at<int32_t>(ws, L.mtile_off);
   r.perm = at<int32_t>(ws, L.perm);
   r.inv = at<int32_t>(ws, L.inv);
-  r.x_perm = gather ? at<__nv_bfloat16>(ws, L.x_perm) : nullptr;
+  r.xexp = at<int32_t>(ws, L.xexp);
+  r.rowexp = at<int32_t>(ws, L.rowexp);
+  r.x_perm = gather ? at<void>(ws, L.x_perm) : nullptr;
   r.status = at<int32_t>(ws, L.status);
   return r;
 }
@@ -110,14 +114,14 @@ moe_status run_route(const void* x, int64_t T, int d, const float* rw, const flo
   const auto* xb = static_cast<const __nv_bfloat16*>(x);
   const int ntiles = int((T + moe::kRouterTile - 1) / moe::kRouterTile);
   cudaError_t e = moe::launch_router_topk(xb, rw, rb, int(T), d, E, k, r.topk_idx, r.topk_w,
-                                          r.rank, r.tile_counts, r.status, s);
+                                          r.rank, r.tile_counts, r.xexp, r.status, s);
   if (e != cudaSuccess) return cuda_fail(e, "router_topk launch");
   if ((e = trace(1, s)) != cudaSuccess) return cuda_fail(e, "trace event");
   e = moe::launch_route_scan(r.tile_counts, ntiles, E, r.tile_base, r.offsets, r.mtile_off, s);
   if (e != cudaSuccess) return cuda_fail(e, "route_scan launch");
   if ((e = trace(2, s)) != cudaSuccess) return cuda_fail(e, "trace event");
-  e = moe::launch_route_scatter(xb, int(T), d, E, k, r.topk_idx, r.rank, r.tile_base, r.perm,
-                                r.inv, r.x_perm, r.status, s);
+  e = moe::launch_route_scatter(xb, int(T), d, E, k, r.topk_idx, r.rank, r.tile_base, r.xexp,
+                                r.perm, r.inv, r.x_perm, r.rowexp, r.status, s);
   if (e != cudaSuccess) return cuda_fail(e, "route_scatter launch");
   if ((e = trace(3, s)) != cudaSuccess) return cuda_fail(e, "trace event");
   return MOE_OK;
@@ -193,6 +197,7 @@ moe_status moe_forward(const void* x_bf16, int64_t T, int d, int W, const float*
   a.offsets = r.offsets;
   a.mtile_off = r.mtile_off;
   a.x_perm = r.x_perm;
+  a.rowexp = r.rowexp;
   a.w_gu = w_gu_fp4;
   a.w_gu_scale = w_gu_scale;
   a.b_gu = static_cast<const __nv_bfloat16*>(b_gu_bf16);

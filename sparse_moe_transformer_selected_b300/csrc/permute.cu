@@ -9,6 +9,8 @@
 // deterministic without atomics.
 #include "common.cuh"
 
+#include <cuda_fp16.h>
+
 namespace moe {
 namespace {
 
@@ -66,12 +68,15 @@ route_scan_kernel(const int32_t* __restrict__ tile_counts, int ntiles, int E,
   }
 }
 
-// One warp per routed row (t, j): write perm / inv and copy x[t] to its row.
+// One warp per routed row (t, j): write perm / inv and copy x[t] to its row,
+// converted to f16 after an exact power-of-two scaling by 2^e_t (e_t puts the
+// token's largest |x| in [2^14, 2^15), so every bf16 value is held exactly).
 __global__ void __launch_bounds__(256)
 route_scatter_kernel(const __nv_bfloat16* __restrict__ x, int T, int d, int E, int k,
                      const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ rank,
-                     const int32_t* __restrict__ tile_base, int32_t* __restrict__ perm,
-                     int32_t* __restrict__ inv, __nv_bfloat16* __restrict__ x_perm,
+                     const int32_t* __restrict__ tile_base, const int32_t* __restrict__ xexp,
+                     int32_t* __restrict__ perm, int32_t* __restrict__ inv,
+                     __half* __restrict__ x_perm, int32_t* __restrict__ rowexp,
                      int32_t* __restrict__ status) {
   const int64_t R = (int64_t)T * k;
   const int64_t q = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -93,10 +98,25 @@ route_scatter_kernel(const __nv_bfloat16* __restrict__ x, int T, int d, int E, i
     if (inv) inv[q] = (int32_t)row;
   }
   if (x_perm) {
+    const int et = xexp[t];
+    if (lane == 0) rowexp[row] = et;
+    const float f = __int_as_float((et + 127) << 23);   // 2^e_t, |e_t| <= 126
     const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * d);
     uint4* dst = reinterpret_cast<uint4*>(x_perm + (size_t)row * d);
     const int n16 = d / 8;
-    for (int i = lane; i < n16; i += 32) dst[i] = src[i];
+    for (int i = lane; i < n16; i += 32) {
+      const uint4 v = src[i];
+      const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const float lo = __uint_as_float(in[c] << 16) * f;
+        const float hi = __uint_as_float(in[c] & 0xFFFF0000u) * f;
+        const __half2 h = __floats2half2_rn(lo, hi);
+        o[c] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+      dst[i] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
   }
 }
 
@@ -112,13 +132,15 @@ cudaError_t launch_route_scan(const int32_t* tile_counts, int ntiles, int E,
 
 cudaError_t launch_route_scatter(const __nv_bfloat16* x, int T, int d, int E, int k,
                                  const int32_t* topk_idx, const int32_t* rank,
-                                 const int32_t* tile_base, int32_t* perm, int32_t* inv,
-                                 __nv_bfloat16* x_perm, int32_t* status, cudaStream_t s) {
+                                 const int32_t* tile_base, const int32_t* xexp, int32_t* perm,
+                                 int32_t* inv, void* x_perm, int32_t* rowexp, int32_t* status,
+                                 cudaStream_t s) {
   const int64_t R = (int64_t)T * k;
   const int warps_per_block = 8;
   const int64_t grid = (R + warps_per_block - 1) / warps_per_block;
   route_scatter_kernel<<<(unsigned)grid, warps_per_block * 32, 0, s>>>(
-      x, T, d, E, k, topk_idx, rank, tile_base, perm, inv, x_perm, status);
+      x, T, d, E, k, topk_idx, rank, tile_base, xexp, perm, inv,
+      static_cast<__half*>(x_perm), rowexp, status);
   return cudaGetLastError();
 }
 

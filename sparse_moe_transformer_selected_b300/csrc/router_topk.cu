@@ -29,7 +29,7 @@ router_topk_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict_
                    const float* __restrict__ rb, int T, int d, int E, int k,
                    int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
                    int32_t* __restrict__ rank, int32_t* __restrict__ tile_counts,
-                   int32_t* __restrict__ status) {
+                   int32_t* __restrict__ xexp, int32_t* __restrict__ status) {
   __shared__ float xs[kTT][kKC + 1];
   __shared__ float wl[kKC * kLgStride];  // W chunk [k][e]; later logits [t][e]
   __shared__ uint32_t mask[kMaxE];       // bit t: token t of this tile picked e
@@ -40,6 +40,7 @@ router_topk_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict_
   if (blockIdx.x == 0 && tid == 0) status[0] = 0;
   for (int e = tid; e < kMaxE; e += kThreads) mask[e] = 0u;
 
+  float xmax = 0.f;   // max |x| over this thread's share of token (tid >> 3)
   float acc[4][NPER];
 #pragma unroll
   for (int i = 0; i < 4; ++i)
@@ -56,6 +57,7 @@ router_topk_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict_
         const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
         v[0] = __low2float(a); v[1] = __high2float(a);
         v[2] = __low2float(b); v[3] = __high2float(b);
+        xmax = fmaxf(xmax, fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3]))));
       }
 #pragma unroll
       for (int c = 0; c < 4; ++c) xs[tl][kq + c] = v[c];
@@ -82,6 +84,15 @@ router_topk_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict_
       }
     }
     __syncthreads();
+  }
+
+  // per-token exponent for holding x in f16: largest |x| scaled into [2^14, 2^15)
+  xmax = fmaxf(xmax, __shfl_xor_sync(0xffffffffu, xmax, 1));
+  xmax = fmaxf(xmax, __shfl_xor_sync(0xffffffffu, xmax, 2));
+  xmax = fmaxf(xmax, __shfl_xor_sync(0xffffffffu, xmax, 4));
+  if ((tid & 7) == 0 && t0 + (tid >> 3) < T) {
+    const int et = (xmax > 0.f && isfinite(xmax)) ? 14 - ilogbf(xmax) : 0;
+    xexp[t0 + (tid >> 3)] = max(-126, min(126, et));
   }
 
   // logits (+ bias) into shared memory, row per token
@@ -167,14 +178,15 @@ router_topk_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict_
 cudaError_t launch_router_topk(const __nv_bfloat16* x, const float* router_w,
                                const float* router_b, int T, int d, int E, int k,
                                int32_t* topk_idx, float* topk_w, int32_t* rank,
-                               int32_t* tile_counts, int32_t* status, cudaStream_t s) {
+                               int32_t* tile_counts, int32_t* xexp, int32_t* status,
+                               cudaStream_t s) {
   const int grid = (T + kTT - 1) / kTT;
   const int nper = (E + 31) / 32;
 #define MOE_ROUTER_CASE(N)                                                          \
   case N:                                                                           \
     router_topk_kernel<N><<<grid, kThreads, 0, s>>>(x, router_w, router_b, T, d, E, \
                                                     k, topk_idx, topk_w, rank,      \
-                                                    tile_counts, status);           \
+                                                    tile_counts, xexp, status);     \
     break;
   switch (nper) {
     MOE_ROUTER_CASE(1)
