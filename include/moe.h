@@ -165,6 +165,42 @@ moe_status moe_workspace_region(int64_t T, int d, int W, int E, int k, int which
  */
 moe_status moe_set_trace_events(void* const* events, int n);
 
+/*
+ * Size of the scratch array built into the library for moe_forward_noalloc:
+ * 16 MiB, enough for about 128 tokens at d = W = 2880 with k = 4.
+ */
+#define MOE_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+
+/*
+ * moe_forward without a workspace argument, for callers that cannot allocate
+ * device memory while they run the block (an engine plugin whose host forbids
+ * allocation while serving, a real-time loop with a no-allocation rule, code
+ * that is handed only its input and output buffers).  It computes exactly
+ * what moe_forward computes, through the same kernels; the scratch is a
+ * device array of MOE_NOALLOC_SCRATCH_BYTES inside the library, which every
+ * GPU that loads the library keeps until the process exits.  This is a
+ * convenience of this library; the pages the block follows have no
+ * counterpart.
+ *   - Arguments, layouts and results are those of moe_forward.
+ *   - Shapes whose moe_workspace_bytes() exceeds MOE_NOALLOC_SCRATCH_BYTES are
+ *     rejected with MOE_ERR_WORKSPACE and a message from moe_last_error();
+ *     nothing is enqueued.
+ *   - No cudaMalloc, cudaFree or other allocation happens.  The first call on
+ *     a device looks up the array's device address (cudaGetSymbolAddress) with
+ *     that device current; make that first call before any stream capture.
+ *   - All calls share the one array and it keeps the last call's contents.
+ *     Every call rewrites all of it that it reads, so nothing needs clearing,
+ *     but calls that overlap on the GPU (two streams, two threads) race on it:
+ *     issue them one after another.  moe_poll_status cannot read this array's
+ *     status word; errors from argument checks are returned as usual.
+ */
+moe_status moe_forward_noalloc(const void* x_bf16, int64_t T, int d, int W,
+                               const float* router_w, const float* router_b,
+                               const uint8_t* w_gu_fp4, const uint8_t* w_gu_scale,
+                               const void* b_gu_bf16, const uint8_t* w_dn_fp4,
+                               const uint8_t* w_dn_scale, const void* b_dn_bf16, int E, int k,
+                               float limit, float alpha, void* out_bf16, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -129,6 +129,11 @@ moe_status run_route(const void* x, int64_t T, int d, const float* rw, const flo
 
 }  // namespace
 
+namespace moe {
+// Lets other translation units of the library report through moe_last_error().
+void set_last_error(const std::string& msg) { g_last_error = msg; }
+}  // namespace moe
+
 extern "C" {
 
 size_t moe_workspace_bytes(int64_t T, int d, int W, int E, int k) {

@@ -25,7 +25,11 @@ REGIONS = {"topk_idx": 0, "topk_w": 1, "offsets": 2, "perm": 3, "inv": 4,
 
 # Every symbol include/moe.h declares.
 EXPORTS = ("moe_workspace_bytes", "moe_forward", "moe_route", "moe_poll_status",
-           "moe_last_error", "moe_workspace_region", "moe_set_trace_events")
+           "moe_last_error", "moe_workspace_region", "moe_set_trace_events",
+           "moe_forward_noalloc")
+
+# Scratch built into the library for moe_forward_noalloc (MOE_NOALLOC_SCRATCH_BYTES).
+NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
 class MoEError(RuntimeError):
@@ -64,6 +68,9 @@ def load() -> ctypes.CDLL:
     lib.moe_workspace_region.restype = I32
     lib.moe_set_trace_events.argtypes = [ctypes.POINTER(P), I32]
     lib.moe_set_trace_events.restype = I32
+    lib.moe_forward_noalloc.argtypes = [P, I64, I32, I32, P, P, P, P, P, P, P, P, I32, I32, F32,
+                                        F32, P, P]
+    lib.moe_forward_noalloc.restype = I32
     _lib = lib
     return lib
 
@@ -133,3 +140,14 @@ def moe_set_trace_events(events) -> int:
     handles = [e if isinstance(e, int) else e.cuda_event for e in events]
     arr = (ctypes.c_void_p * len(handles))(*handles)
     return _check(load().moe_set_trace_events(arr, len(handles)))
+
+
+def moe_forward_noalloc(x_bf16, T, d, W, router_w, router_b, w_gu_fp4, w_gu_scale, b_gu_bf16,
+                        w_dn_fp4, w_dn_scale, b_dn_bf16, E, k, limit, alpha, out_bf16,
+                        stream=None) -> int:
+    """moe_forward with the library's built-in scratch instead of a workspace,
+    for callers that cannot allocate device memory; see include/moe.h."""
+    return _check(load().moe_forward_noalloc(
+        _ptr(x_bf16), T, d, W, _ptr(router_w), _ptr(router_b), _ptr(w_gu_fp4),
+        _ptr(w_gu_scale), _ptr(b_gu_bf16), _ptr(w_dn_fp4), _ptr(w_dn_scale), _ptr(b_dn_bf16),
+        E, k, limit, alpha, _ptr(out_bf16), _stream(stream)))
