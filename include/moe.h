@@ -145,8 +145,10 @@ const char* moe_last_error(void);
  * tests: writes its byte offset and size.  Contents are valid after a
  * moe_forward (or, for the routing tables, moe_route) on that workspace.
  *   which: 0 topk_idx int32[T,k]   1 topk_w fp32[T,k]     2 offsets int32[E+1]
- *          3 perm int32[T·k]       4 inv int32[T,k]       5 x_perm bf16[T·k,d]
+ *          3 perm int32[T·k]       4 inv int32[T,k]       5 x_perm f16[T·k,d]
  *          6 h_hi bf16[T·k,W]      7 h_lo bf16[T·k,W]     8 y fp32[T·k,d]
+ * x_perm holds each routed row's token scaled by 2^e_t (e_t puts the token's
+ * largest |x| in [2^14, 2^15), so the f16 value is exact).
  * Returns MOE_ERR_SHAPE for an invalid shape or `which`.
  */
 moe_status moe_workspace_region(int64_t T, int d, int W, int E, int k, int which,

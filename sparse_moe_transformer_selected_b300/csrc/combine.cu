@@ -14,15 +14,22 @@ constexpr int kThreads = 128;
 
 __global__ void __launch_bounds__(kThreads)
 combine_kernel(const float* __restrict__ y, const float* __restrict__ topk_w,
-               const int32_t* __restrict__ inv, int d, int k,
-               __nv_bfloat16* __restrict__ out) {
+               const int32_t* __restrict__ inv, int d, int k, int R,
+               __nv_bfloat16* __restrict__ out, int32_t* __restrict__ status) {
   const int t = blockIdx.x;
   int32_t rows[8];
   float w[8];
+  bool bad = false;
   for (int j = 0; j < k; ++j) {
     rows[j] = inv[(size_t)t * k + j];
     w[j] = topk_w[(size_t)t * k + j];
+    if (rows[j] < 0 || rows[j] >= R) {   // a row the permutation never wrote
+      bad = true;
+      rows[j] = 0;
+      w[j] = 0.f;
+    }
   }
+  if (bad && threadIdx.x == 0) atomicMax(status, kStatusBounds);
   const int n4 = d / 4;
   for (int i = threadIdx.x; i < n4; i += kThreads) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -45,8 +52,8 @@ combine_kernel(const float* __restrict__ y, const float* __restrict__ topk_w,
 }  // namespace
 
 cudaError_t launch_combine(const float* y, const float* topk_w, const int32_t* inv, int T,
-                           int d, int k, __nv_bfloat16* out, cudaStream_t s) {
-  combine_kernel<<<T, kThreads, 0, s>>>(y, topk_w, inv, d, k, out);
+                           int d, int k, __nv_bfloat16* out, int32_t* status, cudaStream_t s) {
+  combine_kernel<<<T, kThreads, 0, s>>>(y, topk_w, inv, d, k, T * k, out, status);
   return cudaGetLastError();
 }
 

@@ -115,8 +115,10 @@ cudaError_t launch_gateup(const GemmArgs& a, cudaStream_t s);
 // K4: y = (h_hi + h_lo) · W_dn^T + b_dn, per expert segment.
 cudaError_t launch_down(const GemmArgs& a, cudaStream_t s);
 
-// K5: out[t] = bf16(Σ_j w[t,j] · y[inv[t,j]]).
+// K5: out[t] = bf16(Σ_j w[t,j] · y[inv[t,j]]); a row index outside [0, T·k)
+// is skipped and recorded in the status word.
 cudaError_t launch_combine(const float* y, const float* topk_w, const int32_t* inv,
-                           int T, int d, int k, __nv_bfloat16* out, cudaStream_t s);
+                           int T, int d, int k, __nv_bfloat16* out, int32_t* status,
+                           cudaStream_t s);
 
 }  // namespace moe

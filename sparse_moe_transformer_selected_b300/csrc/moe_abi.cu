@@ -222,7 +222,7 @@ moe_status moe_forward(const void* x_bf16, int64_t T, int d, int W, const float*
   if (e != cudaSuccess) return cuda_fail(e, "down launch");
   if ((e = trace(5, s)) != cudaSuccess) return cuda_fail(e, "trace event");
   e = moe::launch_combine(a.y, r.topk_w, r.inv, int(T), d, k,
-                          static_cast<__nv_bfloat16*>(out_bf16), s);
+                          static_cast<__nv_bfloat16*>(out_bf16), r.status, s);
   if (e != cudaSuccess) return cuda_fail(e, "combine launch");
   if ((e = trace(6, s)) != cudaSuccess) return cuda_fail(e, "trace event");
   return MOE_OK;

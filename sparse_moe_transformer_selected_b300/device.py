@@ -91,7 +91,7 @@ class DeviceMoE:
         dtype, shape = {
             "topk_idx": (torch.int32, (self.T, self.k)), "topk_w": (torch.float32, (self.T, self.k)),
             "offsets": (torch.int32, (self.E + 1,)), "perm": (torch.int32, (R,)),
-            "inv": (torch.int32, (self.T, self.k)), "x_perm": (torch.bfloat16, (R, self.d)),
+            "inv": (torch.int32, (self.T, self.k)), "x_perm": (torch.float16, (R, self.d)),
             "h_hi": (torch.bfloat16, (R, self.W)), "h_lo": (torch.bfloat16, (R, self.W)),
             "y": (torch.float32, (R, self.d)),
         }[which]
