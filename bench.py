@@ -7,7 +7,7 @@ A step is one moe_forward over one batch of T synthetic tokens: router, top-4,
 selected softmax, permutation, grouped gate_up GEMM with clamped SwiGLU, grouped
 down GEMM, weighted combine.  The default workload is the gpt-oss-20b MoE layer
 at decode (T = 32, d = W = 2880, E = 32, top-4).  Inputs are resident in HBM
-when the timed region starts; L2 is flushed (a 256 MB write) before every timed
+when the timed region starts; L2 is flushed (a 256 MB write, then a 256 MB read) before every timed
 step.  Prints ONE JSON line (rank 0).
 
 Under torchrun (N > 1) every rank runs an independent replica of the layer on
@@ -37,6 +37,9 @@ from sparse_moe_transformer_selected_b300 import inputs as gen  # noqa: E402
 
 METRIC = "MoE-layer tokens/s at 20b/120b shapes; % of HBM or tensor-pipe roofline"
 STAGES = ["router_topk", "route_scan", "route_scatter", "gate_up", "down", "combine"]
+# kernels one moe_forward launches: router logits, router top-k, scan, scatter,
+# gate_up, down, combine
+KERNELS_PER_STEP = 7
 KERNEL_SOURCES = {
     "router_topk": "router_topk.cu", "route_scan": "permute.cu", "route_scatter": "permute.cu",
     "gate_up": "grouped_gemm_tc.cu", "down": "grouped_gemm_tc.cu", "combine": "combine.cu",
@@ -224,7 +227,7 @@ def config_block(wl, world):
     return {"workload": wl.name, "T": wl.T, "d_model": wl.d, "expert_width": wl.W,
             "experts": wl.E, "top_k": wl.k, "weights": "MXFP4 (E2M1 x 32 + E8M0)",
             "router_bias": wl.router_bias,
-            "l2": "flushed before every timed step (256 MB write)",
+            "l2": "flushed before every timed step (256 MB write, then 256 MB read)",
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
 
 
@@ -248,20 +251,25 @@ def run_ours(args, wl):
     dev = DeviceMoE.upload(inp)
     stream = torch.cuda.current_stream()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    drain = torch.ones(64 << 20, dtype=torch.float32, device="cuda")   # 256 MB
 
     def flush_l2():
+        # write a buffer twice the size of L2, then read another one: the read
+        # evicts the dirty lines of the write, so their write-back to HBM does
+        # not run inside the next timed step
         flush.fill_(1)
+        drain.sum()
 
     for _ in range(args.warmup):
         dev.forward()
     torch.cuda.synchronize()
     counts = np.diff(dev.region("offsets").cpu().numpy())
 
-    # device-timed steps, each preceded by an L2 flush; stage events per step
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(args.steps)]
-    for row in ev:                                  # materialise the event handles
-        for e in row:
-            e.record(stream)
+    # device-timed steps, each preceded by an L2 flush; one event pair around
+    # each moe_forward (nothing recorded between its kernels, so consecutive
+    # kernels overlap their launches as they do for a user)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
@@ -269,16 +277,30 @@ def run_ours(args, wl):
     with ClockSampler(local_rank) as clk:
         for s in range(args.steps):
             flush_l2()
-            moe.moe_set_trace_events(ev[s])
+            ev[s][0].record(stream)
             dev.forward()
-        moe.moe_set_trace_events(None)
+            ev[s][1].record(stream)
         torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    step_ms = [r[0].elapsed_time(r[6]) for r in ev]
-    stage_ms = {name: [r[i].elapsed_time(r[i + 1]) for r in ev] for i, name in enumerate(STAGES)}
+    step_ms = [a_.elapsed_time(b_) for a_, b_ in ev]
     ms = statistics.fmean(step_ms)
+
+    # per-stage breakdown, in separate (untimed-for-the-result) steps with CUDA
+    # events recorded by the library between its stages
+    tev = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(args.steps)]
+    for row in tev:                                 # materialise the event handles
+        for e in row:
+            e.record(stream)
+    torch.cuda.synchronize()
+    for s in range(args.steps):
+        flush_l2()
+        moe.moe_set_trace_events(tev[s])
+        dev.forward()
+    moe.moe_set_trace_events(None)
+    torch.cuda.synchronize()
+    stage_ms = {name: [r[i].elapsed_time(r[i + 1]) for r in tev] for i, name in enumerate(STAGES)}
 
     # end to end through the public call: pinned host x in, pinned host out back
     x_host = dev.x.cpu().pin_memory()
@@ -344,7 +366,7 @@ def run_ours(args, wl):
         "e2e": {"value": tokens / (e2e * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(dev.x.numel() * 2),
                 "d2h_bytes_per_step": int(dev.out.numel() * 2)},
-        "gpu_launches": len(STAGES) * args.steps,
+        "gpu_launches": KERNELS_PER_STEP * args.steps,
         "roofline": roof,
         "stages_ms": {k_: round(v, 5) for k_, v in mean_stage.items()},
         "active_experts": work["_active"],

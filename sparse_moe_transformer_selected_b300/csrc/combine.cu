@@ -17,6 +17,7 @@ combine_kernel(const float* __restrict__ y, const float* __restrict__ topk_w,
                const int32_t* __restrict__ inv, int d, int k, int R,
                __nv_bfloat16* __restrict__ out, int32_t* __restrict__ status) {
   const int t = blockIdx.x;
+  pdl_wait();
   int32_t rows[8];
   float w[8];
   bool bad = false;
@@ -53,8 +54,8 @@ combine_kernel(const float* __restrict__ y, const float* __restrict__ topk_w,
 
 cudaError_t launch_combine(const float* y, const float* topk_w, const int32_t* inv, int T,
                            int d, int k, __nv_bfloat16* out, int32_t* status, cudaStream_t s) {
-  combine_kernel<<<T, kThreads, 0, s>>>(y, topk_w, inv, d, k, T * k, out, status);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel, dim3(T), dim3(kThreads), 0, s, y, topk_w, inv, d, k, T * k,
+                    out, status);
 }
 
 }  // namespace moe

@@ -7,12 +7,65 @@
 
 namespace moe {
 
+// Programmatic dependent launch.  Every kernel of the block is launched with
+// the programmatic-serialization attribute, so its launch and prologue overlap
+// the previous kernel's tail; each kernel calls pdl_wait() before its first
+// global-memory access (it returns once the previous kernel has completed and
+// its writes are visible).  Only kernels whose CTAs are all resident at once
+// (the persistent GEMMs) call pdl_trigger(), and only after their own
+// pdl_wait(); the others let the dependent launch when they exit.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Router tile: tokens per CTA of the router kernel.  Also the granularity of
 // the per-tile expert histogram the permutation is built from.
 constexpr int kRouterTile = 32;
-// Row tile of the grouped GEMMs (tcgen05 M).  An expert's segment of the
-// permuted rows is cut into ceil(count / kGemmBM) row tiles.
+// Largest token chunk of the grouped GEMMs.  An expert's segment of the
+// permuted rows is cut into ceil(count / chunk) chunks, chunk <= kGemmBM (the
+// shared-memory-staged design always uses kGemmBM: its MMA M side).
 constexpr int kGemmBM = 128;
+
+// Router work split.  A CTA of the logits kernel takes 32 tokens x a group of
+// experts x a range of d.  A decode-sized batch has one or two 32-token tiles,
+// so it uses groups of 32 experts and cuts d into ranges (at least 256 long,
+// multiples of 32) to give the GPU a few dozen CTAs; the partial sums are added
+// in a fixed order.  A prefill batch takes all experts per CTA (more reuse of
+// each loaded x value) and few or no d ranges.
+inline int router_expert_group(int64_t T, int E) {
+  return (T <= 256 || E <= 32) ? 32 : (E + 31) / 32 * 32;
+}
+inline int router_split_len(int64_t T, int d, int E) {
+  const int64_t ntiles = (T + kRouterTile - 1) / kRouterTile;
+  const int64_t groups = (E + router_expert_group(T, E) - 1) / router_expert_group(T, E);
+  int64_t want = (4 * 148 + ntiles * groups - 1) / (ntiles * groups);
+  if (want < 1) want = 1;
+  int64_t len = (d + want - 1) / want;
+  len = (len + 31) / 32 * 32;
+  if (len < 256) len = 256;
+  return int(len < d ? len : (d + 31) / 32 * 32);
+}
+inline int router_splits(int64_t T, int d, int E) {
+  const int len = router_split_len(T, d, E);
+  return (d + len - 1) / len;
+}
 
 // Device status word codes (values equal the public moe_status codes).
 constexpr int kStatusTimeout = 7;
@@ -23,14 +76,14 @@ struct Workspace {
   size_t status;       // int32[64]
   size_t topk_idx;     // int32[T*k]
   size_t topk_w;       // float[T*k]
+  size_t logit_part;   // float[nks*T*E] router partial sums, one slab per K range
   size_t rank;         // int32[T*k]   rank of (t,j) inside its router tile
   size_t tile_counts;  // int32[ntiles*E]  rows of expert e in router tile
   size_t tile_base;    // int32[ntiles*E]  first permuted row of (tile, e)
   size_t offsets;      // int32[E+1]
-  size_t mtile_off;    // int32[E+1]   prefix of ceil(count/kGemmBM)
+  size_t mtile_off;    // int32[E+1]   prefix of ceil(count/chunk)
   size_t perm;         // int32[R]
   size_t inv;          // int32[R]
-  size_t xexp;         // int32[T]   per-token exponent e_t of the f16 scaling
   size_t rowexp;       // int32[R]   e_t of the token of each permuted row
   size_t x_perm;       // f16[R, d]  x[t] * 2^e_t
   size_t h_hi;         // bf16[R, W]
@@ -54,6 +107,7 @@ inline Workspace workspace_layout(int64_t T, int d, int W, int E, int k) {
   ws.status = take(64 * sizeof(int32_t));
   ws.topk_idx = take(size_t(R) * 4);
   ws.topk_w = take(size_t(R) * 4);
+  ws.logit_part = take(size_t(router_splits(T, d, E)) * size_t(T) * E * 4);
   ws.rank = take(size_t(R) * 4);
   ws.tile_counts = take(size_t(ntiles) * E * 4);
   ws.tile_base = take(size_t(ntiles) * E * 4);
@@ -61,7 +115,6 @@ inline Workspace workspace_layout(int64_t T, int d, int W, int E, int k) {
   ws.mtile_off = take(size_t(E + 1) * 4);
   ws.perm = take(size_t(R) * 4);
   ws.inv = take(size_t(R) * 4);
-  ws.xexp = take(size_t(T) * 4);
   ws.rowexp = take(size_t(R) * 4);
   ws.x_perm = take(size_t(R) * d * 2);
   ws.h_hi = take(size_t(R) * W * 2);
@@ -74,32 +127,36 @@ inline Workspace workspace_layout(int64_t T, int d, int W, int E, int k) {
 // ---------------------------------------------------------------- kernels --
 // Host-side launchers, one per stage.  All return the launch's cudaError_t.
 
-// K1: logits, top-k, selected softmax, per-tile histogram and in-tile ranks,
-// and the per-token exponent e_t = 14 - floor(log2 max|x_t|) used to hold x in
-// f16 exactly.  Also clears the status word (the first kernel of every call).
+// K1: logits (K-split partial sums, then summed in order with the bias), top-k,
+// selected softmax, per-tile histogram and in-tile ranks.  The first kernel
+// also clears the status word.
 cudaError_t launch_router_topk(const __nv_bfloat16* x, const float* router_w,
                                const float* router_b, int T, int d, int E, int k,
-                               int32_t* topk_idx, float* topk_w, int32_t* rank,
-                               int32_t* tile_counts, int32_t* xexp, int32_t* status,
+                               float* logit_part, int32_t* topk_idx, float* topk_w,
+                               int32_t* rank, int32_t* tile_counts, int32_t* status,
                                cudaStream_t s);
 
-// K2a: expert offsets, per-(tile, expert) bases, row-tile prefix.
-cudaError_t launch_route_scan(const int32_t* tile_counts, int ntiles, int E,
+// K2a: expert offsets, per-(tile, expert) bases, prefix of chunks of `chunk` rows.
+cudaError_t launch_route_scan(const int32_t* tile_counts, int ntiles, int E, int chunk,
                               int32_t* tile_base, int32_t* offsets, int32_t* mtile_off,
                               cudaStream_t s);
 
 // K2b: perm / inv tables and (optionally) the gathered activations in f16,
-// x_perm[row] = x[t] * 2^e_t, rowexp[row] = e_t.
+// x_perm[row] = x[t] * 2^e_t with e_t = 14 - floor(log2 max|x_t|) (so the
+// token's largest |x| lies in [2^14, 2^15) and every bf16 value is held
+// exactly), rowexp[row] = e_t.
 cudaError_t launch_route_scatter(const __nv_bfloat16* x, int T, int d, int E, int k,
                                  const int32_t* topk_idx, const int32_t* rank,
-                                 const int32_t* tile_base, const int32_t* xexp, int32_t* perm,
-                                 int32_t* inv, void* x_perm, int32_t* rowexp, int32_t* status,
+                                 const int32_t* tile_base, int32_t* perm, int32_t* inv,
+                                 void* x_perm, int32_t* rowexp, int32_t* status,
                                  cudaStream_t s);
 
 struct GemmArgs {
   int R, d, W, E;
+  int nb;                     // token chunk (multiple of 16, <= kGemmBM)
+  int stages_c, stages_b;     // ring depths of the TMEM design (set by its launcher)
   const int32_t* offsets;     // [E+1]
-  const int32_t* mtile_off;   // [E+1]
+  const int32_t* mtile_off;   // [E+1] prefix of ceil(count / nb)
   const void* x_perm;         // f16 [R, d], each row scaled by 2^rowexp[row]
   const int32_t* rowexp;      // [R]
   const uint8_t* w_gu; const uint8_t* w_gu_scale; const __nv_bfloat16* b_gu;
@@ -114,6 +171,18 @@ struct GemmArgs {
 cudaError_t launch_gateup(const GemmArgs& a, cudaStream_t s);
 // K4: y = (h_hi + h_lo) · W_dn^T + b_dn, per expert segment.
 cudaError_t launch_down(const GemmArgs& a, cudaStream_t s);
+
+// K3 / K4 with the dequantised weights as the MMA's A operand in tensor memory
+// (expert_gemm_tmem.cu).  Same arguments and results as launch_gateup /
+// launch_down; usable when its shared-memory plan fits (the reduction length
+// sets the size of the per-unit scale buffers).
+bool expert_gemm_tmem_fits(const GemmArgs& a);
+// Token chunk of the TMEM design for R routed rows over E experts: small
+// chunks (N = 16) when experts get few tokens, so an activation stage is a
+// few KB and the ring can be deep; 128 when they get many.
+int expert_gemm_tmem_chunk(int64_t R, int E);
+cudaError_t launch_gateup_tmem(const GemmArgs& a, cudaStream_t s);
+cudaError_t launch_down_tmem(const GemmArgs& a, cudaStream_t s);
 
 // K5: out[t] = bf16(Σ_j w[t,j] · y[inv[t,j]]); a row index outside [0, T·k)
 // is skipped and recorded in the status word.

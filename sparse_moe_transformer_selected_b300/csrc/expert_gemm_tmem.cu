@@ -1,0 +1,828 @@
+// K3 / K4 — grouped expert GEMMs with the dequantised weights held in tensor
+// memory (tcgen05 "A from TMEM" form).
+//
+// Each expert's segment of the permuted rows is multiplied by that expert's
+// MXFP4 weights ("OpenAI 最新开源模型 gpt-oss 架构与训练解析", 模型架构: MoE
+// weights in MXFP4, experts are gated-SwiGLU FFNs with clamping and the +1
+// term on the up branch; 更深对比更宽: d = W = 2880).
+//
+// The weights are the M side of the MMA and the tokens the N side:
+//   D[weight row, token] = Σ_k A[weight row, k] · B[token, k]
+// A (128 weight rows x 128 K per stage) is never written to shared memory: the
+// packed E2M1 codes arrive by TMA (128 rows x 256 K = 16 KB per code stage),
+// eight dequantiser warps convert them in registers and store them into TMEM
+// with tcgen05.st, and tcgen05.mma reads A from TMEM.  B (a chunk of nb tokens
+// x 64 K per stage, 128-byte swizzle) arrives by TMA.  The chunk nb is 16 when
+// experts get a few tokens each (a decode step: the kernel streams weights and
+// the activation ring is many small stages deep) and up to 128 when they get
+// many (prefill: experts are cut into 128-token chunks).
+//
+// Persistent kernel, one CTA per SM, 16 warps:
+//   warp 0      producer: scales (1-D bulk copy) and codes (TMA)
+//   warp 1      MMA issuer (one elected thread)
+//   warp 2      TMEM allocator (512 columns: 2 accumulator buffers of 128,
+//               each 128/nb accumulators of nb columns; 4 A stages of 64)
+//   warp 3      producer: activations (TMA)
+//   warps 4-7   epilogue, TMEM lane quarter = warp % 4
+//   warps 8-15  dequantisers, lane quarter = warp % 4, K half = (warp - 8) / 4
+// Work unit = (token chunk of one expert, weight M tile), chunk-major so a
+// chunk's activations and an expert's weights stay in L2 while they are reused.
+//
+// Number formats (exact products, fp32 accumulation):
+//   gate_up: A = E2M1 -> f16 (cvt.rn.f16x2.e2m1x2) times 2^(s - r_n), r_n the
+//            largest scale byte of weight row n; B = x · 2^e_t in f16 (the
+//            permute stage scales each token so its largest |x| lies in
+//            [2^14, 2^15), which holds every bf16 value).  The epilogue
+//            multiplies by 2^(r_n - 127) · 2^(-e_t).  Exact while a row's scales
+//            lie within 2^23 of its largest.
+//   down:    A = E2M1 -> f16 bits moved into a bf16 field (a factor 2^-112)
+//            times 2^(s - 15), exact for every scale byte <= 142; B = h as two
+//            bf16 terms (hi + lo), two MMAs per K step.
+#include "common.cuh"
+#include "tc_ptx.cuh"
+
+#include <cudaTypedefs.h>
+#include <cuda_fp16.h>
+#include <math.h>
+
+#include <mutex>
+
+namespace moe {
+namespace {
+
+constexpr int kNBMax = kGemmBM;              // largest token chunk (MMA N)
+constexpr int kMW = 128;                     // weight rows per unit (MMA M, TMEM lanes)
+constexpr int kCK = 256;                     // K per code stage: 128 B of codes per row
+constexpr int kAK = 128;                     // K per A stage: 64 TMEM columns
+constexpr int kBK = 64;                      // K per activation stage (one 128-byte row)
+constexpr int kMaxC = 8;                     // code-ring depth, most
+constexpr int kAStages = 4;
+constexpr int kMaxB = 16;                    // activation-ring depth, most
+constexpr int kRing = 4;                     // per-unit row-factor ring
+constexpr int kThreads = 512;
+constexpr int kWarpProd = 0, kWarpMMA = 1, kWarpTmem = 2, kWarpProdB = 3, kWarpEpi0 = 4,
+              kWarpDq0 = 8;
+constexpr int kTmemCols = 512;
+constexpr int kACol0 = 2 * kNBMax;           // first A-stage column
+constexpr int kACols = kAK / 2;              // columns per A stage
+constexpr int kCodeStageBytes = kMW * kCK / 2;   // 16 KB
+constexpr int kCodeBoxRows = 64;
+constexpr int kBox = 16;                     // rows per activation TMA box
+// code, A and B rings (full + empty each), scales and accumulators (2 + 2
+// each), the row-factor ring, and the final MMA drain
+constexpr int kNumBars = 2 * kMaxC + 2 * kAStages + 2 * kMaxB + 4 + 4 + 2 * kRing + 1;
+constexpr long long kSpinLimit = 4000000000ll;   // clock cycles before a wait gives up
+constexpr int kMaxSmem = 232448;                 // 227 KB opt-in per CTA
+
+enum class Mode { GateUp, Down };
+
+template <Mode M>
+struct Cfg;
+template <>
+struct Cfg<Mode::GateUp> {
+  static constexpr int NOPS = 1;      // B operands per K step: x
+  static constexpr bool kBf16 = false;
+};
+template <>
+struct Cfg<Mode::Down> {
+  static constexpr int NOPS = 2;      // h_hi, h_lo
+  static constexpr bool kBf16 = true;
+};
+
+struct Lay {
+  int codes, bt, bstage, sc, scbuf, rf, bars, misc, total;
+};
+
+// Shared-memory plan for reduction length K (nsb = K/32 scale bytes per row),
+// token chunk nb and ring depths nc (codes) and nbs (activations).
+template <Mode M>
+__host__ __device__ inline Lay layout(int nsb, int nb, int nc, int nbs) {
+  Lay l{};
+  int off = 0;
+  l.codes = off;
+  off += nc * kCodeStageBytes;
+  l.bstage = Cfg<M>::NOPS * nb * 128;
+  l.bt = off;
+  off += nbs * l.bstage;
+  l.scbuf = (kMW * nsb + 15) / 16 * 16;
+  l.sc = off;
+  off += 2 * l.scbuf;
+  l.rf = off;
+  off += kRing * kMW * 4;
+  off = (off + 7) & ~7;
+  l.bars = off;
+  off += kNumBars * 8;
+  l.misc = off;
+  off += 16;
+  l.total = off;
+  return l;
+}
+
+struct Unit {
+  int e, r0, n, mt;   // expert, first permuted row of the chunk, tokens in it, weight tile
+};
+
+__device__ __forceinline__ int expert_of_chunk(const int32_t* mtile_off, int E, int g) {
+  int lo = 0, hi = E;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(mtile_off + mid) <= g) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ Unit unit_of(const GemmArgs& a, int n_mt, int u) {
+  const int g = u / n_mt;
+  Unit w;
+  w.mt = u - g * n_mt;
+  w.e = expert_of_chunk(a.mtile_off, a.E, g);
+  w.r0 = __ldg(a.offsets + w.e) + (g - __ldg(a.mtile_off + w.e)) * a.nb;
+  w.n = min(a.nb, __ldg(a.offsets + w.e + 1) - w.r0);
+  return w;
+}
+
+// Bounded wait: true when the phase completed; false after a timeout (recorded
+// in the status word) or when another thread of the CTA gave up.
+__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                           int32_t* status) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (clock64() - t0 > kSpinLimit) {
+      *abort_flag = 1;
+      atomicMax(status, kStatusTimeout);
+      return false;
+    }
+  }
+}
+
+// Ring position: slot and phase parity, advanced in step by every role.
+struct Ring {
+  int slot = 0;
+  uint32_t phase = 0;
+  __device__ __forceinline__ void next(int n) {
+    if (++slot == n) { slot = 0; phase ^= 1; }
+  }
+};
+
+// Record of the loads a producer ring has in flight, so an aborting producer
+// can wait for them to land before the CTA exits.
+struct Inflight {
+  uint32_t issued = 0, parity = 0;
+  __device__ __forceinline__ void mark(int slot, uint32_t phase) {
+    issued |= 1u << slot;
+    parity = (parity & ~(1u << slot)) | (phase << slot);
+  }
+  __device__ __forceinline__ void drain(uint64_t* bars, int n) const {
+    const long long t0 = clock64();
+    for (int s = 0; s < n; ++s) {
+      if (!(issued >> s & 1u)) continue;
+      while (!ptx::mbar_try_wait(&bars[s], (parity >> s) & 1u) && clock64() - t0 < kSpinLimit) {
+      }
+    }
+  }
+};
+
+// ------------------------------------------------------------- dequant --
+
+// 2^delta as an f16x2 pair (delta <= 0); 0 below the f16 subnormal range.
+__device__ __forceinline__ uint32_t f16x2_pow2(int delta) {
+  uint32_t b;
+  if (delta >= -14) b = uint32_t(delta + 15) << 10;
+  else if (delta >= -24) b = 1u << (delta + 24);
+  else b = 0;
+  return b | (b << 16);
+}
+
+// 2^p as a bf16x2 pair, -126 <= p <= 127.
+__device__ __forceinline__ uint32_t bf16x2_pow2(int p) {
+  const uint32_t b = uint32_t(p + 127) << 7;
+  return b | (b << 16);
+}
+
+__device__ __forceinline__ uint32_t hmul2_f16(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t hmul2_bf16(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// 8 E2M1 codes (one 32-bit word, the even K index in the low nibble of each
+// byte) -> 4 f16x2 words holding K pairs (0,1), (2,3), (4,5), (6,7).
+__device__ __forceinline__ uint4 e2m1x8_to_f16(uint32_t w) {
+  uint4 r;
+  asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
+      " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+      " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}\n"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "r"(w));
+  return r;
+}
+
+// f16 bit pattern of an E2M1 value -> bf16 bit pattern of the same value times
+// 2^-112 (the exponent/mantissa field moves right by 3; the sign stays).
+__device__ __forceinline__ uint32_t f16x2_to_bf16x2_scaled(uint32_t t) {
+  return ((t >> 3) & 0x0FFF0FFFu) ^ (t & 0x80008000u);
+}
+
+template <Mode M>
+struct Dequant;
+
+template <>
+struct Dequant<Mode::GateUp> {
+  // 2^(s - r_n) in f16
+  __device__ __forceinline__ static uint32_t factor(int s, int rn) { return f16x2_pow2(s - rn); }
+  __device__ __forceinline__ static void convert(uint32_t w, uint32_t f, uint32_t* out) {
+    const uint4 v = e2m1x8_to_f16(w);
+    out[0] = hmul2_f16(v.x, f);
+    out[1] = hmul2_f16(v.y, f);
+    out[2] = hmul2_f16(v.z, f);
+    out[3] = hmul2_f16(v.w, f);
+  }
+};
+
+template <>
+struct Dequant<Mode::Down> {
+  // 2^(s - 15) in bf16 (the bit move left a factor 2^-112); r_n unused.
+  __device__ __forceinline__ static uint32_t factor(int s, int) { return bf16x2_pow2(min(s - 15, 127)); }
+  __device__ __forceinline__ static void convert(uint32_t w, uint32_t f, uint32_t* out) {
+    const uint4 v = e2m1x8_to_f16(w);
+    out[0] = hmul2_bf16(f16x2_to_bf16x2_scaled(v.x), f);
+    out[1] = hmul2_bf16(f16x2_to_bf16x2_scaled(v.y), f);
+    out[2] = hmul2_bf16(f16x2_to_bf16x2_scaled(v.z), f);
+    out[3] = hmul2_bf16(f16x2_to_bf16x2_scaled(v.w), f);
+  }
+};
+
+// Largest byte of the `nsb` bytes at smem byte offset `base` (4-aligned buffer).
+__device__ __forceinline__ int row_max_byte(const uint32_t* buf, uint32_t base, int nsb) {
+  const uint32_t end = base + uint32_t(nsb);
+  const uint32_t w0 = base >> 2, w1 = (end + 3) >> 2;
+  const uint32_t mlo = 0xFFFFFFFFu << (8 * (base & 3));
+  const uint32_t mhi = (end & 3) ? (0xFFFFFFFFu >> (8 * (4 - (end & 3)))) : 0xFFFFFFFFu;
+  uint32_t m;
+  if (w1 - w0 == 1) {
+    m = buf[w0] & mlo & mhi;
+  } else {
+    m = __vmaxu4(buf[w0] & mlo, buf[w1 - 1] & mhi);
+    for (uint32_t i = w0 + 1; i + 1 < w1; ++i) m = __vmaxu4(m, buf[i]);
+  }
+  m = __vmaxu4(m, m >> 16);
+  m = __vmaxu4(m, m >> 8);
+  return int(m & 0xFF);
+}
+
+// 16 columns of the unit's result for this warp's 32 lanes: the sum of the
+// nacc accumulators (stride nb columns), added in a fixed order.
+__device__ __forceinline__ void sum_accumulators(uint32_t taddr, int nb, int nacc, float (&acc)[16]) {
+  uint32_t v[16];
+  ptx::tmem_ld_32x32b_x16(taddr, v);
+  ptx::tmem_ld_wait();
+#pragma unroll
+  for (int j = 0; j < 16; ++j) acc[j] = __uint_as_float(v[j]);
+  for (int i = 1; i < nacc; ++i) {
+    ptx::tmem_ld_32x32b_x16(taddr + i * nb, v);
+    ptx::tmem_ld_wait();
+#pragma unroll
+    for (int j = 0; j < 16; ++j) acc[j] += __uint_as_float(v[j]);
+  }
+}
+
+// ------------------------------------------------------------- kernel --
+
+template <Mode M>
+__global__ void __launch_bounds__(kThreads, 1)
+moe_expert_gemm_tmem(const __grid_constant__ CUtensorMap map_w,
+                     const __grid_constant__ CUtensorMap map_b0,
+                     const __grid_constant__ CUtensorMap map_b1, const GemmArgs a) {
+  using C = Cfg<M>;
+  constexpr int NOPS = C::NOPS;
+  constexpr bool kGateUp = (M == Mode::GateUp);
+
+  const int K = kGateUp ? a.d : a.W;                 // reduction length
+  const int nsb = K / 32;                            // scale bytes per weight row
+  const int nA = (K + kAK - 1) / kAK;                // A stages per unit
+  const int nC = (K + kCK - 1) / kCK;                // code stages per unit
+  const int nKB = (K + kBK - 1) / kBK;               // activation stages per unit
+  const int rpe = kGateUp ? 2 * a.W : a.d;           // weight rows per expert
+  const int n_out = kGateUp ? a.W : a.d;
+  const int rows_per_tile = kGateUp ? kMW / 2 : kMW; // output features per unit
+  const int n_mt = (n_out + rows_per_tile - 1) / rows_per_tile;
+  const int NC = a.stages_c, NBS = a.stages_b;
+  // Independent accumulators per unit: an accumulator buffer is kNBMax columns
+  // and a chunk needs nb, so a small chunk spreads the K16 steps over several
+  // accumulators (MMAs into one accumulator wait for each other; a decode-sized
+  // N = 16 MMA is short, so one chain would leave the tensor pipe idle).
+  const int nacc_max = kNBMax / a.nb;
+  const int nk16 = (K + 15) / 16;
+  const int nacc = nacc_max < nk16 ? nacc_max : nk16;
+  const Lay L = layout<M>(nsb, a.nb, NC, NBS);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* codes = smem + L.codes;
+  uint8_t* bt = smem + L.bt;
+  uint8_t* scb = smem + L.sc;
+  float* rf = reinterpret_cast<float*>(smem + L.rf);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
+  uint64_t* code_full = bars;
+  uint64_t* code_empty = code_full + kMaxC;
+  uint64_t* a_full = code_empty + kMaxC;
+  uint64_t* a_empty = a_full + kAStages;
+  uint64_t* b_full = a_empty + kAStages;
+  uint64_t* b_empty = b_full + kMaxB;
+  uint64_t* sc_full = b_empty + kMaxB;
+  uint64_t* sc_empty = sc_full + 2;
+  uint64_t* acc_full = sc_empty + 2;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* rf_full = acc_empty + 2;
+  uint64_t* rf_empty = rf_full + kRing;
+  uint64_t* mma_done = rf_empty + kRing;
+  uint32_t* tmem_base_p = reinterpret_cast<uint32_t*>(smem + L.misc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kMaxC; ++s) {
+      ptx::mbar_init(&code_full[s], 1);
+      ptx::mbar_init(&code_empty[s], 8);
+    }
+    for (int s = 0; s < kAStages; ++s) {
+      ptx::mbar_init(&a_full[s], 8);
+      ptx::mbar_init(&a_empty[s], 1);
+    }
+    for (int s = 0; s < kMaxB; ++s) {
+      ptx::mbar_init(&b_full[s], 1);
+      ptx::mbar_init(&b_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      ptx::mbar_init(&sc_full[s], 1);
+      ptx::mbar_init(&sc_empty[s], 8);
+      ptx::mbar_init(&acc_full[s], 1);
+      ptx::mbar_init(&acc_empty[s], 4);
+    }
+    for (int s = 0; s < kRing; ++s) {
+      ptx::mbar_init(&rf_full[s], 4);
+      ptx::mbar_init(&rf_empty[s], 4);
+    }
+    ptx::mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == kWarpTmem) {
+    ptx::tmem_alloc(tmem_base_p, kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_base_p;
+  // Everything above overlapped the previous kernel; from here on global
+  // memory written by earlier kernels is read.  gate_up lets the down kernel
+  // start its own prologue now (its CTAs take an SM as this kernel's leave).
+  pdl_wait();
+  if (kGateUp) pdl_trigger();
+  const int units = __ldg(a.mtile_off + a.E) * n_mt;   // token chunks x weight tiles
+
+  if (warp == kWarpProd) {
+    // ------------------------------------------- producer: scales and codes --
+    if (ptx::elect_one()) {
+      ptx::tma_prefetch_desc(&map_w);
+      Ring cr;
+      Inflight c_in, s_in;
+      bool ok = true;
+      int q = 0;
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++q) {
+        const Unit w = unit_of(a, n_mt, u);
+        // the unit's scale rows (1-D bulk copies of contiguous rows)
+        const int sb = q & 1;
+        if (!wait_phase(&sc_empty[sb], ((q >> 1) & 1) ^ 1, abort_flag, a.status)) { ok = false; break; }
+        const uint8_t* wscale = kGateUp ? a.w_gu_scale : a.w_dn_scale;
+        int row_a, row_b;
+        if constexpr (kGateUp) {
+          const int n0 = w.mt * (kMW / 2);
+          const int nrows = min(kMW / 2, a.W - n0);
+          row_a = w.e * rpe + n0;
+          row_b = w.e * rpe + a.W + n0;
+          const uint32_t bytes = uint32_t(nrows * nsb);
+          ptx::mbar_arrive_expect_tx(&sc_full[sb], 2 * bytes);
+          uint8_t* dst = scb + sb * L.scbuf;
+          ptx::bulk_load(dst, wscale + size_t(row_a) * nsb, bytes, &sc_full[sb]);
+          ptx::bulk_load(dst + (kMW / 2) * nsb, wscale + size_t(row_b) * nsb, bytes, &sc_full[sb]);
+        } else {
+          const int m0 = w.mt * kMW;
+          const int nrows = min(kMW, a.d - m0);
+          row_a = w.e * rpe + m0;
+          row_b = row_a + kCodeBoxRows;
+          const uint32_t bytes = uint32_t(nrows * nsb);
+          ptx::mbar_arrive_expect_tx(&sc_full[sb], bytes);
+          ptx::bulk_load(scb + sb * L.scbuf, wscale + size_t(row_a) * nsb, bytes, &sc_full[sb]);
+        }
+        s_in.mark(sb, (q >> 1) & 1);
+        for (int cs = 0; cs < nC; ++cs) {
+          if (!wait_phase(&code_empty[cr.slot], cr.phase ^ 1, abort_flag, a.status)) { ok = false; break; }
+          uint8_t* cdst = codes + cr.slot * kCodeStageBytes;
+          ptx::mbar_arrive_expect_tx(&code_full[cr.slot], kCodeStageBytes);
+          ptx::tma_load_2d(cdst, &map_w, &code_full[cr.slot], cs * (kCK / 2), row_a);
+          ptx::tma_load_2d(cdst + kCodeStageBytes / 2, &map_w, &code_full[cr.slot], cs * (kCK / 2), row_b);
+          c_in.mark(cr.slot, cr.phase);
+          cr.next(NC);
+        }
+      }
+      if (!ok) {
+        c_in.drain(code_full, NC);
+        s_in.drain(sc_full, 2);
+      }
+    }
+  } else if (warp == kWarpProdB) {
+    // --------------------------------------------- producer: activations --
+    if (ptx::elect_one()) {
+      ptx::tma_prefetch_desc(&map_b0);
+      if (NOPS > 1) ptx::tma_prefetch_desc(&map_b1);
+      Ring br;
+      Inflight b_in;
+      bool ok = true;
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+        const Unit w = unit_of(a, n_mt, u);
+        const int nt = (w.n + kBox - 1) / kBox;      // 16-row boxes
+        for (int jb = 0; jb < nKB; ++jb) {
+          if (!wait_phase(&b_empty[br.slot], br.phase ^ 1, abort_flag, a.status)) { ok = false; break; }
+          ptx::mbar_arrive_expect_tx(&b_full[br.slot], uint32_t(NOPS * nt * kBox * 128));
+          uint8_t* bdst = bt + br.slot * L.bstage;
+          for (int op = 0; op < NOPS; ++op) {
+            const CUtensorMap* mp = op == 0 ? &map_b0 : &map_b1;
+            for (int g = 0; g < nt; ++g)
+              ptx::tma_load_2d(bdst + op * a.nb * 128 + g * kBox * 128, mp, &b_full[br.slot],
+                               jb * kBK, w.r0 + kBox * g);
+          }
+          b_in.mark(br.slot, br.phase);
+          br.next(NBS);
+        }
+      }
+      if (!ok) b_in.drain(b_full, NBS);
+    }
+  } else if (warp == kWarpMMA) {
+    // ------------------------------------------------------------ MMA issuer --
+    if (ptx::elect_one()) {
+      Ring ar, br;
+      bool ok = true;
+      int q = 0;
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++q) {
+        const Unit w = unit_of(a, n_mt, u);
+        const int N = (w.n + 15) & ~15;
+        const uint32_t idesc = ptx::idesc_f16(kMW, N, C::kBf16);
+        const int buf = q & 1;
+        if (!wait_phase(&acc_empty[buf], ((q >> 1) & 1) ^ 1, abort_flag, a.status)) { ok = false; break; }
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + buf * kNBMax;
+        int step = 0;                                // K16 step of the unit
+        for (int ja = 0; ja < nA && ok; ++ja) {
+          if (!wait_phase(&a_full[ar.slot], ar.phase, abort_flag, a.status)) { ok = false; break; }
+          const uint32_t a_tmem = tmem_base + kACol0 + ar.slot * kACols;
+          for (int h = 0; h < 2; ++h) {
+            const int jb = ja * 2 + h;
+            if (jb >= nKB) break;
+            if (!wait_phase(&b_full[br.slot], br.phase, abort_flag, a.status)) { ok = false; break; }
+            ptx::tc_fence_after();
+            uint8_t* bst = bt + br.slot * L.bstage;
+            for (int kk = 0; kk < kBK / 16; ++kk, ++step) {
+              if (jb * kBK + kk * 16 >= K) break;
+              // K16 steps rotate over nacc independent accumulators
+              const uint32_t acc = d_tmem + (step % nacc) * a.nb;
+#pragma unroll
+              for (int op = 0; op < NOPS; ++op) {
+                const uint64_t bdesc =
+                    ptx::desc_kmajor_sw128(ptx::smem_u32(bst + op * a.nb * 128)) + 2 * kk;
+                ptx::mma_f16_tmem_a(acc, a_tmem + (h * 4 + kk) * 8, bdesc, idesc,
+                                    (step >= nacc || op != 0) ? 1u : 0u);
+              }
+            }
+            ptx::mma_commit(&b_empty[br.slot]);
+            br.next(NBS);
+          }
+          if (!ok) break;
+          ptx::mma_commit(&a_empty[ar.slot]);
+          ar.next(kAStages);
+        }
+        if (!ok) break;
+        ptx::mma_commit(&acc_full[buf]);
+      }
+      // every issued MMA completes before TMEM is released
+      ptx::mma_commit(mma_done);
+      const long long t0 = clock64();
+      while (!ptx::mbar_try_wait(mma_done, 0) && clock64() - t0 < kSpinLimit) {
+      }
+    }
+  } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + 4) {
+    // ------------------------------------------------------------- epilogue --
+    const int quarter = warp & 3;
+    const int Ln = quarter * 32 + lane;          // TMEM lane = weight row of the tile
+    int q = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x, ++q) {
+      const Unit w = unit_of(a, n_mt, u);
+      const int buf = q & 1, ring = q % kRing;
+      const bool ok = wait_phase(&acc_full[buf], (q >> 1) & 1, abort_flag, a.status) &&
+                      wait_phase(&rf_full[ring], (q / kRing) & 1, abort_flag, a.status);
+      if (!__all_sync(0xffffffffu, ok)) break;   // warp-uniform: tcgen05.ld is .sync.aligned
+      ptx::tc_fence_after();
+      const float rowf = rf[ring * kMW + Ln];
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&rf_empty[ring]);
+      const uint32_t taddr = tmem_base + (uint32_t(quarter * 32) << 16) + buf * kNBMax;
+      if constexpr (kGateUp) {
+        const bool is_up = Ln & 1;
+        const int n = w.mt * (kMW / 2) + (Ln >> 1);
+        const bool nvalid = n < a.W;
+        const float bias =
+            nvalid ? __bfloat162float(a.b_gu[size_t(w.e) * 2 * a.W + (is_up ? a.W : 0) + n]) : 0.f;
+        for (int c = 0; c < w.n; c += 16) {
+          float acc[16];
+          sum_accumulators(taddr + c, a.nb, nacc, acc);
+          float z[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int col = c + j;
+            const float colf = col < w.n ? __int_as_float((127 - __ldg(a.rowexp + w.r0 + col)) << 23) : 0.f;
+            z[j] = acc[j] * rowf * colf + bias;
+          }
+          // gate lanes are even, up lanes odd: the even lane finishes tokens
+          // c..c+7, the odd lane tokens c+8..c+15
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj) {
+            const float send = is_up ? z[jj] : z[8 + jj];
+            const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
+            const float zg = is_up ? recv : z[jj];
+            const float zu = is_up ? z[8 + jj] : recv;
+            const int col = c + (is_up ? 8 + jj : jj);
+            const float gg = fminf(zg, a.limit);
+            const float uu = fminf(fmaxf(zu, -a.limit), a.limit);
+            const float hv = gg * (1.0f / (1.0f + expf(-a.alpha * gg))) * (uu + 1.0f);
+            const __nv_bfloat16 hh = __float2bfloat16_rn(hv);
+            const __nv_bfloat16 hl = __float2bfloat16_rn(hv - __bfloat162float(hh));
+            if (nvalid && col < w.n) {
+              const size_t o = size_t(w.r0 + col) * a.W + n;
+              a.h_hi[o] = hh;
+              a.h_lo[o] = hl;
+            }
+          }
+        }
+      } else {
+        const int n = w.mt * kMW + Ln;
+        const bool nvalid = n < a.d;
+        const float bias = nvalid ? __bfloat162float(a.b_dn[size_t(w.e) * a.d + n]) : 0.f;
+        for (int c = 0; c < w.n; c += 16) {
+          float acc[16];
+          sum_accumulators(taddr + c, a.nb, nacc, acc);
+          if (nvalid) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (c + j < w.n) a.y[size_t(w.r0 + c + j) * a.d + n] = acc[j] * rowf + bias;
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&acc_empty[buf]);
+    }
+  } else if (warp >= kWarpDq0) {
+    // --------------------------------------------------------- dequantisers --
+    // Software-pipelined: the tcgen05.st of A stage j drains while stage j+1
+    // is converted (two register buffers); stage j is handed to the MMA
+    // (tcgen05.wait::st, fence, arrive) just before stage j+1 is stored.
+    const int quarter = warp & 3;
+    const int hf = (warp - kWarpDq0) >> 2;       // K half of every A stage
+    const int Ln = quarter * 32 + lane;          // TMEM lane = weight row of the tile
+    const int sr = kGateUp ? ((Ln & 1) ? kMW / 2 + (Ln >> 1) : (Ln >> 1)) : Ln;   // smem row
+    const uint32_t lane_addr = uint32_t(quarter * 32) << 16;
+    Ring cr, ar;
+    int pending = -1;                            // A slot stored but not yet handed over
+    bool ok = true;
+    uint32_t r0[32], r1[32];
+
+    // Convert this thread's 64 codes of A stage ja (code stage in `cst`) into r.
+    auto convert = [&](const uint8_t* cst, const uint8_t* srow, bool valid, int rn, int ja,
+                       uint32_t (&r)[32]) {
+      const int b0 = (ja * kAK + hf * 64) / 32;  // first of the two scale blocks
+      uint32_t s01 = 0;
+      if (valid && b0 < nsb) {
+        // one 16-bit read when the row's byte offset is even (K/32 odd makes
+        // every other row start at an odd offset)
+        const uint8_t* sp = srow + b0;
+        if (b0 + 1 >= nsb) s01 = sp[0];
+        else if ((reinterpret_cast<uintptr_t>(sp) & 1u) == 0) s01 = *reinterpret_cast<const uint16_t*>(sp);
+        else s01 = uint32_t(sp[0]) | (uint32_t(sp[1]) << 8);
+      }
+      const uint32_t f0 = (valid && b0 < nsb) ? Dequant<M>::factor(int(s01 & 0xFF), rn) : 0u;
+      const uint32_t f1 = (valid && b0 + 1 < nsb) ? Dequant<M>::factor(int(s01 >> 8), rn) : 0u;
+      const int ch = (ja & 1) * 4 + hf * 2;      // 16-byte chunk of the 128-byte row
+      const uint4 x0 = *reinterpret_cast<const uint4*>(cst + ptx::sw128_offset(sr, ch));
+      const uint4 x1 = *reinterpret_cast<const uint4*>(cst + ptx::sw128_offset(sr, ch + 1));
+      const uint32_t wv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+      for (int c = 0; c < 8; ++c) Dequant<M>::convert(wv[c], c < 4 ? f0 : f1, &r[4 * c]);
+    };
+    // Hand the pending stage to the MMA once its stores have landed.
+    auto hand_over = [&]() {
+      if (pending < 0) return;
+      ptx::tmem_st_wait();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&a_full[pending]);
+      pending = -1;
+    };
+    // Store r as A stage slot ar.slot (after the MMA has released it).
+    auto store = [&](const uint32_t (&r)[32]) -> bool {
+      if (!__all_sync(0xffffffffu, wait_phase(&a_empty[ar.slot], ar.phase ^ 1, abort_flag, a.status)))
+        return false;
+      ptx::tmem_st_32x32b_x32(tmem_base + lane_addr + kACol0 + ar.slot * kACols + hf * 32, r);
+      pending = ar.slot;
+      ar.next(kAStages);
+      return true;
+    };
+
+    int q = 0;
+    for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++q) {
+      const Unit w = unit_of(a, n_mt, u);
+      const bool valid = kGateUp ? (w.mt * (kMW / 2) + (Ln >> 1) < a.W) : (w.mt * kMW + Ln < a.d);
+      const int sb = q & 1, ring = q % kRing;
+      ok = __all_sync(0xffffffffu, wait_phase(&sc_full[sb], (q >> 1) & 1, abort_flag, a.status));
+      if (!ok) break;
+      const uint8_t* srow = scb + sb * L.scbuf + sr * nsb;
+      int rn = 0;
+      if (kGateUp && valid)
+        rn = row_max_byte(reinterpret_cast<const uint32_t*>(scb + sb * L.scbuf), uint32_t(sr * nsb), nsb);
+      if (hf == 0) {
+        ok = __all_sync(0xffffffffu, wait_phase(&rf_empty[ring], ((q / kRing) & 1) ^ 1, abort_flag, a.status));
+        if (!ok) break;
+        rf[ring * kMW + Ln] = valid ? (kGateUp ? ldexpf(1.0f, rn - 127) : 1.0f) : 0.f;
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&rf_full[ring]);
+      }
+      for (int cs = 0; cs < nC && ok; ++cs) {
+        ok = __all_sync(0xffffffffu, wait_phase(&code_full[cr.slot], cr.phase, abort_flag, a.status));
+        if (!ok) break;
+        const uint8_t* cst = codes + cr.slot * kCodeStageBytes;
+        const int ja0 = cs * 2;
+        const bool second = ja0 + 1 < nA;
+        // Each store drains while the next stage converts; a register buffer is
+        // rewritten only after its own store has completed (hand_over waits).
+        convert(cst, srow, valid, rn, ja0, r0);
+        hand_over();                              // the previous code stage's last A stage
+        if (!(ok = store(r0))) break;
+        if (second) convert(cst, srow, valid, rn, ja0 + 1, r1);
+        // the code stage has been read: release it
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&code_empty[cr.slot]);
+        cr.next(NC);
+        if (second) {
+          hand_over();                            // r0
+          if (!(ok = store(r1))) break;           // pending into the next code stage
+        }
+      }
+      if (!ok) break;
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&sc_empty[sb]);
+    }
+    // the last stage (or, after a failure, whatever was stored) reaches the MMA
+    // or at least completes before TMEM is released
+    if (ok) hand_over();
+    else ptx::tmem_st_wait();
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpTmem) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ host --
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// Row-major [rows, cols] matrix of `esize`-byte elements, box {box_cols, box_rows},
+// 128-byte swizzle.
+cudaError_t make_map(CUtensorMap* map, CUtensorMapDataType dt, int esize, const void* base,
+                     long long rows, long long cols, int box_cols, int box_rows) {
+  auto enc = get_encode();
+  if (!enc) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {cuuint64_t(cols), cuuint64_t(rows)};
+  const cuuint64_t strides[1] = {cuuint64_t(cols) * esize};
+  const cuuint32_t box[2] = {cuuint32_t(box_cols), cuuint32_t(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+int num_sms() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
+}
+
+// Ring depths for one launch: deep code prefetch when the kernel streams
+// weights (small chunks), a deep activation ring in whatever shared memory is
+// left (at most kMaxB stages).
+template <Mode M>
+void plan(GemmArgs& a) {
+  const int K = (M == Mode::GateUp) ? a.d : a.W;
+  a.stages_c = a.nb <= 32 ? 6 : 3;
+  const Lay base = layout<M>(K / 32, a.nb, a.stages_c, 0);
+  const int room = kMaxSmem - 1024 - base.total;
+  const int per = Cfg<M>::NOPS * a.nb * 128;
+  a.stages_b = room / per < kMaxB ? room / per : kMaxB;
+}
+
+template <Mode M>
+size_t smem_bytes(const GemmArgs& a) {
+  const int K = (M == Mode::GateUp) ? a.d : a.W;
+  return size_t(layout<M>(K / 32, a.nb, a.stages_c, a.stages_b).total) + 1024;
+}
+
+template <Mode M>
+cudaError_t launch(const GemmArgs& args, cudaStream_t s) {
+  GemmArgs a = args;
+  plan<M>(a);
+  const size_t smem = smem_bytes<M>(a);
+  if (a.stages_b < 2 || smem > size_t(kMaxSmem) || a.nb < 16 || a.nb > kNBMax || a.nb % 16)
+    return cudaErrorInvalidConfiguration;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(moe_expert_gemm_tmem<M>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  CUtensorMap mw, m0, m1;
+  cudaError_t e;
+  if (M == Mode::GateUp) {
+    e = make_map(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.w_gu, (long long)a.E * 2 * a.W, a.d / 2,
+                 kCK / 2, kCodeBoxRows);
+    if (e == cudaSuccess)
+      e = make_map(&m0, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.x_perm, a.R, a.d, kBK, kBox);
+    m1 = m0;
+  } else {
+    e = make_map(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.w_dn, (long long)a.E * a.d, a.W / 2,
+                 kCK / 2, kCodeBoxRows);
+    if (e == cudaSuccess)
+      e = make_map(&m0, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.h_hi, a.R, a.W, kBK, kBox);
+    if (e == cudaSuccess)
+      e = make_map(&m1, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.h_lo, a.R, a.W, kBK, kBox);
+  }
+  if (e != cudaSuccess) return e;
+  const int n_out = (M == Mode::GateUp) ? a.W : a.d;
+  const int rows_per_tile = (M == Mode::GateUp) ? kMW / 2 : kMW;
+  const long long n_mt = (n_out + rows_per_tile - 1) / rows_per_tile;
+  const long long units_bound = (long long)(a.R / a.nb + a.E) * n_mt;
+  const int grid = int(units_bound < num_sms() ? units_bound : num_sms());
+  return launch_pdl(moe_expert_gemm_tmem<M>, dim3(grid), dim3(kThreads), smem, s, mw, m0, m1, a);
+}
+
+}  // namespace
+
+int expert_gemm_tmem_chunk(int64_t R, int E) {
+  const int64_t avg = R / (E > 0 ? E : 1);
+  return avg <= 8 ? 16 : avg <= 16 ? 32 : avg <= 32 ? 64 : 128;
+}
+
+bool expert_gemm_tmem_fits(const GemmArgs& args) {
+  GemmArgs a = args;
+  a.nb = expert_gemm_tmem_chunk(a.R, a.E);
+  GemmArgs g = a, d = a;
+  plan<Mode::GateUp>(g);
+  plan<Mode::Down>(d);
+  return g.stages_b >= 2 && d.stages_b >= 2 && smem_bytes<Mode::GateUp>(g) <= size_t(kMaxSmem) &&
+         smem_bytes<Mode::Down>(d) <= size_t(kMaxSmem);
+}
+cudaError_t launch_gateup_tmem(const GemmArgs& a, cudaStream_t s) { return launch<Mode::GateUp>(a, s); }
+cudaError_t launch_down_tmem(const GemmArgs& a, cudaStream_t s) { return launch<Mode::Down>(a, s); }
+
+}  // namespace moe

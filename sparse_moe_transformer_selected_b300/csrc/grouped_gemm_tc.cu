@@ -90,8 +90,10 @@ __device__ __forceinline__ int expert_of_tile(const int32_t* mtile_off, int E, i
   return lo;
 }
 
-__device__ __forceinline__ Unit unit_of(const GemmArgs& a, int mt_total, int u, int n_step) {
-  const int nt = u / mt_total, g = u - nt * mt_total;
+// Units are dealt row-tile-major: the CTAs in flight share a few activation
+// row tiles (and the weights of one or two experts), which stay in L2.
+__device__ __forceinline__ Unit unit_of(const GemmArgs& a, int n_tiles, int u, int n_step) {
+  const int g = u / n_tiles, nt = u - g * n_tiles;
   Unit w;
   w.e = expert_of_tile(a.mtile_off, a.E, g);
   const int off = __ldg(a.offsets + w.e);
@@ -229,8 +231,6 @@ moe_gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a0,
   const int n_step = kGateUp ? kBN / 2 : kBN;           // output columns per unit
   const int n_out = kGateUp ? a.W : a.d;
   const int n_tiles = (n_out + n_step - 1) / n_step;
-  const int mt_total = __ldg(a.mtile_off + a.E);
-  const int units = mt_total * n_tiles;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -255,6 +255,8 @@ moe_gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a0,
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_base_p;
+  pdl_wait();
+  const int units = __ldg(a.mtile_off + a.E) * n_tiles;   // row tiles x N tiles
 
   if (warp == kWarpTMA) {
     // ------------------------------------------------------ TMA producer --
@@ -267,7 +269,7 @@ moe_gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a0,
       uint32_t lastph = 0;    // bit s: phase parity of that last load
       bool ok = true;
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-        const Unit w = unit_of(a, mt_total, u, n_step);
+        const Unit w = unit_of(a, n_tiles, u, n_step);
         for (int kb = 0; kb < KB; ++kb) {
           if (!wait_phase(&empty[stage], phase ^ 1, abort_flag, a.status)) { ok = false; break; }
           ptx::mbar_arrive_expect_tx(&a_full[stage], NA * kATileBytes);
@@ -337,7 +339,7 @@ moe_gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a0,
     const int row = quarter * 32 + lane;
     int q = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x, ++q) {
-      const Unit w = unit_of(a, mt_total, u, n_step);
+      const Unit w = unit_of(a, n_tiles, u, n_step);
       const int buf = q & 1;
       bool ok = wait_phase(&acc_full[buf], (q >> 1) & 1, abort_flag, a.status) &&
                 wait_phase(&cf_ready[q % S::kRing], (q / S::kRing) & 1, abort_flag, a.status);
@@ -443,7 +445,7 @@ moe_gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a0,
     int q = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++q) {
-      const Unit w = unit_of(a, mt_total, u, n_step);
+      const Unit w = unit_of(a, n_tiles, u, n_step);
       int nrow;
       bool valid;
       if constexpr (kGateUp) {
@@ -459,6 +461,7 @@ moe_gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a0,
       const uint8_t* srow = wscale + wrow * nsb;
       int rn = 0;
       if (valid) {
+#pragma unroll 8
         for (int j = 0; j < nsb; ++j) rn = max(rn, int(__ldg(srow + j)));
       }
       colfac[(q % S::kRing) * kBN + i] = valid ? (kGateUp ? ldexpf(1.0f, rn - 127) : 1.0f) : 0.f;
@@ -586,8 +589,7 @@ cudaError_t launch(const GemmArgs& a, cudaStream_t s) {
   const int n_out = (M == Mode::GateUp) ? a.W : a.d;
   const long long units_bound = (long long)(a.R / kBM + a.E) * ((n_out + n_step - 1) / n_step);
   const int grid = int(units_bound < num_sms() ? units_bound : num_sms());
-  moe_gemm_tc_kernel<M><<<grid, kThreads, S::kAlloc, s>>>(m0, m1, a);
-  return cudaGetLastError();
+  return launch_pdl(moe_gemm_tc_kernel<M>, dim3(grid), dim3(kThreads), S::kAlloc, s, m0, m1, a);
 }
 
 }  // namespace

@@ -5,6 +5,8 @@
 
 #include <stdarg.h>
 #include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
 
 #include <mutex>
 #include <string>
@@ -70,12 +72,33 @@ moe_status check_device() {
   return MOE_OK;
 }
 
+// Which grouped-GEMM design runs K3/K4.  The weight-in-TMEM kernels are the
+// default wherever their shared-memory plan fits; MOE_GEMM=smem selects the
+// kernels that stage dequantised weights in shared memory (a diagnostic and
+// tuning knob; both produce results within the same tolerances).
+bool use_tmem_gemm(const moe::GemmArgs& a) {
+  const char* s = getenv("MOE_GEMM");
+  if (s && strcmp(s, "smem") == 0) return false;
+  return moe::expert_gemm_tmem_fits(a);
+}
+
+moe::GemmArgs gemm_args(int64_t T, int d, int W, int E, int k) {
+  moe::GemmArgs a{};
+  a.R = int(T * k);
+  a.d = d;
+  a.W = W;
+  a.E = E;
+  a.nb = moe::kGemmBM;
+  return a;
+}
+
 template <class T>
 T* at(void* base, size_t off) {
   return reinterpret_cast<T*>(static_cast<char*>(base) + off);
 }
 
 struct RouteOut {
+  float* logit_part;
   int32_t* topk_idx;
   float* topk_w;
   int32_t* rank;
@@ -85,7 +108,6 @@ struct RouteOut {
   int32_t* mtile_off;
   int32_t* perm;
   int32_t* inv;
-  int32_t* xexp;
   int32_t* rowexp;
   void* x_perm;
   int32_t* status;
@@ -93,6 +115,7 @@ struct RouteOut {
 
 RouteOut route_tables(void* ws, const moe::Workspace& L, bool gather) {
   RouteOut r;
+  r.logit_part = at<float>(ws, L.logit_part);
   r.topk_idx = at<int32_t>(ws, L.topk_idx);
   r.topk_w = at<float>(ws, L.topk_w);
   r.rank = at<int32_t>(ws, L.rank);
@@ -102,7 +125,6 @@ RouteOut route_tables(void* ws, const moe::Workspace& L, bool gather) {
   r.mtile_off = at<int32_t>(ws, L.mtile_off);
   r.perm = at<int32_t>(ws, L.perm);
   r.inv = at<int32_t>(ws, L.inv);
-  r.xexp = at<int32_t>(ws, L.xexp);
   r.rowexp = at<int32_t>(ws, L.rowexp);
   r.x_perm = gather ? at<void>(ws, L.x_perm) : nullptr;
   r.status = at<int32_t>(ws, L.status);
@@ -110,18 +132,19 @@ RouteOut route_tables(void* ws, const moe::Workspace& L, bool gather) {
 }
 
 moe_status run_route(const void* x, int64_t T, int d, const float* rw, const float* rb, int E,
-                     int k, const RouteOut& r, cudaStream_t s) {
+                     int k, int chunk, const RouteOut& r, cudaStream_t s) {
   const auto* xb = static_cast<const __nv_bfloat16*>(x);
   const int ntiles = int((T + moe::kRouterTile - 1) / moe::kRouterTile);
-  cudaError_t e = moe::launch_router_topk(xb, rw, rb, int(T), d, E, k, r.topk_idx, r.topk_w,
-                                          r.rank, r.tile_counts, r.xexp, r.status, s);
+  cudaError_t e = moe::launch_router_topk(xb, rw, rb, int(T), d, E, k, r.logit_part, r.topk_idx,
+                                          r.topk_w, r.rank, r.tile_counts, r.status, s);
   if (e != cudaSuccess) return cuda_fail(e, "router_topk launch");
   if ((e = trace(1, s)) != cudaSuccess) return cuda_fail(e, "trace event");
-  e = moe::launch_route_scan(r.tile_counts, ntiles, E, r.tile_base, r.offsets, r.mtile_off, s);
+  e = moe::launch_route_scan(r.tile_counts, ntiles, E, chunk, r.tile_base, r.offsets, r.mtile_off,
+                             s);
   if (e != cudaSuccess) return cuda_fail(e, "route_scan launch");
   if ((e = trace(2, s)) != cudaSuccess) return cuda_fail(e, "trace event");
-  e = moe::launch_route_scatter(xb, int(T), d, E, k, r.topk_idx, r.rank, r.tile_base, r.xexp,
-                                r.perm, r.inv, r.x_perm, r.rowexp, r.status, s);
+  e = moe::launch_route_scatter(xb, int(T), d, E, k, r.topk_idx, r.rank, r.tile_base, r.perm,
+                                r.inv, r.x_perm, r.rowexp, r.status, s);
   if (e != cudaSuccess) return cuda_fail(e, "route_scatter launch");
   if ((e = trace(3, s)) != cudaSuccess) return cuda_fail(e, "trace event");
   return MOE_OK;
@@ -189,16 +212,14 @@ moe_status moe_forward(const void* x_bf16, int64_t T, int d, int W, const float*
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const RouteOut r = route_tables(workspace, L, true);
+  moe::GemmArgs a = gemm_args(T, d, W, E, k);
+  const bool tmem = use_tmem_gemm(a);
+  if (tmem) a.nb = moe::expert_gemm_tmem_chunk(a.R, E);
   cudaError_t e = trace(0, s);
   if (e != cudaSuccess) return cuda_fail(e, "trace event");
-  st = run_route(x_bf16, T, d, router_w, router_b, E, k, r, s);
+  st = run_route(x_bf16, T, d, router_w, router_b, E, k, a.nb, r, s);
   if (st != MOE_OK) return st;
 
-  moe::GemmArgs a;
-  a.R = int(T * k);
-  a.d = d;
-  a.W = W;
-  a.E = E;
   a.offsets = r.offsets;
   a.mtile_off = r.mtile_off;
   a.x_perm = r.x_perm;
@@ -215,10 +236,10 @@ moe_status moe_forward(const void* x_bf16, int64_t T, int d, int W, const float*
   a.h_lo = at<__nv_bfloat16>(workspace, L.h_lo);
   a.y = at<float>(workspace, L.y);
   a.status = r.status;
-  e = moe::launch_gateup(a, s);
+  e = tmem ? moe::launch_gateup_tmem(a, s) : moe::launch_gateup(a, s);
   if (e != cudaSuccess) return cuda_fail(e, "gate_up launch");
   if ((e = trace(4, s)) != cudaSuccess) return cuda_fail(e, "trace event");
-  e = moe::launch_down(a, s);
+  e = tmem ? moe::launch_down_tmem(a, s) : moe::launch_down(a, s);
   if (e != cudaSuccess) return cuda_fail(e, "down launch");
   if ((e = trace(5, s)) != cudaSuccess) return cuda_fail(e, "trace event");
   e = moe::launch_combine(a.y, r.topk_w, r.inv, int(T), d, k,
@@ -251,7 +272,7 @@ moe_status moe_route(const void* x_bf16, int64_t T, int d, const float* router_w
   if (st != MOE_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const RouteOut r = route_tables(workspace, L, false);
-  st = run_route(x_bf16, T, d, router_w, router_b, E, k, r, s);
+  st = run_route(x_bf16, T, d, router_w, router_b, E, k, moe::kGemmBM, r, s);
   if (st != MOE_OK) return st;
   const size_t R = size_t(T) * k;
   struct { void* dst; const void* src; size_t n; } copies[] = {

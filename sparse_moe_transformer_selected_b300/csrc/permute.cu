@@ -10,6 +10,7 @@
 #include "common.cuh"
 
 #include <cuda_fp16.h>
+#include <math.h>
 
 namespace moe {
 namespace {
@@ -19,7 +20,7 @@ constexpr int kScanThreads = 1024;
 // One CTA.  Thread (g, e) sums expert e over a contiguous range of tiles,
 // then the partial sums are scanned in tile order and in expert order.
 __global__ void __launch_bounds__(kScanThreads)
-route_scan_kernel(const int32_t* __restrict__ tile_counts, int ntiles, int E,
+route_scan_kernel(const int32_t* __restrict__ tile_counts, int ntiles, int E, int chunk,
                   int32_t* __restrict__ tile_base, int32_t* __restrict__ offsets,
                   int32_t* __restrict__ mtile_off) {
   __shared__ int32_t part[kScanThreads];
@@ -29,8 +30,9 @@ route_scan_kernel(const int32_t* __restrict__ tile_counts, int ntiles, int E,
   const int G = kScanThreads / E;           // E <= 256 -> G >= 4
   const int g = tid / E, e = tid - g * E;
   const bool active = g < G;
-  const int chunk = (ntiles + G - 1) / G;
-  const int ta = min(ntiles, g * chunk), tb = min(ntiles, ta + chunk);
+  const int span = (ntiles + G - 1) / G;      // router tiles per thread
+  const int ta = min(ntiles, g * span), tb = min(ntiles, ta + span);
+  pdl_wait();
   int32_t sum = 0;
   if (active)
     for (int t = ta; t < tb; ++t) sum += tile_counts[(size_t)t * E + e];
@@ -53,7 +55,7 @@ route_scan_kernel(const int32_t* __restrict__ tile_counts, int ntiles, int E,
       offsets[q] = run;
       mtile_off[q] = mrun;
       run += total[q];
-      mrun += (total[q] + kGemmBM - 1) / kGemmBM;
+      mrun += (total[q] + chunk - 1) / chunk;
     }
     offsets[E] = run;
     mtile_off[E] = mrun;
@@ -74,13 +76,14 @@ route_scan_kernel(const int32_t* __restrict__ tile_counts, int ntiles, int E,
 __global__ void __launch_bounds__(256)
 route_scatter_kernel(const __nv_bfloat16* __restrict__ x, int T, int d, int E, int k,
                      const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ rank,
-                     const int32_t* __restrict__ tile_base, const int32_t* __restrict__ xexp,
+                     const int32_t* __restrict__ tile_base,
                      int32_t* __restrict__ perm, int32_t* __restrict__ inv,
                      __half* __restrict__ x_perm, int32_t* __restrict__ rowexp,
                      int32_t* __restrict__ status) {
   const int64_t R = (int64_t)T * k;
   const int64_t q = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
+  pdl_wait();
   if (q >= R) return;
   const int t = (int)(q / k);
   const int e = topk_idx[q];
@@ -98,12 +101,23 @@ route_scatter_kernel(const __nv_bfloat16* __restrict__ x, int T, int d, int E, i
     if (inv) inv[q] = (int32_t)row;
   }
   if (x_perm) {
-    const int et = xexp[t];
-    if (lane == 0) rowexp[row] = et;
-    const float f = __int_as_float((et + 127) << 23);   // 2^e_t, |e_t| <= 126
     const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * d);
     uint4* dst = reinterpret_cast<uint4*>(x_perm + (size_t)row * d);
     const int n16 = d / 8;
+    float xmax = 0.f;                                    // largest |x| of the token
+    for (int i = lane; i < n16; i += 32) {
+      const uint4 v = src[i];
+      const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        xmax = fmaxf(xmax, fmaxf(fabsf(__uint_as_float(in[c] << 16)),
+                                 fabsf(__uint_as_float(in[c] & 0xFFFF0000u))));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) xmax = fmaxf(xmax, __shfl_xor_sync(0xffffffffu, xmax, off));
+    const int et = (xmax > 0.f && isfinite(xmax)) ? max(-126, min(126, 14 - ilogbf(xmax))) : 0;
+    if (lane == 0) rowexp[row] = et;
+    const float f = __int_as_float((et + 127) << 23);   // 2^e_t, |e_t| <= 126
     for (int i = lane; i < n16; i += 32) {
       const uint4 v = src[i];
       const uint32_t in[4] = {v.x, v.y, v.z, v.w};
@@ -122,26 +136,24 @@ route_scatter_kernel(const __nv_bfloat16* __restrict__ x, int T, int d, int E, i
 
 }  // namespace
 
-cudaError_t launch_route_scan(const int32_t* tile_counts, int ntiles, int E,
+cudaError_t launch_route_scan(const int32_t* tile_counts, int ntiles, int E, int chunk,
                               int32_t* tile_base, int32_t* offsets, int32_t* mtile_off,
                               cudaStream_t s) {
-  route_scan_kernel<<<1, kScanThreads, 0, s>>>(tile_counts, ntiles, E, tile_base, offsets,
-                                               mtile_off);
-  return cudaGetLastError();
+  return launch_pdl(route_scan_kernel, dim3(1), dim3(kScanThreads), 0, s, tile_counts, ntiles, E,
+                    chunk, tile_base, offsets, mtile_off);
 }
 
 cudaError_t launch_route_scatter(const __nv_bfloat16* x, int T, int d, int E, int k,
                                  const int32_t* topk_idx, const int32_t* rank,
-                                 const int32_t* tile_base, const int32_t* xexp, int32_t* perm,
-                                 int32_t* inv, void* x_perm, int32_t* rowexp, int32_t* status,
+                                 const int32_t* tile_base, int32_t* perm, int32_t* inv,
+                                 void* x_perm, int32_t* rowexp, int32_t* status,
                                  cudaStream_t s) {
   const int64_t R = (int64_t)T * k;
   const int warps_per_block = 8;
   const int64_t grid = (R + warps_per_block - 1) / warps_per_block;
-  route_scatter_kernel<<<(unsigned)grid, warps_per_block * 32, 0, s>>>(
-      x, T, d, E, k, topk_idx, rank, tile_base, xexp, perm, inv,
-      static_cast<__half*>(x_perm), rowexp, status);
-  return cudaGetLastError();
+  return launch_pdl(route_scatter_kernel, dim3((unsigned)grid), dim3(warps_per_block * 32), 0, s,
+                    x, T, d, E, k, topk_idx, rank, tile_base, perm, inv,
+                    static_cast<__half*>(x_perm), rowexp, status);
 }
 
 }  // namespace moe

@@ -7,9 +7,13 @@
 // experts).  Ties go to the lower expert index; slots are ordered by
 // (logit desc, index asc).
 //
-// One CTA = 32 tokens x all E experts.  fp32 FMA on CUDA cores: the router is
-// 2·T·d·E flops, well under 1% of the block, and fp32 keeps the selection
-// faithful to the exact logits except at true near-ties.
+// Two kernels.  router_logits: a CTA takes 32 tokens x all E experts over one
+// range of K and writes that range's partial dot products (fp32 FMA on CUDA
+// cores); small T is split over many K ranges so the few tokens of a decode
+// step still spread over the GPU.  router_topk: a CTA sums the partials of 32
+// tokens in a fixed order, adds the bias, and selects.  The router is 2·T·d·E
+// flops, well under 1% of the block; fp32 keeps the selection faithful to the
+// exact logits except at true near-ties.
 #include "common.cuh"
 
 #include <math.h>
@@ -25,29 +29,29 @@ constexpr int kLgStride = kMaxE + 8;     // floats per row of the logits / W til
 
 template <int NPER>   // experts per lane: e = lane + 32*i, i < NPER
 __global__ void __launch_bounds__(kThreads)
-router_topk_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__ rw,
-                   const float* __restrict__ rb, int T, int d, int E, int k,
-                   int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
-                   int32_t* __restrict__ rank, int32_t* __restrict__ tile_counts,
-                   int32_t* __restrict__ xexp, int32_t* __restrict__ status) {
+router_logits_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__ rw, int T,
+                     int d, int E, int kc, int eg, float* __restrict__ part,
+                     int32_t* __restrict__ status) {
   __shared__ float xs[kTT][kKC + 1];
-  __shared__ float wl[kKC * kLgStride];  // W chunk [k][e]; later logits [t][e]
-  __shared__ uint32_t mask[kMaxE];       // bit t: token t of this tile picked e
-  __shared__ int32_t sel[kTT][8];
+  __shared__ float wl[kKC * kLgStride];  // W chunk [k][e]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int t0 = blockIdx.x * kTT;
-  if (blockIdx.x == 0 && tid == 0) status[0] = 0;
-  for (int e = tid; e < kMaxE; e += kThreads) mask[e] = 0u;
+  const int ks = blockIdx.y;
+  const int kb = ks * kc, ke = min(d, kb + kc);
+  const int e0 = blockIdx.z * eg;                // this CTA's experts: e0 .. e0+eg-1
+  const int ne = min(eg, E - e0);
+  pdl_wait();
+  if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && tid == 0)
+    status[0] = 0;                               // first kernel of a call
 
-  float xmax = 0.f;   // max |x| over this thread's share of token (tid >> 3)
   float acc[4][NPER];
 #pragma unroll
   for (int i = 0; i < 4; ++i)
 #pragma unroll
     for (int j = 0; j < NPER; ++j) acc[i][j] = 0.f;
 
-  for (int k0 = 0; k0 < d; k0 += kKC) {
+  for (int k0 = kb; k0 < ke; k0 += kKC) {
     {  // x chunk: 32 tokens x 32 k, 4 bf16 per thread
       const int tl = tid >> 3, kq = (tid & 7) * 4, t = t0 + tl;
       float v[4] = {0.f, 0.f, 0.f, 0.f};
@@ -57,14 +61,13 @@ router_topk_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict_
         const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
         v[0] = __low2float(a); v[1] = __high2float(a);
         v[2] = __low2float(b); v[3] = __high2float(b);
-        xmax = fmaxf(xmax, fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3]))));
       }
 #pragma unroll
       for (int c = 0; c < 4; ++c) xs[tl][kq + c] = v[c];
     }
-    for (int idx = tid; idx < E * (kKC / 4); idx += kThreads) {  // W chunk, transposed
+    for (int idx = tid; idx < ne * (kKC / 4); idx += kThreads) {  // W chunk, transposed
       const int e = idx >> 3, kq = (idx & 7) * 4;
-      const float4 w4 = *reinterpret_cast<const float4*>(rw + (size_t)e * d + k0 + kq);
+      const float4 w4 = *reinterpret_cast<const float4*>(rw + (size_t)(e0 + e) * d + k0 + kq);
       wl[(kq + 0) * kLgStride + e] = w4.x;
       wl[(kq + 1) * kLgStride + e] = w4.y;
       wl[(kq + 2) * kLgStride + e] = w4.z;
@@ -86,24 +89,41 @@ router_topk_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict_
     __syncthreads();
   }
 
-  // per-token exponent for holding x in f16: largest |x| scaled into [2^14, 2^15)
-  xmax = fmaxf(xmax, __shfl_xor_sync(0xffffffffu, xmax, 1));
-  xmax = fmaxf(xmax, __shfl_xor_sync(0xffffffffu, xmax, 2));
-  xmax = fmaxf(xmax, __shfl_xor_sync(0xffffffffu, xmax, 4));
-  if ((tid & 7) == 0 && t0 + (tid >> 3) < T) {
-    const int et = (xmax > 0.f && isfinite(xmax)) ? 14 - ilogbf(xmax) : 0;
-    xexp[t0 + (tid >> 3)] = max(-126, min(126, et));
-  }
-
-  // logits (+ bias) into shared memory, row per token
+  // this K range's contribution to the logits of the tile's tokens
 #pragma unroll
-  for (int j = 0; j < NPER; ++j) {
-    const int e = lane + 32 * j;
-    if (e < E) {
-      const float b = rb[e];
+  for (int i = 0; i < 4; ++i) {
+    const int t = t0 + warp * 4 + i;
+    if (t >= T) break;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) wl[(warp * 4 + i) * kLgStride + e] = acc[i][j] + b;
+    for (int j = 0; j < NPER; ++j) {
+      const int e = lane + 32 * j;
+      if (e < ne) part[((size_t)ks * T + t) * E + e0 + e] = acc[i][j];
     }
+  }
+}
+
+template <int NPER>
+__global__ void __launch_bounds__(kThreads)
+router_topk_kernel(const float* __restrict__ part, int nks, const float* __restrict__ rb, int T,
+                   int E, int k, int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
+                   int32_t* __restrict__ rank, int32_t* __restrict__ tile_counts) {
+  __shared__ float wl[kTT * kLgStride];  // logits [t][e]
+  __shared__ uint32_t mask[kMaxE];       // bit t: token t of this tile picked e
+  __shared__ int32_t sel[kTT][8];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int t0 = blockIdx.x * kTT;
+  const int ntok = min(kTT, T - t0);
+  for (int e = tid; e < kMaxE; e += kThreads) mask[e] = 0u;
+  pdl_wait();
+
+  // logits = the K-range partial sums in a fixed order, then the bias
+  for (int idx = tid; idx < ntok * E; idx += kThreads) {
+    const int tl = idx / E, e = idx - tl * E;
+    float v = 0.f;
+#pragma unroll 4
+    for (int s = 0; s < nks; ++s) v += part[((size_t)s * T + t0 + tl) * E + e];
+    wl[tl * kLgStride + e] = v + rb[e];
   }
   __syncthreads();
 
@@ -163,7 +183,6 @@ router_topk_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict_
   }
   __syncthreads();
 
-  const int ntok = min(kTT, T - t0);
   for (int e = tid; e < E; e += kThreads)
     tile_counts[(size_t)blockIdx.x * E + e] = __popc(mask[e]);
   for (int q = tid; q < ntok * k; q += kThreads) {
@@ -177,31 +196,52 @@ router_topk_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict_
 
 cudaError_t launch_router_topk(const __nv_bfloat16* x, const float* router_w,
                                const float* router_b, int T, int d, int E, int k,
-                               int32_t* topk_idx, float* topk_w, int32_t* rank,
-                               int32_t* tile_counts, int32_t* xexp, int32_t* status,
+                               float* logit_part, int32_t* topk_idx, float* topk_w,
+                               int32_t* rank, int32_t* tile_counts, int32_t* status,
                                cudaStream_t s) {
-  const int grid = (T + kTT - 1) / kTT;
-  const int nper = (E + 31) / 32;
-#define MOE_ROUTER_CASE(N)                                                          \
-  case N:                                                                           \
-    router_topk_kernel<N><<<grid, kThreads, 0, s>>>(x, router_w, router_b, T, d, E, \
-                                                    k, topk_idx, topk_w, rank,      \
-                                                    tile_counts, xexp, status);     \
+  const int ntiles = (T + kTT - 1) / kTT;
+  const int nks = router_splits(T, d, E);
+  const int kc = router_split_len(T, d, E);
+  const int eg = router_expert_group(T, E);
+  const dim3 g1(ntiles, nks, (E + eg - 1) / eg);
+  const int nper_g = eg / 32;                    // experts per lane in the logits kernel
+  const int nper = (E + 31) / 32;                // ... and in the top-k kernel
+  if (nper_g < 1 || nper_g > 8 || nper > 8) return cudaErrorInvalidValue;
+  cudaError_t e = cudaSuccess;
+#define MOE_LOGITS_CASE(N)                                                                   \
+  case N:                                                                                    \
+    e = launch_pdl(router_logits_kernel<N>, g1, dim3(kThreads), 0, s, x, router_w, T, d, E,   \
+                   kc, eg, logit_part, status);                                              \
+    break;
+  switch (nper_g) {
+    MOE_LOGITS_CASE(1)
+    MOE_LOGITS_CASE(2)
+    MOE_LOGITS_CASE(3)
+    MOE_LOGITS_CASE(4)
+    MOE_LOGITS_CASE(5)
+    MOE_LOGITS_CASE(6)
+    MOE_LOGITS_CASE(7)
+    MOE_LOGITS_CASE(8)
+  }
+#undef MOE_LOGITS_CASE
+  if (e != cudaSuccess) return e;
+#define MOE_TOPK_CASE(N)                                                                     \
+  case N:                                                                                    \
+    e = launch_pdl(router_topk_kernel<N>, dim3(ntiles), dim3(kThreads), 0, s, logit_part,    \
+                   nks, router_b, T, E, k, topk_idx, topk_w, rank, tile_counts);             \
     break;
   switch (nper) {
-    MOE_ROUTER_CASE(1)
-    MOE_ROUTER_CASE(2)
-    MOE_ROUTER_CASE(3)
-    MOE_ROUTER_CASE(4)
-    MOE_ROUTER_CASE(5)
-    MOE_ROUTER_CASE(6)
-    MOE_ROUTER_CASE(7)
-    MOE_ROUTER_CASE(8)
-    default:
-      return cudaErrorInvalidValue;
+    MOE_TOPK_CASE(1)
+    MOE_TOPK_CASE(2)
+    MOE_TOPK_CASE(3)
+    MOE_TOPK_CASE(4)
+    MOE_TOPK_CASE(5)
+    MOE_TOPK_CASE(6)
+    MOE_TOPK_CASE(7)
+    MOE_TOPK_CASE(8)
   }
-#undef MOE_ROUTER_CASE
-  return cudaGetLastError();
+#undef MOE_TOPK_CASE
+  return e;
 }
 
 }  // namespace moe

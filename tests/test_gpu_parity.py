@@ -202,3 +202,28 @@ def test_zero_tokens_is_a_no_op():
                     sentinel, dev.workspace, 0)
     torch.cuda.synchronize()
     assert torch.all(sentinel == 3.0)
+
+
+# ------------------------------------------- the other grouped-GEMM design --
+
+@pytest.mark.parametrize("name", ["T1", "ragged77", "d96_w160", "E256", "k8"])
+def test_edge_shapes_smem_staged_gemm(name, monkeypatch):
+    """MOE_GEMM=smem runs K3/K4 with the dequantised weights staged in shared
+    memory (tokens as the MMA M side) instead of tensor memory; it must meet
+    the same bar."""
+    monkeypatch.setenv("MOE_GEMM", "smem")
+    inp = gen.make_inputs(EDGE[name])
+    dev, out, ref = _run(inp)
+    _check_full(dev, out, ref, EDGE[name].k)
+
+
+def test_both_gemm_designs_agree_on_decode(monkeypatch):
+    """The two designs round differently only in fp32 summation order, so on
+    the 20b decode layer they agree to well inside the oracle tolerance."""
+    inp = gen.make_inputs(gen.WORKLOADS["gptoss20b_decode"])
+    dev = DeviceMoE.upload(inp)
+    a = bf16_to_f64(dev.forward().clone())
+    monkeypatch.setenv("MOE_GEMM", "smem")
+    b = bf16_to_f64(dev.forward().clone())
+    moe.moe_poll_status(dev.workspace)
+    parity.check_output(a, b, what="tmem vs smem design")
