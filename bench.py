@@ -42,7 +42,7 @@ STAGES = ["router_topk", "route_scan", "route_scatter", "gate_up", "down", "comb
 KERNELS_PER_STEP = 7
 KERNEL_SOURCES = {
     "router_topk": "router_topk.cu", "route_scan": "permute.cu", "route_scatter": "permute.cu",
-    "gate_up": "grouped_gemm_tc.cu", "down": "grouped_gemm_tc.cu", "combine": "combine.cu",
+    "gate_up": "expert_gemm_tmem.cu", "down": "expert_gemm_tmem.cu", "combine": "combine.cu",
 }
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 

@@ -22,7 +22,7 @@
 //   warp 1      MMA issuer (one elected thread)
 //   warp 2      TMEM allocator (512 columns: 2 accumulator buffers of 128,
 //               each 128/nb accumulators of nb columns; 4 A stages of 64)
-//   warp 3      producer: activations (TMA)
+//   warp 3      producer: activations (TMA, one nb-row box per operand and stage)
 //   warps 4-7   epilogue, TMEM lane quarter = warp % 4
 //   warps 8-15  dequantisers, lane quarter = warp % 4, K half = (warp - 8) / 4
 // Work unit = (token chunk of one expert, weight M tile), chunk-major so a
@@ -67,7 +67,6 @@ constexpr int kACol0 = 2 * kNBMax;           // first A-stage column
 constexpr int kACols = kAK / 2;              // columns per A stage
 constexpr int kCodeStageBytes = kMW * kCK / 2;   // 16 KB
 constexpr int kCodeBoxRows = 64;
-constexpr int kBox = 16;                     // rows per activation TMA box
 // code, A and B rings (full + empty each), scales and accumulators (2 + 2
 // each), the row-factor ring, and the final MMA drain
 constexpr int kNumBars = 2 * kMaxC + 2 * kAStages + 2 * kMaxB + 4 + 4 + 2 * kRing + 1;
@@ -452,17 +451,15 @@ moe_expert_gemm_tmem(const __grid_constant__ CUtensorMap map_w,
       bool ok = true;
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
         const Unit w = unit_of(a, n_mt, u);
-        const int nt = (w.n + kBox - 1) / kBox;      // 16-row boxes
         for (int jb = 0; jb < nKB; ++jb) {
           if (!wait_phase(&b_empty[br.slot], br.phase ^ 1, abort_flag, a.status)) { ok = false; break; }
-          ptx::mbar_arrive_expect_tx(&b_full[br.slot], uint32_t(NOPS * nt * kBox * 128));
+          // one box of nb rows per operand (rows past the chunk are other
+          // experts' tokens or zero fill, and only feed accumulator columns the
+          // epilogue ignores)
+          ptx::mbar_arrive_expect_tx(&b_full[br.slot], uint32_t(NOPS * a.nb * 128));
           uint8_t* bdst = bt + br.slot * L.bstage;
-          for (int op = 0; op < NOPS; ++op) {
-            const CUtensorMap* mp = op == 0 ? &map_b0 : &map_b1;
-            for (int g = 0; g < nt; ++g)
-              ptx::tma_load_2d(bdst + op * a.nb * 128 + g * kBox * 128, mp, &b_full[br.slot],
-                               jb * kBK, w.r0 + kBox * g);
-          }
+          ptx::tma_load_2d(bdst, &map_b0, &b_full[br.slot], jb * kBK, w.r0);
+          if (NOPS > 1) ptx::tma_load_2d(bdst + a.nb * 128, &map_b1, &b_full[br.slot], jb * kBK, w.r0);
           b_in.mark(br.slot, br.phase);
           br.next(NBS);
         }
@@ -483,26 +480,35 @@ moe_expert_gemm_tmem(const __grid_constant__ CUtensorMap map_w,
         if (!wait_phase(&acc_empty[buf], ((q >> 1) & 1) ^ 1, abort_flag, a.status)) { ok = false; break; }
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + buf * kNBMax;
-        int step = 0;                                // K16 step of the unit
+        // This single thread's instruction stream sets the pace for short
+        // MMAs, so the loop keeps per-MMA work to a few adds: descriptors are
+        // built once per stage, the K16 loop is unrolled, and the accumulator
+        // rotates by increment-and-reset.
+        uint32_t acc_addr = d_tmem;
+        int acc_i = 0, steps_left_init = nacc;       // first pass over each accumulator
         for (int ja = 0; ja < nA && ok; ++ja) {
           if (!wait_phase(&a_full[ar.slot], ar.phase, abort_flag, a.status)) { ok = false; break; }
-          const uint32_t a_tmem = tmem_base + kACol0 + ar.slot * kACols;
+          const uint32_t a_stage = tmem_base + kACol0 + ar.slot * kACols;
+#pragma unroll
           for (int h = 0; h < 2; ++h) {
             const int jb = ja * 2 + h;
             if (jb >= nKB) break;
             if (!wait_phase(&b_full[br.slot], br.phase, abort_flag, a.status)) { ok = false; break; }
             ptx::tc_fence_after();
-            uint8_t* bst = bt + br.slot * L.bstage;
-            for (int kk = 0; kk < kBK / 16; ++kk, ++step) {
-              if (jb * kBK + kk * 16 >= K) break;
-              // K16 steps rotate over nacc independent accumulators
-              const uint32_t acc = d_tmem + (step % nacc) * a.nb;
+            const uint32_t bsm = ptx::smem_u32(bt + br.slot * L.bstage);
+            const uint64_t bdesc0 = ptx::desc_kmajor_sw128(bsm);
+            const uint64_t bdesc1 = ptx::desc_kmajor_sw128(bsm + uint32_t(a.nb * 128));
+            const int nk = min(kBK / 16, (K - jb * kBK) / 16);   // 2 or 4 (K % 32 == 0)
+            const uint32_t a_half = a_stage + h * 32;
 #pragma unroll
-              for (int op = 0; op < NOPS; ++op) {
-                const uint64_t bdesc =
-                    ptx::desc_kmajor_sw128(ptx::smem_u32(bst + op * a.nb * 128)) + 2 * kk;
-                ptx::mma_f16_tmem_a(acc, a_tmem + (h * 4 + kk) * 8, bdesc, idesc,
-                                    (step >= nacc || op != 0) ? 1u : 0u);
+            for (int kk = 0; kk < kBK / 16; ++kk) {
+              if (kk < nk) {
+                const uint32_t accumulate = steps_left_init > 0 ? 0u : 1u;
+                ptx::mma_f16_tmem_a(acc_addr, a_half + kk * 8, bdesc0 + 2 * kk, idesc, accumulate);
+                if (NOPS > 1) ptx::mma_f16_tmem_a(acc_addr, a_half + kk * 8, bdesc1 + 2 * kk, idesc, 1u);
+                if (steps_left_init > 0) --steps_left_init;
+                acc_addr += a.nb;
+                if (++acc_i == nacc) { acc_i = 0; acc_addr = d_tmem; }
               }
             }
             ptx::mma_commit(&b_empty[br.slot]);
@@ -787,15 +793,15 @@ cudaError_t launch(const GemmArgs& args, cudaStream_t s) {
     e = make_map(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.w_gu, (long long)a.E * 2 * a.W, a.d / 2,
                  kCK / 2, kCodeBoxRows);
     if (e == cudaSuccess)
-      e = make_map(&m0, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.x_perm, a.R, a.d, kBK, kBox);
+      e = make_map(&m0, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.x_perm, a.R, a.d, kBK, a.nb);
     m1 = m0;
   } else {
     e = make_map(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.w_dn, (long long)a.E * a.d, a.W / 2,
                  kCK / 2, kCodeBoxRows);
     if (e == cudaSuccess)
-      e = make_map(&m0, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.h_hi, a.R, a.W, kBK, kBox);
+      e = make_map(&m0, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.h_hi, a.R, a.W, kBK, a.nb);
     if (e == cudaSuccess)
-      e = make_map(&m1, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.h_lo, a.R, a.W, kBK, kBox);
+      e = make_map(&m1, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.h_lo, a.R, a.W, kBK, a.nb);
   }
   if (e != cudaSuccess) return e;
   const int n_out = (M == Mode::GateUp) ? a.W : a.d;
