@@ -52,26 +52,33 @@ namespace {
 
 constexpr int kNBMax = kGemmBM;              // largest token chunk (MMA N)
 constexpr int kMW = 128;                     // weight rows per unit (MMA M, TMEM lanes)
-constexpr int kCK = 256;                     // K per code stage: 128 B of codes per row
-constexpr int kAK = 128;                     // K per A stage: 64 TMEM columns
-constexpr int kBK = 64;                      // K per activation stage (one 128-byte row)
+constexpr int kSK = 256;                     // K per stage: 128 B of codes per row, 128 TMEM columns of A
+constexpr int kACols = kSK / 2;              // TMEM columns per A stage
 constexpr int kMaxC = 8;                     // code-ring depth, most
-constexpr int kAStages = 4;
+constexpr int kMaxA = 3;                     // A-ring depth, most
 constexpr int kMaxB = 16;                    // activation-ring depth, most
 constexpr int kRing = 4;                     // per-unit row-factor ring
 constexpr int kThreads = 512;
 constexpr int kWarpProd = 0, kWarpMMA = 1, kWarpTmem = 2, kWarpProdB = 3, kWarpEpi0 = 4,
               kWarpDq0 = 8;
 constexpr int kTmemCols = 512;
-constexpr int kACol0 = 2 * kNBMax;           // first A-stage column
-constexpr int kACols = kAK / 2;              // columns per A stage
-constexpr int kCodeStageBytes = kMW * kCK / 2;   // 16 KB
+constexpr int kCodeStageBytes = kMW * kSK / 2;   // 16 KB
 constexpr int kCodeBoxRows = 64;
 // code, A and B rings (full + empty each), scales and accumulators (2 + 2
 // each), the row-factor ring, and the final MMA drain
-constexpr int kNumBars = 2 * kMaxC + 2 * kAStages + 2 * kMaxB + 4 + 4 + 2 * kRing + 1;
+constexpr int kNumBars = 2 * kMaxC + 2 * kMaxA + 2 * kMaxB + 4 + 4 + 2 * kRing + 1;
 constexpr long long kSpinLimit = 4000000000ll;   // clock cycles before a wait gives up
 constexpr int kMaxSmem = 232448;                 // 227 KB opt-in per CTA
+
+// K of one activation stage: 256 for small chunks (a stage is a few KB and
+// one wait covers a whole A stage), 64 for large ones (a stage of 128 tokens x
+// 256 K would not leave room for a ring).
+__host__ __device__ inline int act_stage_k(int nb) { return nb <= 32 ? 256 : 64; }
+// A stages that fit in TMEM next to two accumulators of nb columns.
+__host__ __device__ inline int a_stages(int nb) {
+  const int n = (kTmemCols - 2 * nb) / kACols;
+  return n < kMaxA ? n : kMaxA;
+}
 
 enum class Mode { GateUp, Down };
 
@@ -100,7 +107,7 @@ __host__ __device__ inline Lay layout(int nsb, int nb, int nc, int nbs) {
   int off = 0;
   l.codes = off;
   off += nc * kCodeStageBytes;
-  l.bstage = Cfg<M>::NOPS * nb * 128;
+  l.bstage = Cfg<M>::NOPS * (act_stage_k(nb) / 64) * nb * 128;
   l.bt = off;
   off += nbs * l.bstage;
   l.scbuf = (kMW * nsb + 15) / 16 * 16;
@@ -278,22 +285,6 @@ __device__ __forceinline__ int row_max_byte(const uint32_t* buf, uint32_t base, 
   return int(m & 0xFF);
 }
 
-// 16 columns of the unit's result for this warp's 32 lanes: the sum of the
-// nacc accumulators (stride nb columns), added in a fixed order.
-__device__ __forceinline__ void sum_accumulators(uint32_t taddr, int nb, int nacc, float (&acc)[16]) {
-  uint32_t v[16];
-  ptx::tmem_ld_32x32b_x16(taddr, v);
-  ptx::tmem_ld_wait();
-#pragma unroll
-  for (int j = 0; j < 16; ++j) acc[j] = __uint_as_float(v[j]);
-  for (int i = 1; i < nacc; ++i) {
-    ptx::tmem_ld_32x32b_x16(taddr + i * nb, v);
-    ptx::tmem_ld_wait();
-#pragma unroll
-    for (int j = 0; j < 16; ++j) acc[j] += __uint_as_float(v[j]);
-  }
-}
-
 // ------------------------------------------------------------- kernel --
 
 template <Mode M>
@@ -307,21 +298,16 @@ moe_expert_gemm_tmem(const __grid_constant__ CUtensorMap map_w,
 
   const int K = kGateUp ? a.d : a.W;                 // reduction length
   const int nsb = K / 32;                            // scale bytes per weight row
-  const int nA = (K + kAK - 1) / kAK;                // A stages per unit
-  const int nC = (K + kCK - 1) / kCK;                // code stages per unit
-  const int nKB = (K + kBK - 1) / kBK;               // activation stages per unit
+  const int nS = (K + kSK - 1) / kSK;                // stages (code = A) per unit
+  const int bk = act_stage_k(a.nb);                  // K per activation stage
+  const int nKB = (K + bk - 1) / bk;                 // activation stages per unit
   const int rpe = kGateUp ? 2 * a.W : a.d;           // weight rows per expert
   const int n_out = kGateUp ? a.W : a.d;
   const int rows_per_tile = kGateUp ? kMW / 2 : kMW; // output features per unit
   const int n_mt = (n_out + rows_per_tile - 1) / rows_per_tile;
   const int NC = a.stages_c, NBS = a.stages_b;
-  // Independent accumulators per unit: an accumulator buffer is kNBMax columns
-  // and a chunk needs nb, so a small chunk spreads the K16 steps over several
-  // accumulators (MMAs into one accumulator wait for each other; a decode-sized
-  // N = 16 MMA is short, so one chain would leave the tensor pipe idle).
-  const int nacc_max = kNBMax / a.nb;
-  const int nk16 = (K + 15) / 16;
-  const int nacc = nacc_max < nk16 ? nacc_max : nk16;
+  const int NAS = a_stages(a.nb);
+  const int a_col0 = 2 * a.nb;                       // TMEM: accumulators first, then A
   const Lay L = layout<M>(nsb, a.nb, NC, NBS);
 
   extern __shared__ uint8_t smem_raw[];
@@ -334,8 +320,8 @@ moe_expert_gemm_tmem(const __grid_constant__ CUtensorMap map_w,
   uint64_t* code_full = bars;
   uint64_t* code_empty = code_full + kMaxC;
   uint64_t* a_full = code_empty + kMaxC;
-  uint64_t* a_empty = a_full + kAStages;
-  uint64_t* b_full = a_empty + kAStages;
+  uint64_t* a_empty = a_full + kMaxA;
+  uint64_t* b_full = a_empty + kMaxA;
   uint64_t* b_empty = b_full + kMaxB;
   uint64_t* sc_full = b_empty + kMaxB;
   uint64_t* sc_empty = sc_full + 2;
@@ -354,7 +340,7 @@ moe_expert_gemm_tmem(const __grid_constant__ CUtensorMap map_w,
       ptx::mbar_init(&code_full[s], 1);
       ptx::mbar_init(&code_empty[s], 8);
     }
-    for (int s = 0; s < kAStages; ++s) {
+    for (int s = 0; s < kMaxA; ++s) {
       ptx::mbar_init(&a_full[s], 8);
       ptx::mbar_init(&a_empty[s], 1);
     }
@@ -426,12 +412,12 @@ moe_expert_gemm_tmem(const __grid_constant__ CUtensorMap map_w,
           ptx::bulk_load(scb + sb * L.scbuf, wscale + size_t(row_a) * nsb, bytes, &sc_full[sb]);
         }
         s_in.mark(sb, (q >> 1) & 1);
-        for (int cs = 0; cs < nC; ++cs) {
+        for (int cs = 0; cs < nS; ++cs) {
           if (!wait_phase(&code_empty[cr.slot], cr.phase ^ 1, abort_flag, a.status)) { ok = false; break; }
           uint8_t* cdst = codes + cr.slot * kCodeStageBytes;
           ptx::mbar_arrive_expect_tx(&code_full[cr.slot], kCodeStageBytes);
-          ptx::tma_load_2d(cdst, &map_w, &code_full[cr.slot], cs * (kCK / 2), row_a);
-          ptx::tma_load_2d(cdst + kCodeStageBytes / 2, &map_w, &code_full[cr.slot], cs * (kCK / 2), row_b);
+          ptx::tma_load_2d(cdst, &map_w, &code_full[cr.slot], cs * (kSK / 2), row_a);
+          ptx::tma_load_2d(cdst + kCodeStageBytes / 2, &map_w, &code_full[cr.slot], cs * (kSK / 2), row_b);
           c_in.mark(cr.slot, cr.phase);
           cr.next(NC);
         }
@@ -449,17 +435,25 @@ moe_expert_gemm_tmem(const __grid_constant__ CUtensorMap map_w,
       Ring br;
       Inflight b_in;
       bool ok = true;
+      const int subs_per_stage = bk / 64;
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
         const Unit w = unit_of(a, n_mt, u);
         for (int jb = 0; jb < nKB; ++jb) {
           if (!wait_phase(&b_empty[br.slot], br.phase ^ 1, abort_flag, a.status)) { ok = false; break; }
-          // one box of nb rows per operand (rows past the chunk are other
-          // experts' tokens or zero fill, and only feed accumulator columns the
-          // epilogue ignores)
-          ptx::mbar_arrive_expect_tx(&b_full[br.slot], uint32_t(NOPS * a.nb * 128));
+          // one box of nb rows x 64 K per sub-tile and operand (rows past the
+          // chunk are other experts' tokens or zero fill, and only feed
+          // accumulator columns the epilogue ignores); sub-tiles past K are
+          // not loaded and not read
+          const int k0 = jb * bk;
+          const int subs = min(subs_per_stage, (K - k0 + 63) / 64);
+          ptx::mbar_arrive_expect_tx(&b_full[br.slot], uint32_t(NOPS * subs * a.nb * 128));
           uint8_t* bdst = bt + br.slot * L.bstage;
-          ptx::tma_load_2d(bdst, &map_b0, &b_full[br.slot], jb * kBK, w.r0);
-          if (NOPS > 1) ptx::tma_load_2d(bdst + a.nb * 128, &map_b1, &b_full[br.slot], jb * kBK, w.r0);
+          for (int sb2 = 0; sb2 < subs; ++sb2) {
+            ptx::tma_load_2d(bdst + (sb2 * NOPS) * a.nb * 128, &map_b0, &b_full[br.slot], k0 + 64 * sb2, w.r0);
+            if (NOPS > 1)
+              ptx::tma_load_2d(bdst + (sb2 * NOPS + 1) * a.nb * 128, &map_b1, &b_full[br.slot],
+                               k0 + 64 * sb2, w.r0);
+          }
           b_in.mark(br.slot, br.phase);
           br.next(NBS);
         }
@@ -468,6 +462,9 @@ moe_expert_gemm_tmem(const __grid_constant__ CUtensorMap map_w,
     }
   } else if (warp == kWarpMMA) {
     // ------------------------------------------------------------ MMA issuer --
+    // One thread's instruction stream sets the pace for short MMAs, so the
+    // loop keeps per-MMA work to a few adds: descriptors are built once per
+    // activation stage and the K16 loop is unrolled.
     if (ptx::elect_one()) {
       Ring ar, br;
       bool ok = true;
@@ -479,36 +476,31 @@ moe_expert_gemm_tmem(const __grid_constant__ CUtensorMap map_w,
         const int buf = q & 1;
         if (!wait_phase(&acc_empty[buf], ((q >> 1) & 1) ^ 1, abort_flag, a.status)) { ok = false; break; }
         ptx::tc_fence_after();
-        const uint32_t d_tmem = tmem_base + buf * kNBMax;
-        // This single thread's instruction stream sets the pace for short
-        // MMAs, so the loop keeps per-MMA work to a few adds: descriptors are
-        // built once per stage, the K16 loop is unrolled, and the accumulator
-        // rotates by increment-and-reset.
-        uint32_t acc_addr = d_tmem;
-        int acc_i = 0, steps_left_init = nacc;       // first pass over each accumulator
-        for (int ja = 0; ja < nA && ok; ++ja) {
+        const uint32_t d_tmem = tmem_base + buf * a.nb;
+        uint32_t accumulate = 0;
+        int jb = 0;                                  // activation stage of the unit
+        for (int ja = 0; ja < nS && ok; ++ja) {
           if (!wait_phase(&a_full[ar.slot], ar.phase, abort_flag, a.status)) { ok = false; break; }
-          const uint32_t a_stage = tmem_base + kACol0 + ar.slot * kACols;
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int jb = ja * 2 + h;
-            if (jb >= nKB) break;
+          const uint32_t a_stage = tmem_base + a_col0 + ar.slot * kACols;
+          // the activation stages inside this A stage
+          for (int kb = ja * kSK; kb < min(K, (ja + 1) * kSK); kb += bk, ++jb) {
             if (!wait_phase(&b_full[br.slot], br.phase, abort_flag, a.status)) { ok = false; break; }
             ptx::tc_fence_after();
             const uint32_t bsm = ptx::smem_u32(bt + br.slot * L.bstage);
-            const uint64_t bdesc0 = ptx::desc_kmajor_sw128(bsm);
-            const uint64_t bdesc1 = ptx::desc_kmajor_sw128(bsm + uint32_t(a.nb * 128));
-            const int nk = min(kBK / 16, (K - jb * kBK) / 16);   // 2 or 4 (K % 32 == 0)
-            const uint32_t a_half = a_stage + h * 32;
+            const int nk = min(bk, K - kb) / 16;         // K16 steps in this stage
+            const uint32_t a_cols = a_stage + (kb - ja * kSK) / 2;
+            for (int kk0 = 0; kk0 < nk; kk0 += 4) {      // one 64-K sub-tile at a time
+              const uint32_t sub = bsm + uint32_t((kk0 / 4) * NOPS * a.nb * 128);
+              const uint64_t bdesc0 = ptx::desc_kmajor_sw128(sub);
+              const uint64_t bdesc1 = ptx::desc_kmajor_sw128(sub + uint32_t(a.nb * 128));
+              const int n4 = min(4, nk - kk0);           // 2 or 4 (K % 32 == 0)
 #pragma unroll
-            for (int kk = 0; kk < kBK / 16; ++kk) {
-              if (kk < nk) {
-                const uint32_t accumulate = steps_left_init > 0 ? 0u : 1u;
-                ptx::mma_f16_tmem_a(acc_addr, a_half + kk * 8, bdesc0 + 2 * kk, idesc, accumulate);
-                if (NOPS > 1) ptx::mma_f16_tmem_a(acc_addr, a_half + kk * 8, bdesc1 + 2 * kk, idesc, 1u);
-                if (steps_left_init > 0) --steps_left_init;
-                acc_addr += a.nb;
-                if (++acc_i == nacc) { acc_i = 0; acc_addr = d_tmem; }
+              for (int kk = 0; kk < 4; ++kk) {
+                if (kk < n4) {
+                  ptx::mma_f16_tmem_a(d_tmem, a_cols + (kk0 + kk) * 8, bdesc0 + 2 * kk, idesc, accumulate);
+                  if (NOPS > 1) ptx::mma_f16_tmem_a(d_tmem, a_cols + (kk0 + kk) * 8, bdesc1 + 2 * kk, idesc, 1u);
+                  accumulate = 1u;
+                }
               }
             }
             ptx::mma_commit(&b_empty[br.slot]);
@@ -516,7 +508,7 @@ moe_expert_gemm_tmem(const __grid_constant__ CUtensorMap map_w,
           }
           if (!ok) break;
           ptx::mma_commit(&a_empty[ar.slot]);
-          ar.next(kAStages);
+          ar.next(NAS);
         }
         if (!ok) break;
         ptx::mma_commit(&acc_full[buf]);
@@ -542,7 +534,7 @@ moe_expert_gemm_tmem(const __grid_constant__ CUtensorMap map_w,
       const float rowf = rf[ring * kMW + Ln];
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&rf_empty[ring]);
-      const uint32_t taddr = tmem_base + (uint32_t(quarter * 32) << 16) + buf * kNBMax;
+      const uint32_t taddr = tmem_base + (uint32_t(quarter * 32) << 16) + buf * a.nb;
       if constexpr (kGateUp) {
         const bool is_up = Ln & 1;
         const int n = w.mt * (kMW / 2) + (Ln >> 1);
@@ -550,14 +542,15 @@ moe_expert_gemm_tmem(const __grid_constant__ CUtensorMap map_w,
         const float bias =
             nvalid ? __bfloat162float(a.b_gu[size_t(w.e) * 2 * a.W + (is_up ? a.W : 0) + n]) : 0.f;
         for (int c = 0; c < w.n; c += 16) {
-          float acc[16];
-          sum_accumulators(taddr + c, a.nb, nacc, acc);
+          uint32_t v[16];
+          ptx::tmem_ld_32x32b_x16(taddr + c, v);
+          ptx::tmem_ld_wait();
           float z[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int col = c + j;
             const float colf = col < w.n ? __int_as_float((127 - __ldg(a.rowexp + w.r0 + col)) << 23) : 0.f;
-            z[j] = acc[j] * rowf * colf + bias;
+            z[j] = __uint_as_float(v[j]) * rowf * colf + bias;
           }
           // gate lanes are even, up lanes odd: the even lane finishes tokens
           // c..c+7, the odd lane tokens c+8..c+15
@@ -585,12 +578,13 @@ moe_expert_gemm_tmem(const __grid_constant__ CUtensorMap map_w,
         const bool nvalid = n < a.d;
         const float bias = nvalid ? __bfloat162float(a.b_dn[size_t(w.e) * a.d + n]) : 0.f;
         for (int c = 0; c < w.n; c += 16) {
-          float acc[16];
-          sum_accumulators(taddr + c, a.nb, nacc, acc);
+          uint32_t v[16];
+          ptx::tmem_ld_32x32b_x16(taddr + c, v);
+          ptx::tmem_ld_wait();
           if (nvalid) {
 #pragma unroll
             for (int j = 0; j < 16; ++j)
-              if (c + j < w.n) a.y[size_t(w.r0 + c + j) * a.d + n] = acc[j] * rowf + bias;
+              if (c + j < w.n) a.y[size_t(w.r0 + c + j) * a.d + n] = __uint_as_float(v[j]) * rowf + bias;
           }
         }
       }
@@ -600,60 +594,17 @@ moe_expert_gemm_tmem(const __grid_constant__ CUtensorMap map_w,
     }
   } else if (warp >= kWarpDq0) {
     // --------------------------------------------------------- dequantisers --
-    // Software-pipelined: the tcgen05.st of A stage j drains while stage j+1
-    // is converted (two register buffers); stage j is handed to the MMA
-    // (tcgen05.wait::st, fence, arrive) just before stage j+1 is stored.
+    // Warp (quarter, hf) converts K range [hf*128, hf*128+128) of every 256-K
+    // stage for its 32 weight rows: 128 codes -> 64 TMEM columns, one
+    // tcgen05.st.  The two warps of a lane quarter share the SM partition, so
+    // one converts while the other's store drains.
     const int quarter = warp & 3;
-    const int hf = (warp - kWarpDq0) >> 2;       // K half of every A stage
+    const int hf = (warp - kWarpDq0) >> 2;
     const int Ln = quarter * 32 + lane;          // TMEM lane = weight row of the tile
     const int sr = kGateUp ? ((Ln & 1) ? kMW / 2 + (Ln >> 1) : (Ln >> 1)) : Ln;   // smem row
     const uint32_t lane_addr = uint32_t(quarter * 32) << 16;
     Ring cr, ar;
-    int pending = -1;                            // A slot stored but not yet handed over
     bool ok = true;
-    uint32_t r0[32], r1[32];
-
-    // Convert this thread's 64 codes of A stage ja (code stage in `cst`) into r.
-    auto convert = [&](const uint8_t* cst, const uint8_t* srow, bool valid, int rn, int ja,
-                       uint32_t (&r)[32]) {
-      const int b0 = (ja * kAK + hf * 64) / 32;  // first of the two scale blocks
-      uint32_t s01 = 0;
-      if (valid && b0 < nsb) {
-        // one 16-bit read when the row's byte offset is even (K/32 odd makes
-        // every other row start at an odd offset)
-        const uint8_t* sp = srow + b0;
-        if (b0 + 1 >= nsb) s01 = sp[0];
-        else if ((reinterpret_cast<uintptr_t>(sp) & 1u) == 0) s01 = *reinterpret_cast<const uint16_t*>(sp);
-        else s01 = uint32_t(sp[0]) | (uint32_t(sp[1]) << 8);
-      }
-      const uint32_t f0 = (valid && b0 < nsb) ? Dequant<M>::factor(int(s01 & 0xFF), rn) : 0u;
-      const uint32_t f1 = (valid && b0 + 1 < nsb) ? Dequant<M>::factor(int(s01 >> 8), rn) : 0u;
-      const int ch = (ja & 1) * 4 + hf * 2;      // 16-byte chunk of the 128-byte row
-      const uint4 x0 = *reinterpret_cast<const uint4*>(cst + ptx::sw128_offset(sr, ch));
-      const uint4 x1 = *reinterpret_cast<const uint4*>(cst + ptx::sw128_offset(sr, ch + 1));
-      const uint32_t wv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-#pragma unroll
-      for (int c = 0; c < 8; ++c) Dequant<M>::convert(wv[c], c < 4 ? f0 : f1, &r[4 * c]);
-    };
-    // Hand the pending stage to the MMA once its stores have landed.
-    auto hand_over = [&]() {
-      if (pending < 0) return;
-      ptx::tmem_st_wait();
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&a_full[pending]);
-      pending = -1;
-    };
-    // Store r as A stage slot ar.slot (after the MMA has released it).
-    auto store = [&](const uint32_t (&r)[32]) -> bool {
-      if (!__all_sync(0xffffffffu, wait_phase(&a_empty[ar.slot], ar.phase ^ 1, abort_flag, a.status)))
-        return false;
-      ptx::tmem_st_32x32b_x32(tmem_base + lane_addr + kACol0 + ar.slot * kACols + hf * 32, r);
-      pending = ar.slot;
-      ar.next(kAStages);
-      return true;
-    };
-
     int q = 0;
     for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++q) {
       const Unit w = unit_of(a, n_mt, u);
@@ -672,35 +623,48 @@ moe_expert_gemm_tmem(const __grid_constant__ CUtensorMap map_w,
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&rf_full[ring]);
       }
-      for (int cs = 0; cs < nC && ok; ++cs) {
+      for (int cs = 0; cs < nS; ++cs) {
         ok = __all_sync(0xffffffffu, wait_phase(&code_full[cr.slot], cr.phase, abort_flag, a.status));
         if (!ok) break;
         const uint8_t* cst = codes + cr.slot * kCodeStageBytes;
-        const int ja0 = cs * 2;
-        const bool second = ja0 + 1 < nA;
-        // Each store drains while the next stage converts; a register buffer is
-        // rewritten only after its own store has completed (hand_over waits).
-        convert(cst, srow, valid, rn, ja0, r0);
-        hand_over();                              // the previous code stage's last A stage
-        if (!(ok = store(r0))) break;
-        if (second) convert(cst, srow, valid, rn, ja0 + 1, r1);
-        // the code stage has been read: release it
+        // this thread's 4 scale blocks of the stage
+        const int b0 = cs * (kSK / 32) + hf * 4;
+        uint32_t f[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int b = b0 + i;
+          f[i] = (valid && b < nsb) ? Dequant<M>::factor(int(srow[b]), rn) : 0u;
+        }
+        // 128 codes: 4 x 16 bytes of the 128-byte swizzled row
+        uint4 x[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          x[i] = *reinterpret_cast<const uint4*>(cst + ptx::sw128_offset(sr, hf * 4 + i));
+        // the code stage has been read
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&code_empty[cr.slot]);
         cr.next(NC);
-        if (second) {
-          hand_over();                            // r0
-          if (!(ok = store(r1))) break;           // pending into the next code stage
+        uint32_t r[64];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          Dequant<M>::convert(x[i].x, f[i], &r[16 * i + 0]);
+          Dequant<M>::convert(x[i].y, f[i], &r[16 * i + 4]);
+          Dequant<M>::convert(x[i].z, f[i], &r[16 * i + 8]);
+          Dequant<M>::convert(x[i].w, f[i], &r[16 * i + 12]);
         }
+        ok = __all_sync(0xffffffffu, wait_phase(&a_empty[ar.slot], ar.phase ^ 1, abort_flag, a.status));
+        if (!ok) break;
+        ptx::tmem_st_32x32b_x64(tmem_base + lane_addr + a_col0 + ar.slot * kACols + hf * 64, r);
+        ptx::tmem_st_wait();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&a_full[ar.slot]);
+        ar.next(NAS);
       }
       if (!ok) break;
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&sc_empty[sb]);
     }
-    // the last stage (or, after a failure, whatever was stored) reaches the MMA
-    // or at least completes before TMEM is released
-    if (ok) hand_over();
-    else ptx::tmem_st_wait();
   }
 
   ptx::tc_fence_before();
@@ -763,7 +727,7 @@ void plan(GemmArgs& a) {
   a.stages_c = a.nb <= 32 ? 6 : 3;
   const Lay base = layout<M>(K / 32, a.nb, a.stages_c, 0);
   const int room = kMaxSmem - 1024 - base.total;
-  const int per = Cfg<M>::NOPS * a.nb * 128;
+  const int per = layout<M>(K / 32, a.nb, a.stages_c, 1).bstage;
   a.stages_b = room / per < kMaxB ? room / per : kMaxB;
 }
 
@@ -778,7 +742,8 @@ cudaError_t launch(const GemmArgs& args, cudaStream_t s) {
   GemmArgs a = args;
   plan<M>(a);
   const size_t smem = smem_bytes<M>(a);
-  if (a.stages_b < 2 || smem > size_t(kMaxSmem) || a.nb < 16 || a.nb > kNBMax || a.nb % 16)
+  if (a.stages_b < 2 || smem > size_t(kMaxSmem) || a.nb < 16 || a.nb > kNBMax || a.nb % 16 ||
+      a_stages(a.nb) < 2)
     return cudaErrorInvalidConfiguration;
   static bool configured = false;
   if (!configured) {
@@ -791,17 +756,17 @@ cudaError_t launch(const GemmArgs& args, cudaStream_t s) {
   cudaError_t e;
   if (M == Mode::GateUp) {
     e = make_map(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.w_gu, (long long)a.E * 2 * a.W, a.d / 2,
-                 kCK / 2, kCodeBoxRows);
+                 kSK / 2, kCodeBoxRows);
     if (e == cudaSuccess)
-      e = make_map(&m0, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.x_perm, a.R, a.d, kBK, a.nb);
+      e = make_map(&m0, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.x_perm, a.R, a.d, 64, a.nb);
     m1 = m0;
   } else {
     e = make_map(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.w_dn, (long long)a.E * a.d, a.W / 2,
-                 kCK / 2, kCodeBoxRows);
+                 kSK / 2, kCodeBoxRows);
     if (e == cudaSuccess)
-      e = make_map(&m0, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.h_hi, a.R, a.W, kBK, a.nb);
+      e = make_map(&m0, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.h_hi, a.R, a.W, 64, a.nb);
     if (e == cudaSuccess)
-      e = make_map(&m1, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.h_lo, a.R, a.W, kBK, a.nb);
+      e = make_map(&m1, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.h_lo, a.R, a.W, 64, a.nb);
   }
   if (e != cudaSuccess) return e;
   const int n_out = (M == Mode::GateUp) ? a.W : a.d;
