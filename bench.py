@@ -163,6 +163,28 @@ def kernel_traffic(kernel: str, workload: str):
     return None
 
 
+# ---------------------------------------------------------- replicas --
+
+def max_over_ranks(values, world: int, device="cpu"):
+    """Per-rank timings -> their maximum over all ranks (every rank gets it).
+
+    The layer needs no exchange between GPUs, so N > 1 runs N independent
+    replicas; the job is as fast as its slowest rank.
+    """
+    if world <= 1:
+        return [float(v) for v in values]
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def whole_job_tokens_per_s(tokens_per_rank: int, world: int, ms_slowest: float) -> float:
+    """Tokens of all ranks over the slowest rank's step time (weak scaling)."""
+    return tokens_per_rank * world / (ms_slowest * 1e-3)
+
+
 # ------------------------------------------------------------- CPU arm --
 
 def oracle_sample(inp, n_tokens: int, seed: int = 99):
@@ -321,10 +343,7 @@ def run_ours(args, wl):
     moe.moe_poll_status(dev.workspace)
     e2e = statistics.fmean(e2e_ms)
 
-    if world > 1:
-        t = torch.tensor([ms, e2e], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, e2e = float(t[0]), float(t[1])
+    ms, e2e = max_over_ranks([ms, e2e], world, device="cuda")
 
     if rank != 0:
         if world > 1:
@@ -357,13 +376,14 @@ def run_ours(args, wl):
 
     tokens = wl.T * world
     line = {
-        "metric": METRIC, "value": tokens / (ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
+        "metric": METRIC, "value": whole_job_tokens_per_s(wl.T, world, ms), "unit": "tokens/s",
+        "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded PCG64: x~N(0,1) bf16, random MXFP4 experts)",
         "config": config_block(wl, world),
         "clocks": clk.summary(),
-        "e2e": {"value": tokens / (e2e * 1e-3), "unit": "tokens/s",
+        "e2e": {"value": whole_job_tokens_per_s(wl.T, world, e2e), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(dev.x.numel() * 2),
                 "d2h_bytes_per_step": int(dev.out.numel() * 2)},
         "gpu_launches": KERNELS_PER_STEP * args.steps,

@@ -101,8 +101,11 @@ size_t moe_workspace_bytes(int64_t T, int d, int W, int E, int k);
  *   alpha       sigmoid slope (1.702 for gpt-oss)
  *   out_bf16    [T, d]        bf16, written completely
  * Precision: router logits, softmax and all accumulation in fp32; h is carried
- * between the two GEMMs as a pair of bf16 terms (hi + lo, about 16 significant
- * bits); y is fp32; out is rounded once, to nearest even.
+ * between the two GEMMs as a pair of 16-bit terms, hi + lo: f16 (about 22
+ * significant bits) when the clamp bounds |h| well inside the f16 range
+ * (limit·(limit+1) < 16384, e.g. limit = 7), otherwise bf16 (about 16 bits);
+ * moe_hidden_format says which.  y is fp32; out is rounded once, to nearest
+ * even.
  */
 moe_status moe_forward(const void* x_bf16, int64_t T, int d, int W,
                        const float* router_w, const float* router_b,
@@ -146,13 +149,23 @@ const char* moe_last_error(void);
  * moe_forward (or, for the routing tables, moe_route) on that workspace.
  *   which: 0 topk_idx int32[T,k]   1 topk_w fp32[T,k]     2 offsets int32[E+1]
  *          3 perm int32[T·k]       4 inv int32[T,k]       5 x_perm f16[T·k,d]
- *          6 h_hi bf16[T·k,W]      7 h_lo bf16[T·k,W]     8 y fp32[T·k,d]
+ *          6 h_hi [T·k,W]          7 h_lo [T·k,W]         8 y fp32[T·k,d]
+ * h_hi and h_lo are f16 or bf16 as moe_hidden_format reports.
  * x_perm holds each routed row's token scaled by 2^e_t (e_t puts the token's
  * largest |x| in [2^14, 2^15), so the f16 value is exact).
  * Returns MOE_ERR_SHAPE for an invalid shape or `which`.
  */
 moe_status moe_workspace_region(int64_t T, int d, int W, int E, int k, int which,
                                 size_t* offset, size_t* bytes);
+
+/*
+ * The 16-bit type moe_forward uses for the two terms of h (hi + lo) on this
+ * shape and clamp: *is_f16 = 1 for f16, 0 for bf16.  This only describes the
+ * intermediate tables inside the workspace (for inspection); the results do not
+ * depend on it beyond rounding.  Returns MOE_ERR_SHAPE / MOE_ERR_NULL like the
+ * other calls.  The pages have no counterpart: this is an inspection aid.
+ */
+moe_status moe_hidden_format(int64_t T, int d, int W, int E, int k, float limit, int* is_f16);
 
 /*
  * Tracing aid: make moe_forward calls from the calling thread record CUDA

@@ -130,11 +130,15 @@ inline Workspace workspace_layout(int64_t T, int d, int W, int E, int k) {
 // K1: logits (K-split partial sums, then summed in order with the bias), top-k,
 // selected softmax, per-tile histogram and in-tile ranks.  The first kernel
 // also clears the status word.
+// When T has at most kFuseScanTiles tiles and tile_base is given, the last
+// top-k CTA also runs the expert scan (tile_base, offsets, mtile_off for
+// `chunk`) and *scanned is set; otherwise the caller launches the scan.
 cudaError_t launch_router_topk(const __nv_bfloat16* x, const float* router_w,
                                const float* router_b, int T, int d, int E, int k,
                                float* logit_part, int32_t* topk_idx, float* topk_w,
-                               int32_t* rank, int32_t* tile_counts, int32_t* status,
-                               cudaStream_t s);
+                               int32_t* rank, int32_t* tile_counts, int32_t* status, int chunk,
+                               int32_t* tile_base, int32_t* offsets, int32_t* mtile_off,
+                               bool* scanned, cudaStream_t s);
 
 // K2a: expert offsets, per-(tile, expert) bases, prefix of chunks of `chunk` rows.
 cudaError_t launch_route_scan(const int32_t* tile_counts, int ntiles, int E, int chunk,
@@ -162,6 +166,7 @@ struct GemmArgs {
   const uint8_t* w_gu; const uint8_t* w_gu_scale; const __nv_bfloat16* b_gu;
   const uint8_t* w_dn; const uint8_t* w_dn_scale; const __nv_bfloat16* b_dn;
   float limit, alpha;
+  int h_f16;                  // h carried as an f16 pair (else bf16), TMEM design only
   __nv_bfloat16* h_hi; __nv_bfloat16* h_lo;
   float* y;
   int32_t* status;
@@ -181,6 +186,9 @@ bool expert_gemm_tmem_fits(const GemmArgs& a);
 // chunks (N = 16) when experts get few tokens, so an activation stage is a
 // few KB and the ring can be deep; 128 when they get many.
 int expert_gemm_tmem_chunk(int64_t R, int E);
+// Whether the clamp bounds h well inside the f16 range, so the TMEM design
+// carries h as an f16 pair and runs the down GEMM in f16.
+bool hidden_fits_f16(float limit);
 cudaError_t launch_gateup_tmem(const GemmArgs& a, cudaStream_t s);
 cudaError_t launch_down_tmem(const GemmArgs& a, cudaStream_t s);
 

@@ -17,14 +17,15 @@
 // the activation ring is many small stages deep) and up to 128 when they get
 // many (prefill: experts are cut into 128-token chunks).
 //
-// Persistent kernel, one CTA per SM, 16 warps:
+// Persistent kernel, one CTA per SM, 24 warps:
 //   warp 0      producer: scales (1-D bulk copy) and codes (TMA)
 //   warp 1      MMA issuer (one elected thread)
 //   warp 2      TMEM allocator (512 columns: 2 accumulator buffers of 128,
 //               each 128/nb accumulators of nb columns; 4 A stages of 64)
 //   warp 3      producer: activations (TMA, one nb-row box per operand and stage)
 //   warps 4-7   epilogue, TMEM lane quarter = warp % 4
-//   warps 8-15  dequantisers, lane quarter = warp % 4, K half = (warp - 8) / 4
+//   warps 8-23  dequantisers, lane quarter = warp % 4, K quarter of the stage
+//               = (warp - 8) / 4
 // Work unit = (token chunk of one expert, weight M tile), chunk-major so a
 // chunk's activations and an expert's weights stay in L2 while they are reused.
 //
@@ -45,6 +46,7 @@
 #include <cuda_fp16.h>
 #include <math.h>
 
+#include <cmath>
 #include <mutex>
 
 namespace moe {
@@ -58,9 +60,14 @@ constexpr int kMaxC = 8;                     // code-ring depth, most
 constexpr int kMaxA = 3;                     // A-ring depth, most
 constexpr int kMaxB = 16;                    // activation-ring depth, most
 constexpr int kRing = 4;                     // per-unit row-factor ring
-constexpr int kThreads = 512;
+constexpr int kThreads = 768;
 constexpr int kWarpProd = 0, kWarpMMA = 1, kWarpTmem = 2, kWarpProdB = 3, kWarpEpi0 = 4,
               kWarpDq0 = 8;
+// 16 dequantiser warps: 4 per TMEM lane quarter, each converting a quarter
+// (64 K, 32 columns) of every 256-K stage for its 32 weight rows.  Four warps
+// per SM partition hide the latency of each warp's load -> convert -> store
+// chain, which two could not.
+constexpr int kDqWarps = 16;
 constexpr int kTmemCols = 512;
 constexpr int kCodeStageBytes = kMW * kSK / 2;   // 16 KB
 constexpr int kCodeBoxRows = 64;
@@ -149,12 +156,15 @@ __device__ __forceinline__ Unit unit_of(const GemmArgs& a, int n_mt, int u) {
 
 // Bounded wait: true when the phase completed; false after a timeout (recorded
 // in the status word) or when another thread of the CTA gave up.
+// The thread sleeps inside the wait instruction (woken when the phase
+// completes) and wakes at least every 20 us to check the abort flag and the
+// time limit.
 __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                            int32_t* status) {
-  if (ptx::mbar_try_wait(bar, parity)) return true;
+  if (ptx::mbar_try_wait_sleep(bar, parity, 20000u)) return true;
   const long long t0 = clock64();
   while (true) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (ptx::mbar_try_wait_sleep(bar, parity, 20000u)) return true;
     if (*abort_flag) return false;
     if (clock64() - t0 > kSpinLimit) {
       *abort_flag = 1;
@@ -194,11 +204,12 @@ struct Inflight {
 // ------------------------------------------------------------- dequant --
 
 // 2^delta as an f16x2 pair (delta <= 0); 0 below the f16 subnormal range.
+// Branch-free: lanes of a warp hold different rows' scales.
 __device__ __forceinline__ uint32_t f16x2_pow2(int delta) {
-  uint32_t b;
-  if (delta >= -14) b = uint32_t(delta + 15) << 10;
-  else if (delta >= -24) b = 1u << (delta + 24);
-  else b = 0;
+  const int e = delta + 15;                                   // biased exponent
+  const uint32_t normal = uint32_t(max(e, 0)) << 10;
+  const uint32_t sub = (e <= 0 && e > -10) ? (1u << (e + 9)) : 0u;   // 2^(delta+24) ulps
+  const uint32_t b = e > 0 ? normal : sub;
   return b | (b << 16);
 }
 
@@ -287,14 +298,17 @@ __device__ __forceinline__ int row_max_byte(const uint32_t* buf, uint32_t base, 
 
 // ------------------------------------------------------------- kernel --
 
-template <Mode M>
+// F16: the operands are f16 (weights scaled per row by 2^(s - r_n), gate_up's
+// activations x·2^e_t, down's h as an f16 pair); otherwise bf16 (weights at
+// full scale, h as a bf16 pair), which down uses when h is not bounded.
+template <Mode M, bool F16>
 __global__ void __launch_bounds__(kThreads, 1)
 moe_expert_gemm_tmem(const __grid_constant__ CUtensorMap map_w,
                      const __grid_constant__ CUtensorMap map_b0,
                      const __grid_constant__ CUtensorMap map_b1, const GemmArgs a) {
-  using C = Cfg<M>;
-  constexpr int NOPS = C::NOPS;
+  constexpr int NOPS = Cfg<M>::NOPS;
   constexpr bool kGateUp = (M == Mode::GateUp);
+  constexpr Mode DQ = F16 ? Mode::GateUp : Mode::Down;   // dequantiser format
 
   const int K = kGateUp ? a.d : a.W;                 // reduction length
   const int nsb = K / 32;                            // scale bytes per weight row
@@ -338,10 +352,10 @@ moe_expert_gemm_tmem(const __grid_constant__ CUtensorMap map_w,
   if (threadIdx.x == 0) {
     for (int s = 0; s < kMaxC; ++s) {
       ptx::mbar_init(&code_full[s], 1);
-      ptx::mbar_init(&code_empty[s], 8);
+      ptx::mbar_init(&code_empty[s], kDqWarps);
     }
     for (int s = 0; s < kMaxA; ++s) {
-      ptx::mbar_init(&a_full[s], 8);
+      ptx::mbar_init(&a_full[s], kDqWarps);
       ptx::mbar_init(&a_empty[s], 1);
     }
     for (int s = 0; s < kMaxB; ++s) {
@@ -350,7 +364,7 @@ moe_expert_gemm_tmem(const __grid_constant__ CUtensorMap map_w,
     }
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(&sc_full[s], 1);
-      ptx::mbar_init(&sc_empty[s], 8);
+      ptx::mbar_init(&sc_empty[s], kDqWarps);
       ptx::mbar_init(&acc_full[s], 1);
       ptx::mbar_init(&acc_empty[s], 4);
     }
@@ -472,7 +486,7 @@ moe_expert_gemm_tmem(const __grid_constant__ CUtensorMap map_w,
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++q) {
         const Unit w = unit_of(a, n_mt, u);
         const int N = (w.n + 15) & ~15;
-        const uint32_t idesc = ptx::idesc_f16(kMW, N, C::kBf16);
+        const uint32_t idesc = ptx::idesc_f16(kMW, N, !F16);
         const int buf = q & 1;
         if (!wait_phase(&acc_empty[buf], ((q >> 1) & 1) ^ 1, abort_flag, a.status)) { ok = false; break; }
         ptx::tc_fence_after();
@@ -564,12 +578,18 @@ moe_expert_gemm_tmem(const __grid_constant__ CUtensorMap map_w,
             const float gg = fminf(zg, a.limit);
             const float uu = fminf(fmaxf(zu, -a.limit), a.limit);
             const float hv = gg * (1.0f / (1.0f + expf(-a.alpha * gg))) * (uu + 1.0f);
-            const __nv_bfloat16 hh = __float2bfloat16_rn(hv);
-            const __nv_bfloat16 hl = __float2bfloat16_rn(hv - __bfloat162float(hh));
             if (nvalid && col < w.n) {
               const size_t o = size_t(w.r0 + col) * a.W + n;
-              a.h_hi[o] = hh;
-              a.h_lo[o] = hl;
+              if (a.h_f16) {                       // h = hi + lo, two f16 terms
+                const __half hh = __float2half_rn(hv);
+                const __half hl = __float2half_rn(hv - __half2float(hh));
+                reinterpret_cast<__half*>(a.h_hi)[o] = hh;
+                reinterpret_cast<__half*>(a.h_lo)[o] = hl;
+              } else {                             // h = hi + lo, two bf16 terms
+                const __nv_bfloat16 hh = __float2bfloat16_rn(hv);
+                a.h_hi[o] = hh;
+                a.h_lo[o] = __float2bfloat16_rn(hv - __bfloat162float(hh));
+              }
             }
           }
         }
@@ -594,15 +614,16 @@ moe_expert_gemm_tmem(const __grid_constant__ CUtensorMap map_w,
     }
   } else if (warp >= kWarpDq0) {
     // --------------------------------------------------------- dequantisers --
-    // Warp (quarter, hf) converts K range [hf*128, hf*128+128) of every 256-K
-    // stage for its 32 weight rows: 128 codes -> 64 TMEM columns, one
-    // tcgen05.st.  The two warps of a lane quarter share the SM partition, so
-    // one converts while the other's store drains.
+    // Warp (quarter, part) converts K range [part*64, part*64+64) of every
+    // 256-K stage for its 32 weight rows: 64 codes -> 32 TMEM columns, one
+    // tcgen05.st.
     const int quarter = warp & 3;
-    const int hf = (warp - kWarpDq0) >> 2;
+    const int part = (warp - kWarpDq0) >> 2;
     const int Ln = quarter * 32 + lane;          // TMEM lane = weight row of the tile
     const int sr = kGateUp ? ((Ln & 1) ? kMW / 2 + (Ln >> 1) : (Ln >> 1)) : Ln;   // smem row
     const uint32_t lane_addr = uint32_t(quarter * 32) << 16;
+    const uint32_t choff0 = ptx::sw128_offset(sr, part * 2);      // this row's 2 chunks
+    const uint32_t choff1 = ptx::sw128_offset(sr, part * 2 + 1);
     Ring cr, ar;
     bool ok = true;
     int q = 0;
@@ -614,12 +635,12 @@ moe_expert_gemm_tmem(const __grid_constant__ CUtensorMap map_w,
       if (!ok) break;
       const uint8_t* srow = scb + sb * L.scbuf + sr * nsb;
       int rn = 0;
-      if (kGateUp && valid)
+      if (F16 && valid)
         rn = row_max_byte(reinterpret_cast<const uint32_t*>(scb + sb * L.scbuf), uint32_t(sr * nsb), nsb);
-      if (hf == 0) {
+      if (part == 0) {
         ok = __all_sync(0xffffffffu, wait_phase(&rf_empty[ring], ((q / kRing) & 1) ^ 1, abort_flag, a.status));
         if (!ok) break;
-        rf[ring * kMW + Ln] = valid ? (kGateUp ? ldexpf(1.0f, rn - 127) : 1.0f) : 0.f;
+        rf[ring * kMW + Ln] = valid ? (F16 ? ldexpf(1.0f, rn - 127) : 1.0f) : 0.f;
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&rf_full[ring]);
       }
@@ -627,34 +648,37 @@ moe_expert_gemm_tmem(const __grid_constant__ CUtensorMap map_w,
         ok = __all_sync(0xffffffffu, wait_phase(&code_full[cr.slot], cr.phase, abort_flag, a.status));
         if (!ok) break;
         const uint8_t* cst = codes + cr.slot * kCodeStageBytes;
-        // this thread's 4 scale blocks of the stage
-        const int b0 = cs * (kSK / 32) + hf * 4;
-        uint32_t f[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int b = b0 + i;
-          f[i] = (valid && b < nsb) ? Dequant<M>::factor(int(srow[b]), rn) : 0u;
+        // this thread's 2 scale blocks: one 16-bit read when the row starts at
+        // an even byte offset (K/32 odd makes every other row start odd)
+        const int b0 = cs * (kSK / 32) + part * 2;
+        uint32_t s01 = 0;
+        if (valid && b0 < nsb) {
+          const uint8_t* sp = srow + b0;
+          if (b0 + 1 >= nsb) s01 = sp[0];
+          else if ((reinterpret_cast<uintptr_t>(sp) & 1u) == 0) s01 = *reinterpret_cast<const uint16_t*>(sp);
+          else s01 = uint32_t(sp[0]) | (uint32_t(sp[1]) << 8);
         }
-        // 128 codes: 4 x 16 bytes of the 128-byte swizzled row
-        uint4 x[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          x[i] = *reinterpret_cast<const uint4*>(cst + ptx::sw128_offset(sr, hf * 4 + i));
+        const uint32_t f0 = (valid && b0 < nsb) ? Dequant<DQ>::factor(int(s01 & 0xFF), rn) : 0u;
+        const uint32_t f1 = (valid && b0 + 1 < nsb) ? Dequant<DQ>::factor(int(s01 >> 8), rn) : 0u;
+        // 64 codes: 2 x 16 bytes of the 128-byte swizzled row
+        const uint4 x0 = *reinterpret_cast<const uint4*>(cst + choff0);
+        const uint4 x1 = *reinterpret_cast<const uint4*>(cst + choff1);
         // the code stage has been read
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&code_empty[cr.slot]);
         cr.next(NC);
-        uint32_t r[64];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          Dequant<M>::convert(x[i].x, f[i], &r[16 * i + 0]);
-          Dequant<M>::convert(x[i].y, f[i], &r[16 * i + 4]);
-          Dequant<M>::convert(x[i].z, f[i], &r[16 * i + 8]);
-          Dequant<M>::convert(x[i].w, f[i], &r[16 * i + 12]);
-        }
+        uint32_t r[32];
+        Dequant<DQ>::convert(x0.x, f0, &r[0]);
+        Dequant<DQ>::convert(x0.y, f0, &r[4]);
+        Dequant<DQ>::convert(x0.z, f0, &r[8]);
+        Dequant<DQ>::convert(x0.w, f0, &r[12]);
+        Dequant<DQ>::convert(x1.x, f1, &r[16]);
+        Dequant<DQ>::convert(x1.y, f1, &r[20]);
+        Dequant<DQ>::convert(x1.z, f1, &r[24]);
+        Dequant<DQ>::convert(x1.w, f1, &r[28]);
         ok = __all_sync(0xffffffffu, wait_phase(&a_empty[ar.slot], ar.phase ^ 1, abort_flag, a.status));
         if (!ok) break;
-        ptx::tmem_st_32x32b_x64(tmem_base + lane_addr + a_col0 + ar.slot * kACols + hf * 64, r);
+        ptx::tmem_st_32x32b_x32(tmem_base + lane_addr + a_col0 + ar.slot * kACols + part * 32, r);
         ptx::tmem_st_wait();
         ptx::tc_fence_before();
         __syncwarp();
@@ -737,7 +761,7 @@ size_t smem_bytes(const GemmArgs& a) {
   return size_t(layout<M>(K / 32, a.nb, a.stages_c, a.stages_b).total) + 1024;
 }
 
-template <Mode M>
+template <Mode M, bool F16>
 cudaError_t launch(const GemmArgs& args, cudaStream_t s) {
   GemmArgs a = args;
   plan<M>(a);
@@ -747,7 +771,7 @@ cudaError_t launch(const GemmArgs& args, cudaStream_t s) {
     return cudaErrorInvalidConfiguration;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(moe_expert_gemm_tmem<M>,
+    cudaError_t e = cudaFuncSetAttribute(moe_expert_gemm_tmem<M, F16>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
     if (e != cudaSuccess) return e;
     configured = true;
@@ -764,9 +788,11 @@ cudaError_t launch(const GemmArgs& args, cudaStream_t s) {
     e = make_map(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.w_dn, (long long)a.E * a.d, a.W / 2,
                  kSK / 2, kCodeBoxRows);
     if (e == cudaSuccess)
-      e = make_map(&m0, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.h_hi, a.R, a.W, 64, a.nb);
+      e = make_map(&m0, F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                   a.h_hi, a.R, a.W, 64, a.nb);
     if (e == cudaSuccess)
-      e = make_map(&m1, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.h_lo, a.R, a.W, 64, a.nb);
+      e = make_map(&m1, F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                   a.h_lo, a.R, a.W, 64, a.nb);
   }
   if (e != cudaSuccess) return e;
   const int n_out = (M == Mode::GateUp) ? a.W : a.d;
@@ -774,7 +800,7 @@ cudaError_t launch(const GemmArgs& args, cudaStream_t s) {
   const long long n_mt = (n_out + rows_per_tile - 1) / rows_per_tile;
   const long long units_bound = (long long)(a.R / a.nb + a.E) * n_mt;
   const int grid = int(units_bound < num_sms() ? units_bound : num_sms());
-  return launch_pdl(moe_expert_gemm_tmem<M>, dim3(grid), dim3(kThreads), smem, s, mw, m0, m1, a);
+  return launch_pdl(moe_expert_gemm_tmem<M, F16>, dim3(grid), dim3(kThreads), smem, s, mw, m0, m1, a);
 }
 
 }  // namespace
@@ -793,7 +819,14 @@ bool expert_gemm_tmem_fits(const GemmArgs& args) {
   return g.stages_b >= 2 && d.stages_b >= 2 && smem_bytes<Mode::GateUp>(g) <= size_t(kMaxSmem) &&
          smem_bytes<Mode::Down>(d) <= size_t(kMaxSmem);
 }
-cudaError_t launch_gateup_tmem(const GemmArgs& a, cudaStream_t s) { return launch<Mode::GateUp>(a, s); }
-cudaError_t launch_down_tmem(const GemmArgs& a, cudaStream_t s) { return launch<Mode::Down>(a, s); }
+cudaError_t launch_gateup_tmem(const GemmArgs& a, cudaStream_t s) { return launch<Mode::GateUp, true>(a, s); }
+cudaError_t launch_down_tmem(const GemmArgs& a, cudaStream_t s) {
+  return a.h_f16 ? launch<Mode::Down, true>(a, s) : launch<Mode::Down, false>(a, s);
+}
+
+bool hidden_fits_f16(float limit) {
+  // |h| = |g·σ(αg)·(u+1)| <= limit·(limit+1) once g <= limit and |u| <= limit
+  return std::isfinite(limit) && limit >= 0.f && limit * (limit + 1.f) < 16384.f;
+}
 
 }  // namespace moe

@@ -135,13 +135,17 @@ moe_status run_route(const void* x, int64_t T, int d, const float* rw, const flo
                      int k, int chunk, const RouteOut& r, cudaStream_t s) {
   const auto* xb = static_cast<const __nv_bfloat16*>(x);
   const int ntiles = int((T + moe::kRouterTile - 1) / moe::kRouterTile);
+  bool scanned = false;
   cudaError_t e = moe::launch_router_topk(xb, rw, rb, int(T), d, E, k, r.logit_part, r.topk_idx,
-                                          r.topk_w, r.rank, r.tile_counts, r.status, s);
+                                          r.topk_w, r.rank, r.tile_counts, r.status, chunk,
+                                          r.tile_base, r.offsets, r.mtile_off, &scanned, s);
   if (e != cudaSuccess) return cuda_fail(e, "router_topk launch");
   if ((e = trace(1, s)) != cudaSuccess) return cuda_fail(e, "trace event");
-  e = moe::launch_route_scan(r.tile_counts, ntiles, E, chunk, r.tile_base, r.offsets, r.mtile_off,
-                             s);
-  if (e != cudaSuccess) return cuda_fail(e, "route_scan launch");
+  if (!scanned) {
+    e = moe::launch_route_scan(r.tile_counts, ntiles, E, chunk, r.tile_base, r.offsets,
+                               r.mtile_off, s);
+    if (e != cudaSuccess) return cuda_fail(e, "route_scan launch");
+  }
   if ((e = trace(2, s)) != cudaSuccess) return cuda_fail(e, "trace event");
   e = moe::launch_route_scatter(xb, int(T), d, E, k, r.topk_idx, r.rank, r.tile_base, r.perm,
                                 r.inv, r.x_perm, r.rowexp, r.status, s);
@@ -232,6 +236,7 @@ moe_status moe_forward(const void* x_bf16, int64_t T, int d, int W, const float*
   a.b_dn = static_cast<const __nv_bfloat16*>(b_dn_bf16);
   a.limit = limit;
   a.alpha = alpha;
+  a.h_f16 = tmem && moe::hidden_fits_f16(limit) ? 1 : 0;
   a.h_hi = at<__nv_bfloat16>(workspace, L.h_hi);
   a.h_lo = at<__nv_bfloat16>(workspace, L.h_lo);
   a.y = at<float>(workspace, L.y);
@@ -301,6 +306,15 @@ moe_status moe_poll_status(const void* workspace, void* stream) {
 }
 
 const char* moe_last_error(void) { return g_last_error.c_str(); }
+
+moe_status moe_hidden_format(int64_t T, int d, int W, int E, int k, float limit, int* is_f16) {
+  moe_status st = check_shape(T, d, W, E, k);
+  if (st != MOE_OK) return st;
+  if (!is_f16) return fail(MOE_ERR_NULL, "is_f16 is NULL");
+  const moe::GemmArgs a = gemm_args(T, d, W, E, k);
+  *is_f16 = (T > 0 && use_tmem_gemm(a) && moe::hidden_fits_f16(limit)) ? 1 : 0;
+  return MOE_OK;
+}
 
 moe_status moe_set_trace_events(void* const* events, int n) {
   if (n == 0 || events == nullptr) {

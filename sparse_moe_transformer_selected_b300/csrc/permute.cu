@@ -8,6 +8,7 @@
 // (rank inside its tile), all integer and order-free, so the permutation is
 // deterministic without atomics.
 #include "common.cuh"
+#include "route_scan.cuh"
 
 #include <cuda_fp16.h>
 #include <math.h>
@@ -26,48 +27,9 @@ route_scan_kernel(const int32_t* __restrict__ tile_counts, int ntiles, int E, in
   __shared__ int32_t part[kScanThreads];
   __shared__ int32_t total[257];
   __shared__ int32_t off[257];
-  const int tid = threadIdx.x;
-  const int G = kScanThreads / E;           // E <= 256 -> G >= 4
-  const int g = tid / E, e = tid - g * E;
-  const bool active = g < G;
-  const int span = (ntiles + G - 1) / G;      // router tiles per thread
-  const int ta = min(ntiles, g * span), tb = min(ntiles, ta + span);
   pdl_wait();
-  int32_t sum = 0;
-  if (active)
-    for (int t = ta; t < tb; ++t) sum += tile_counts[(size_t)t * E + e];
-  part[tid] = sum;
-  __syncthreads();
-  if (tid < E) {
-    int32_t run = 0;
-    for (int q = 0; q < G; ++q) {
-      const int32_t v = part[q * E + tid];
-      part[q * E + tid] = run;
-      run += v;
-    }
-    total[tid] = run;
-  }
-  __syncthreads();
-  if (tid == 0) {
-    int32_t run = 0, mrun = 0;
-    for (int q = 0; q < E; ++q) {
-      off[q] = run;
-      offsets[q] = run;
-      mtile_off[q] = mrun;
-      run += total[q];
-      mrun += (total[q] + chunk - 1) / chunk;
-    }
-    offsets[E] = run;
-    mtile_off[E] = mrun;
-  }
-  __syncthreads();
-  if (active) {
-    int32_t base = off[e] + part[tid];
-    for (int t = ta; t < tb; ++t) {
-      tile_base[(size_t)t * E + e] = base;
-      base += tile_counts[(size_t)t * E + e];
-    }
-  }
+  scan_tiles<kScanThreads>(tile_counts, ntiles, E, chunk, tile_base, offsets, mtile_off, part, total,
+                           off);
 }
 
 // One warp per routed row (t, j): write perm / inv and copy x[t] to its row,
@@ -104,22 +66,14 @@ route_scatter_kernel(const __nv_bfloat16* __restrict__ x, int T, int d, int E, i
     const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * d);
     uint4* dst = reinterpret_cast<uint4*>(x_perm + (size_t)row * d);
     const int n16 = d / 8;
-    float xmax = 0.f;                                    // largest |x| of the token
-    for (int i = lane; i < n16; i += 32) {
-      const uint4 v = src[i];
+    auto absmax8 = [](const uint4& v, float m) {
       const uint32_t in[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
       for (int c = 0; c < 4; ++c)
-        xmax = fmaxf(xmax, fmaxf(fabsf(__uint_as_float(in[c] << 16)),
-                                 fabsf(__uint_as_float(in[c] & 0xFFFF0000u))));
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) xmax = fmaxf(xmax, __shfl_xor_sync(0xffffffffu, xmax, off));
-    const int et = (xmax > 0.f && isfinite(xmax)) ? max(-126, min(126, 14 - ilogbf(xmax))) : 0;
-    if (lane == 0) rowexp[row] = et;
-    const float f = __int_as_float((et + 127) << 23);   // 2^e_t, |e_t| <= 126
-    for (int i = lane; i < n16; i += 32) {
-      const uint4 v = src[i];
+        m = fmaxf(m, fmaxf(fabsf(__uint_as_float(in[c] << 16)), fabsf(__uint_as_float(in[c] & 0xFFFF0000u))));
+      return m;
+    };
+    auto to_f16 = [](const uint4& v, float f) {
       const uint32_t in[4] = {v.x, v.y, v.z, v.w};
       uint32_t o[4];
 #pragma unroll
@@ -129,7 +83,41 @@ route_scatter_kernel(const __nv_bfloat16* __restrict__ x, int T, int d, int E, i
         const __half2 h = __floats2half2_rn(lo, hi);
         o[c] = *reinterpret_cast<const uint32_t*>(&h);
       }
-      dst[i] = make_uint4(o[0], o[1], o[2], o[3]);
+      return make_uint4(o[0], o[1], o[2], o[3]);
+    };
+    auto exponent = [&](float xmax) {
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) xmax = fmaxf(xmax, __shfl_xor_sync(0xffffffffu, xmax, off));
+      return (xmax > 0.f && isfinite(xmax)) ? max(-126, min(126, 14 - ilogbf(xmax))) : 0;
+    };
+    // A row of up to 32 x kRowRegs 16-byte pieces (d <= 3072) is read once into
+    // registers, all loads in flight together; longer rows take two passes.
+    constexpr int kRowRegs = 12;
+    if (n16 <= 32 * kRowRegs) {
+      uint4 v[kRowRegs];
+      float xmax = 0.f;                                  // largest |x| of the token
+#pragma unroll
+      for (int j = 0; j < kRowRegs; ++j) {
+        const int i = lane + 32 * j;
+        v[j] = i < n16 ? src[i] : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int j = 0; j < kRowRegs; ++j) xmax = absmax8(v[j], xmax);
+      const int et = exponent(xmax);
+      if (lane == 0) rowexp[row] = et;
+      const float f = __int_as_float((et + 127) << 23);  // 2^e_t, |e_t| <= 126
+#pragma unroll
+      for (int j = 0; j < kRowRegs; ++j) {
+        const int i = lane + 32 * j;
+        if (i < n16) dst[i] = to_f16(v[j], f);
+      }
+    } else {
+      float xmax = 0.f;
+      for (int i = lane; i < n16; i += 32) xmax = absmax8(src[i], xmax);
+      const int et = exponent(xmax);
+      if (lane == 0) rowexp[row] = et;
+      const float f = __int_as_float((et + 127) << 23);
+      for (int i = lane; i < n16; i += 32) dst[i] = to_f16(src[i], f);
     }
   }
 }

@@ -15,6 +15,7 @@
 // flops, well under 1% of the block; fp32 keeps the selection faithful to the
 // exact logits except at true near-ties.
 #include "common.cuh"
+#include "route_scan.cuh"
 
 #include <math.h>
 
@@ -42,8 +43,10 @@ router_logits_kernel(const __nv_bfloat16* __restrict__ x, const float* __restric
   const int e0 = blockIdx.z * eg;                // this CTA's experts: e0 .. e0+eg-1
   const int ne = min(eg, E - e0);
   pdl_wait();
-  if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && tid == 0)
+  if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && tid == 0) {
     status[0] = 0;                               // first kernel of a call
+    status[1] = 0;                               // top-k tiles done (fused scan)
+  }
 
   float acc[4][NPER];
 #pragma unroll
@@ -51,6 +54,51 @@ router_logits_kernel(const __nv_bfloat16* __restrict__ x, const float* __restric
 #pragma unroll
     for (int j = 0; j < NPER; ++j) acc[i][j] = 0.f;
 
+  // A decode-sized CTA (one group of 32 experts, at most 8 chunks of 32 K)
+  // issues all of its global loads first, then stages each chunk through
+  // shared memory: one round of memory latency instead of one per chunk.
+  const int nchunks = (ke - kb + kKC - 1) / kKC;
+  if (NPER == 1 && nchunks <= 8) {
+    uint2 xr[8];
+    float4 wr[8];
+    const int tl = tid >> 3, kq = (tid & 7) * 4, t = t0 + tl;
+    const int we = tid >> 3;                      // expert of this thread's W piece
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const int k0 = kb + c * kKC;
+      xr[c] = make_uint2(0, 0);
+      wr[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (c < nchunks) {
+        if (t < T) xr[c] = *reinterpret_cast<const uint2*>(x + (size_t)t * d + k0 + kq);
+        if (we < ne) wr[c] = *reinterpret_cast<const float4*>(rw + (size_t)(e0 + we) * d + k0 + kq);
+      }
+    }
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      if (c >= nchunks) break;
+      const __nv_bfloat162 a2 = *reinterpret_cast<const __nv_bfloat162*>(&xr[c].x);
+      const __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162*>(&xr[c].y);
+      xs[tl][kq + 0] = __low2float(a2);
+      xs[tl][kq + 1] = __high2float(a2);
+      xs[tl][kq + 2] = __low2float(b2);
+      xs[tl][kq + 3] = __high2float(b2);
+      wl[(kq + 0) * kLgStride + we] = wr[c].x;
+      wl[(kq + 1) * kLgStride + we] = wr[c].y;
+      wl[(kq + 2) * kLgStride + we] = wr[c].z;
+      wl[(kq + 3) * kLgStride + we] = wr[c].w;
+      __syncthreads();
+#pragma unroll 4
+      for (int kk = 0; kk < kKC; ++kk) {
+        float xv[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) xv[i] = xs[warp * 4 + i][kk];
+        const float wv = wl[kk * kLgStride + lane];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[i][0] = fmaf(xv[i], wv, acc[i][0]);
+      }
+      __syncthreads();
+    }
+  } else
   for (int k0 = kb; k0 < ke; k0 += kKC) {
     {  // x chunk: 32 tokens x 32 k, 4 bf16 per thread
       const int tl = tid >> 3, kq = (tid & 7) * 4, t = t0 + tl;
@@ -106,10 +154,14 @@ template <int NPER>
 __global__ void __launch_bounds__(kThreads)
 router_topk_kernel(const float* __restrict__ part, int nks, const float* __restrict__ rb, int T,
                    int E, int k, int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
-                   int32_t* __restrict__ rank, int32_t* __restrict__ tile_counts) {
+                   int32_t* __restrict__ rank, int32_t* __restrict__ tile_counts,
+                   int32_t* __restrict__ tiles_done, int chunk, int32_t* __restrict__ tile_base,
+                   int32_t* __restrict__ offsets, int32_t* __restrict__ mtile_off) {
   __shared__ float wl[kTT * kLgStride];  // logits [t][e]
   __shared__ uint32_t mask[kMaxE];       // bit t: token t of this tile picked e
   __shared__ int32_t sel[kTT][8];
+  __shared__ int32_t scan_part[kThreads], scan_total[257], scan_off[257];
+  __shared__ int last_cta;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int t0 = blockIdx.x * kTT;
@@ -117,12 +169,23 @@ router_topk_kernel(const float* __restrict__ part, int nks, const float* __restr
   for (int e = tid; e < kMaxE; e += kThreads) mask[e] = 0u;
   pdl_wait();
 
-  // logits = the K-range partial sums in a fixed order, then the bias
+  // logits = the K-range partial sums in a fixed order, then the bias (up to
+  // 16 partials are all loaded before any is added, one round of loads)
   for (int idx = tid; idx < ntok * E; idx += kThreads) {
     const int tl = idx / E, e = idx - tl * E;
+    const float* p = part + (size_t)(t0 + tl) * E + e;
+    const size_t stride = (size_t)T * E;
     float v = 0.f;
-#pragma unroll 4
-    for (int s = 0; s < nks; ++s) v += part[((size_t)s * T + t0 + tl) * E + e];
+    if (nks <= 16) {
+      float pv[16];
+#pragma unroll
+      for (int s = 0; s < 16; ++s) pv[s] = s < nks ? p[s * stride] : 0.f;
+#pragma unroll
+      for (int s = 0; s < 16; ++s)
+        if (s < nks) v += pv[s];
+    } else {
+      for (int s = 0; s < nks; ++s) v += p[s * stride];
+    }
     wl[tl * kLgStride + e] = v + rb[e];
   }
   __syncthreads();
@@ -190,6 +253,20 @@ router_topk_kernel(const float* __restrict__ part, int nks, const float* __restr
     const int e = sel[tl][j];
     rank[(size_t)(t0 + tl) * k + j] = __popc(mask[e] & ((1u << tl) - 1u));
   }
+
+  // With few tiles the CTA that finishes last also runs the expert scan (the
+  // counter was zeroed by the logits kernel of this call).
+  if (tiles_done != nullptr) {
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) last_cta = atomicAdd(tiles_done, 1) == int(gridDim.x) - 1;
+    __syncthreads();
+    if (last_cta) {
+      __threadfence();
+      scan_tiles<kThreads>(tile_counts, int(gridDim.x), E, chunk, tile_base, offsets, mtile_off,
+                           scan_part, scan_total, scan_off);
+    }
+  }
 }
 
 }  // namespace
@@ -197,8 +274,9 @@ router_topk_kernel(const float* __restrict__ part, int nks, const float* __restr
 cudaError_t launch_router_topk(const __nv_bfloat16* x, const float* router_w,
                                const float* router_b, int T, int d, int E, int k,
                                float* logit_part, int32_t* topk_idx, float* topk_w,
-                               int32_t* rank, int32_t* tile_counts, int32_t* status,
-                               cudaStream_t s) {
+                               int32_t* rank, int32_t* tile_counts, int32_t* status, int chunk,
+                               int32_t* tile_base, int32_t* offsets, int32_t* mtile_off,
+                               bool* scanned, cudaStream_t s) {
   const int ntiles = (T + kTT - 1) / kTT;
   const int nks = router_splits(T, d, E);
   const int kc = router_split_len(T, d, E);
@@ -225,10 +303,15 @@ cudaError_t launch_router_topk(const __nv_bfloat16* x, const float* router_w,
   }
 #undef MOE_LOGITS_CASE
   if (e != cudaSuccess) return e;
+  // few tiles: the last top-k CTA runs the expert scan (no separate launch)
+  const bool fuse = ntiles <= kFuseScanTiles && tile_base != nullptr;
+  int32_t* done = fuse ? status + 1 : nullptr;
+  if (scanned) *scanned = fuse;
 #define MOE_TOPK_CASE(N)                                                                     \
   case N:                                                                                    \
     e = launch_pdl(router_topk_kernel<N>, dim3(ntiles), dim3(kThreads), 0, s, logit_part,    \
-                   nks, router_b, T, E, k, topk_idx, topk_w, rank, tile_counts);             \
+                   nks, router_b, T, E, k, topk_idx, topk_w, rank, tile_counts, done, chunk, \
+                   tile_base, offsets, mtile_off);                                           \
     break;
   switch (nper) {
     MOE_TOPK_CASE(1)

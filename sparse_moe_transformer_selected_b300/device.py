@@ -83,6 +83,11 @@ class DeviceMoE:
                       inv, self.workspace, self.workspace.numel(), stream)
         return idx, w, off, perm, inv
 
+    def hidden_dtype(self) -> torch.dtype:
+        """The 16-bit type of the h_hi / h_lo tables on this shape and clamp."""
+        f16 = moe.moe_hidden_format(self.T, self.d, self.W, self.E, self.k, self.limit)
+        return torch.float16 if f16 else torch.bfloat16
+
     def region(self, which: str) -> torch.Tensor:
         """A view of an intermediate table inside the workspace (after forward)."""
         off, nb = moe.moe_workspace_region(self.T, self.d, self.W, self.E, self.k, which)
@@ -92,7 +97,7 @@ class DeviceMoE:
             "topk_idx": (torch.int32, (self.T, self.k)), "topk_w": (torch.float32, (self.T, self.k)),
             "offsets": (torch.int32, (self.E + 1,)), "perm": (torch.int32, (R,)),
             "inv": (torch.int32, (self.T, self.k)), "x_perm": (torch.float16, (R, self.d)),
-            "h_hi": (torch.bfloat16, (R, self.W)), "h_lo": (torch.bfloat16, (R, self.W)),
+            "h_hi": (self.hidden_dtype(), (R, self.W)), "h_lo": (self.hidden_dtype(), (R, self.W)),
             "y": (torch.float32, (R, self.d)),
         }[which]
         return raw.view(dtype).view(shape)

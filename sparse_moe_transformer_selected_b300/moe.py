@@ -26,7 +26,7 @@ REGIONS = {"topk_idx": 0, "topk_w": 1, "offsets": 2, "perm": 3, "inv": 4,
 # Every symbol include/moe.h declares.
 EXPORTS = ("moe_workspace_bytes", "moe_forward", "moe_route", "moe_poll_status",
            "moe_last_error", "moe_workspace_region", "moe_set_trace_events",
-           "moe_forward_noalloc")
+           "moe_forward_noalloc", "moe_hidden_format")
 
 # Scratch built into the library for moe_forward_noalloc (MOE_NOALLOC_SCRATCH_BYTES).
 NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -71,6 +71,8 @@ def load() -> ctypes.CDLL:
     lib.moe_forward_noalloc.argtypes = [P, I64, I32, I32, P, P, P, P, P, P, P, P, I32, I32, F32,
                                         F32, P, P]
     lib.moe_forward_noalloc.restype = I32
+    lib.moe_hidden_format.argtypes = [I64, I32, I32, I32, I32, F32, ctypes.POINTER(I32)]
+    lib.moe_hidden_format.restype = I32
     _lib = lib
     return lib
 
@@ -131,6 +133,13 @@ def moe_route(x_bf16, T, d, router_w, router_b, E, k, topk_idx, topk_w, offsets,
 
 def moe_poll_status(workspace, stream=None) -> int:
     return _check(load().moe_poll_status(_ptr(workspace), _stream(stream)))
+
+
+def moe_hidden_format(T: int, d: int, W: int, E: int, k: int, limit: float) -> bool:
+    """True when moe_forward carries h as an f16 pair on this shape, else bf16."""
+    v = ctypes.c_int(0)
+    _check(load().moe_hidden_format(T, d, W, E, k, limit, ctypes.byref(v)))
+    return bool(v.value)
 
 
 def moe_set_trace_events(events) -> int:
