@@ -158,12 +158,16 @@ __device__ __forceinline__ Unit unit_of(const GemmArgs& a, int n_mt, int u) {
 // in the status word) or when another thread of the CTA gave up.
 // The thread sleeps inside the wait instruction (woken when the phase
 // completes) and wakes at least every 20 us to check the abort flag and the
-// time limit.
+// time limit.  `backoff_ns` > 0 also sleeps that long between polls: for
+// waits that usually last a whole work unit (the epilogue) or that run far
+// ahead (the producers), so polling does not take issue slots from the
+// dequantisers that share the SM partition.
 __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                           int32_t* status) {
+                                           int32_t* status, uint32_t backoff_ns = 0) {
   if (ptx::mbar_try_wait_sleep(bar, parity, 20000u)) return true;
   const long long t0 = clock64();
   while (true) {
+    if (backoff_ns) __nanosleep(backoff_ns);
     if (ptx::mbar_try_wait_sleep(bar, parity, 20000u)) return true;
     if (*abort_flag) return false;
     if (clock64() - t0 > kSpinLimit) {
@@ -403,7 +407,7 @@ moe_expert_gemm_tmem(const __grid_constant__ CUtensorMap map_w,
         const Unit w = unit_of(a, n_mt, u);
         // the unit's scale rows (1-D bulk copies of contiguous rows)
         const int sb = q & 1;
-        if (!wait_phase(&sc_empty[sb], ((q >> 1) & 1) ^ 1, abort_flag, a.status)) { ok = false; break; }
+        if (!wait_phase(&sc_empty[sb], ((q >> 1) & 1) ^ 1, abort_flag, a.status, 64)) { ok = false; break; }
         const uint8_t* wscale = kGateUp ? a.w_gu_scale : a.w_dn_scale;
         int row_a, row_b;
         if constexpr (kGateUp) {
@@ -427,7 +431,7 @@ moe_expert_gemm_tmem(const __grid_constant__ CUtensorMap map_w,
         }
         s_in.mark(sb, (q >> 1) & 1);
         for (int cs = 0; cs < nS; ++cs) {
-          if (!wait_phase(&code_empty[cr.slot], cr.phase ^ 1, abort_flag, a.status)) { ok = false; break; }
+          if (!wait_phase(&code_empty[cr.slot], cr.phase ^ 1, abort_flag, a.status, 64)) { ok = false; break; }
           uint8_t* cdst = codes + cr.slot * kCodeStageBytes;
           ptx::mbar_arrive_expect_tx(&code_full[cr.slot], kCodeStageBytes);
           ptx::tma_load_2d(cdst, &map_w, &code_full[cr.slot], cs * (kSK / 2), row_a);
@@ -453,7 +457,7 @@ moe_expert_gemm_tmem(const __grid_constant__ CUtensorMap map_w,
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
         const Unit w = unit_of(a, n_mt, u);
         for (int jb = 0; jb < nKB; ++jb) {
-          if (!wait_phase(&b_empty[br.slot], br.phase ^ 1, abort_flag, a.status)) { ok = false; break; }
+          if (!wait_phase(&b_empty[br.slot], br.phase ^ 1, abort_flag, a.status, 64)) { ok = false; break; }
           // one box of nb rows x 64 K per sub-tile and operand (rows past the
           // chunk are other experts' tokens or zero fill, and only feed
           // accumulator columns the epilogue ignores); sub-tiles past K are
@@ -541,7 +545,7 @@ moe_expert_gemm_tmem(const __grid_constant__ CUtensorMap map_w,
     for (int u = blockIdx.x; u < units; u += gridDim.x, ++q) {
       const Unit w = unit_of(a, n_mt, u);
       const int buf = q & 1, ring = q % kRing;
-      const bool ok = wait_phase(&acc_full[buf], (q >> 1) & 1, abort_flag, a.status) &&
+      const bool ok = wait_phase(&acc_full[buf], (q >> 1) & 1, abort_flag, a.status, 256) &&
                       wait_phase(&rf_full[ring], (q / kRing) & 1, abort_flag, a.status);
       if (!__all_sync(0xffffffffu, ok)) break;   // warp-uniform: tcgen05.ld is .sync.aligned
       ptx::tc_fence_after();

@@ -71,6 +71,24 @@ class DeviceMoE:
                         self.workspace, self.workspace.numel(), stream)
         return out
 
+    def capture_graph(self) -> "torch.cuda.CUDAGraph":
+        """A CUDA graph of one moe_forward on this layer's buffers: replaying it
+        reads self.x and writes self.out with a single launch from the host.
+
+        moe_forward neither synchronises nor allocates, so it can be captured;
+        its kernels' programmatic launches become graph edges.  One eager call
+        first sets the kernels' launch attributes outside the capture.
+        """
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            self.forward()
+        torch.cuda.current_stream().wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            self.forward()
+        return graph
+
     def route(self, stream=None):
         T, k, E = self.T, self.k, self.E
         dev = self.x.device

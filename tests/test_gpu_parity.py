@@ -227,3 +227,22 @@ def test_both_gemm_designs_agree_on_decode(monkeypatch):
     b = bf16_to_f64(dev.forward().clone())
     moe.moe_poll_status(dev.workspace)
     parity.check_output(a, b, what="tmem vs smem design")
+
+
+def test_cuda_graph_replay_matches_eager_call():
+    """moe_forward captured into a CUDA graph (the benchmark's end-to-end path)
+    gives the eager call's output bit for bit, and follows new inputs."""
+    inp = gen.make_inputs(gen.WORKLOADS["gptoss20b_decode"])
+    dev = DeviceMoE.upload(inp)
+    eager = dev.forward().clone()
+    graph = dev.capture_graph()
+    dev.out.fill_(0)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(eager.view(torch.int16), dev.out.view(torch.int16))
+    x2 = gen.make_inputs(gen.WORKLOADS["gptoss20b_decode"].with_(seed=77)).x
+    dev.x.copy_(torch.from_numpy(x2.view(np.int16)).view(torch.bfloat16))
+    graph.replay()
+    second = dev.out.clone()
+    assert torch.equal(second.view(torch.int16), dev.forward().view(torch.int16))
+    moe.moe_poll_status(dev.workspace)
