@@ -100,12 +100,20 @@ size_t moe_workspace_bytes(int64_t T, int d, int W, int E, int k);
  *   limit       clamp bound (7.0 for gpt-oss; +inf disables the clamp)
  *   alpha       sigmoid slope (1.702 for gpt-oss)
  *   out_bf16    [T, d]        bf16, written completely
- * Precision: router logits, softmax and all accumulation in fp32; h is carried
- * between the two GEMMs as a pair of 16-bit terms, hi + lo: f16 (about 22
- * significant bits) when the clamp bounds |h| well inside the f16 range
- * (limit·(limit+1) < 16384, e.g. limit = 7), otherwise bf16 (about 16 bits);
- * moe_hidden_format says which.  y is fp32; out is rounded once, to nearest
- * even.
+ * Precision: router logits, softmax and all accumulation in fp32.  The
+ * weights enter the products exactly (code x 2^(scale - 127)).  Two number
+ * formats carry the activations, chosen per call (moe_hidden_format says which):
+ *  - decode-sized loads (at most 16 routed rows per expert on average) with a
+ *    clamp 0 < limit <= 16, weight buffers 32-byte aligned: x and h as sums
+ *    of E4M3 terms fed to the tensor cores' block-scaled MXFP4 x MXFP8
+ *    products: x = hi + lo/16 with a power-of-two scale per 32-element block
+ *    (exact for bf16 x), h = t0 + t1/16 + t2/256 + t3/4096 with one fixed
+ *    scale 2^e that keeps |h| <= limit·(limit+1) inside the E4M3 range
+ *    (about 16 significant bits);
+ *  - otherwise x exactly (f16 after a per-token power-of-two scaling) and h
+ *    as a pair of 16-bit terms, hi + lo: f16 (about 22 significant bits) when
+ *    limit·(limit+1) < 16384, else bf16 (about 16 bits).
+ * y is fp32; out is rounded once, to nearest even.
  */
 moe_status moe_forward(const void* x_bf16, int64_t T, int d, int W,
                        const float* router_w, const float* router_b,
@@ -150,22 +158,33 @@ const char* moe_last_error(void);
  *   which: 0 topk_idx int32[T,k]   1 topk_w fp32[T,k]     2 offsets int32[E+1]
  *          3 perm int32[T·k]       4 inv int32[T,k]       5 x_perm f16[T·k,d]
  *          6 h_hi [T·k,W]          7 h_lo [T·k,W]         8 y fp32[T·k,d]
- * h_hi and h_lo are f16 or bf16 as moe_hidden_format reports.
+ * h_hi and h_lo are f16 or bf16 as moe_hidden_format reports; in the E4M3
+ * terms format the four E4M3 tables start at region 6 and run into region 7.
  * x_perm holds each routed row's token scaled by 2^e_t (e_t puts the token's
- * largest |x| in [2^14, 2^15), so the f16 value is exact).
+ * largest |x| in [2^14, 2^15), so the f16 value is exact); in the E4M3 terms
+ * format it holds the two E4M3 tables of x (hi [T·k,d] then lo [T·k,d]).
  * Returns MOE_ERR_SHAPE for an invalid shape or `which`.
  */
 moe_status moe_workspace_region(int64_t T, int d, int W, int E, int k, int which,
                                 size_t* offset, size_t* bytes);
 
 /*
- * The 16-bit type moe_forward uses for the two terms of h (hi + lo) on this
- * shape and clamp: *is_f16 = 1 for f16, 0 for bf16.  This only describes the
- * intermediate tables inside the workspace (for inspection); the results do not
- * depend on it beyond rounding.  Returns MOE_ERR_SHAPE / MOE_ERR_NULL like the
- * other calls.  The pages have no counterpart: this is an inspection aid.
+ * The number format moe_forward uses for h between the two GEMMs on this shape
+ * and clamp (for weight buffers aligned to 32 bytes):
+ *   *format = MOE_HIDDEN_BF16_PAIR   h = hi + lo, two bf16 tables
+ *             MOE_HIDDEN_F16_PAIR    h = hi + lo, two f16 tables
+ *             MOE_HIDDEN_E4M3_TERMS  h = (t0 + t1/16 + t2/256 + t3/4096) · 2^(*exponent),
+ *                                    four E4M3 tables [T·k,W] one after another
+ * `exponent` may be NULL.  This only describes the intermediate tables inside
+ * the workspace (for inspection); the results do not depend on it beyond
+ * rounding.  Returns MOE_ERR_SHAPE / MOE_ERR_NULL like the other calls.  The
+ * pages have no counterpart: this is an inspection aid.
  */
-moe_status moe_hidden_format(int64_t T, int d, int W, int E, int k, float limit, int* is_f16);
+#define MOE_HIDDEN_BF16_PAIR 0
+#define MOE_HIDDEN_F16_PAIR 1
+#define MOE_HIDDEN_E4M3_TERMS 2
+moe_status moe_hidden_format(int64_t T, int d, int W, int E, int k, float limit, int* format,
+                             int* exponent);
 
 /*
  * Tracing aid: make moe_forward calls from the calling thread record CUDA

@@ -85,12 +85,18 @@ struct Workspace {
   size_t perm;         // int32[R]
   size_t inv;          // int32[R]
   size_t rowexp;       // int32[R]   e_t of the token of each permuted row
-  size_t x_perm;       // f16[R, d]  x[t] * 2^e_t
-  size_t h_hi;         // bf16[R, W]
+  size_t x_perm;       // f16[R, d]  x[t] * 2^e_t; block-scaled design: E4M3 hi [R, d] then lo [R, d]
+  size_t h_hi;         // bf16[R, W]; block-scaled design: 4 E4M3 term tables [R, W] over h_hi and h_lo
   size_t h_lo;         // bf16[R, W]
   size_t y;            // float[R, d]
+  size_t sx_hi;        // uint8[R + kGemmBM, ld_sx]  UE8M0 block scales of x hi (block-scaled design)
+  size_t sx_lo;        // uint8[R + kGemmBM, ld_sx]  ... of x lo
   size_t total;
 };
+
+// Row stride of the activation block-scale tables: d/32 bytes rounded up to a
+// multiple of 16 (the rows of a chunk are copied with 1-D bulk copies).
+inline int scale_row_bytes(int d) { return (d / 32 + 15) / 16 * 16; }
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -120,6 +126,8 @@ inline Workspace workspace_layout(int64_t T, int d, int W, int E, int k) {
   ws.h_hi = take(size_t(R) * W * 2);
   ws.h_lo = take(size_t(R) * W * 2);
   ws.y = take(size_t(R) * d * 4);
+  ws.sx_hi = take(size_t(R + kGemmBM) * scale_row_bytes(d));
+  ws.sx_lo = take(size_t(R + kGemmBM) * scale_row_bytes(d));
   ws.total = off;
   return ws;
 }
@@ -170,6 +178,14 @@ struct GemmArgs {
   __nv_bfloat16* h_hi; __nv_bfloat16* h_lo;
   float* y;
   int32_t* status;
+  // block-scaled design (expert_gemm_mx.cu): activations as sums of E4M3
+  // terms, x = (hi + lo / 16) * 2^(s - 127) with s the hi block's UE8M0 byte
+  // (the lo table holds s - 4), h = (t0 + t1 / 16 + t2 / 256 + t3 / 4096) * 2^h_exp
+  const uint8_t* xq_hi; const uint8_t* xq_lo;   // [R, d]
+  const uint8_t* sx_hi; const uint8_t* sx_lo;   // [R + kGemmBM, ld_sx]
+  int ld_sx;
+  uint8_t* hq;                                  // 4 tables [R, W], term t at hq + t R W
+  int h_exp;
 };
 
 // K3: h = swiglu(x_perm · W_gu^T + b_gu), per expert segment.
@@ -191,6 +207,27 @@ int expert_gemm_tmem_chunk(int64_t R, int E);
 bool hidden_fits_f16(float limit);
 cudaError_t launch_gateup_tmem(const GemmArgs& a, cudaStream_t s);
 cudaError_t launch_down_tmem(const GemmArgs& a, cudaStream_t s);
+
+// K3 / K4 on the block-scaled tensor-core path (expert_gemm_mx.cu): the MXFP4
+// weights are consumed as E2M1 codes with their UE8M0 scales by tcgen05.mma
+// kind::mxf8f6f4, the activations as E4M3 hi / lo pairs with block scales.
+// Usable when mx_fits() holds; gate_up writes h in the pair format down reads.
+bool mx_fits(const GemmArgs& a, float limit);
+int mx_chunk(int64_t R, int E);
+// Exponent of the fixed power-of-two scale of h: |h| <= limit * (limit + 1)
+// maps inside the E4M3 range.
+int mx_hidden_exp(float limit);
+cudaError_t launch_gateup_mx(const GemmArgs& a, cudaStream_t s);
+cudaError_t launch_down_mx(const GemmArgs& a, cudaStream_t s);
+
+// K2b, block-scaled design: perm / inv and x[t] as E4M3 hi / lo pairs with
+// one UE8M0 scale per 32-element block (hi: 2^(e_b) with e_b putting the
+// block's largest |x| in [128, 256); lo: the remainder times 16).
+cudaError_t launch_route_scatter_mx(const __nv_bfloat16* x, int T, int d, int E, int k,
+                                    const int32_t* topk_idx, const int32_t* rank,
+                                    const int32_t* tile_base, int32_t* perm, int32_t* inv,
+                                    uint8_t* xq_hi, uint8_t* xq_lo, uint8_t* sx_hi,
+                                    uint8_t* sx_lo, int ld_sx, int32_t* status, cudaStream_t s);
 
 // K5: out[t] = bf16(Σ_j w[t,j] · y[inv[t,j]]); a row index outside [0, T·k)
 // is skipped and recorded in the status word.

@@ -1,0 +1,704 @@
+// K3 / K4 — grouped expert GEMMs on the block-scaled tensor-core path.
+//
+// Each expert's segment of the permuted rows is multiplied by that expert's
+// MXFP4 weights ("OpenAI 最新开源模型 gpt-oss 架构与训练解析", 模型架构: MoE
+// weights in MXFP4, 32 E2M1 codes sharing one E8M0 scale; experts are
+// gated-SwiGLU FFNs with clamping and the +1 term on the up branch;
+// 更深对比更宽: d = W = 2880).
+//
+// The MXFP4 format is what tcgen05.mma kind::mxf8f6f4 consumes: A is E2M1
+// codes, each 32-element K block with a UE8M0 scale held in tensor memory, so
+// the weights go from HBM to the tensor core without being converted.  The
+// activations are the B side as sums of E4M3 terms, each term with its own
+// block scales, stacked along N: rows t nb .. t nb + nb - 1 of B are term t of
+// the chunk's nb tokens, and the epilogue adds accumulator columns t nb + j.
+//   gate_up: x = hi + lo / 16 (2 terms; a bf16 value splits exactly)
+//   down:    h = (t0 + t1 / 16 + t2 / 256 + t3 / 4096) 2^h_exp (4 terms,
+//            about 16 significant bits)
+// One MMA covers M = 128 weight rows, N = terms x nb, K = 32.
+//
+//   D[weight row, j] = Σ_k A[row, k] 2^(sa - 127) · B[j, k] 2^(sb - 127)
+//
+// Operands in shared memory, 128-byte swizzle, K-major:
+//   A  TMA with the 4-bit "16U4_ALIGN16B" type: every 16 packed codes (8 bytes)
+//      land in 16 bytes (8 bytes of codes, 8 bytes of padding), the layout
+//      the MMA reads E2M1 from.  A box is 128 codes x 64 or 128 rows.  The
+//      type wants the tensor's row length a multiple of 128, so the map covers
+//      the first K - K % 128 codes of each row and a second map, whose base
+//      is the row's last 128 codes, serves the tail.
+//   B  TMA of E4M3 bytes, one box of 128 K x nb rows per operand (hi, lo).
+// Scales in tensor memory, written once per unit by four warps with tcgen05.st
+// (a row's 4 scale bytes of 4 consecutive K blocks share a 32-bit column; the
+// MMA picks the byte with the descriptor's scale-factor ID).
+//
+// Persistent kernel, one CTA per SM, 12 warps:
+//   warp 0      producer: per unit the scale rows (1-D bulk copies), per stage
+//               A and B (TMA); one ring of stages of 256 K
+//   warp 1      MMA issuer (one elected thread)
+//   warp 2      TMEM allocator: 512 columns (2 accumulators of 64, then two
+//               sets of A and B scale columns)
+//   warps 4-7   epilogue, TMEM lane quarter = warp % 4
+//   warps 8-11  scale writers, TMEM lane quarter = warp % 4
+// Work unit = (token chunk of one expert, weight tile of 128 rows), chunk-major.
+#include "common.cuh"
+#include "tc_ptx.cuh"
+
+#include <cudaTypedefs.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <math.h>
+
+#include <mutex>
+
+namespace moe {
+namespace {
+
+constexpr int kMW = 128;                      // weight rows per unit (MMA M)
+constexpr int kBoxK = 128;                    // K per box: one 128-byte swizzle row
+constexpr int kBoxBytesA = kMW * kBoxK;       // 16 KB, one byte per code in shared memory
+constexpr int kNB = 16;                       // token chunk
+constexpr int kHTerms = 4;                    // E4M3 terms of h
+constexpr int kXTerms = 2;                    // E4M3 terms of x
+constexpr int kAccCols = 64;                  // TMEM columns per accumulator
+constexpr int kMaxStages = 8;
+constexpr int kThreads = 384;
+constexpr int kWarpProd = 0, kWarpMMA = 1, kWarpTmem = 2, kWarpEpi0 = 4, kWarpSf0 = 8;
+constexpr int kTmemCols = 512;
+constexpr int kMaxGroups = (kTmemCols - 2 * kAccCols) / 16;   // SF groups (4 K blocks each)
+constexpr long long kSpinLimit = 4000000000ll;
+constexpr int kMaxSmem = 232448;
+// stage ring (full + empty), scales (2 + 2), scale columns (2 + 2),
+// accumulators (2 + 2), final drain
+constexpr int kNumBars = 2 * kMaxStages + 4 + 4 + 4 + 1;
+
+enum class Mode { GateUp, Down };
+
+// Bounded wait: true when the phase completed; false after a timeout (code in
+// status[0], the waiting role's tag in status[4]) or when another thread of
+// the CTA gave up.
+__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                           int32_t* status, uint32_t backoff_ns = 0, int tag = 0) {
+  if (ptx::mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+  const long long t0 = clock64();
+  for (uint32_t n = 1;; ++n) {
+    if (backoff_ns) __nanosleep(backoff_ns);
+    if (ptx::mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+    if ((n & 31) == 0) {
+      if (*abort_flag) return false;
+      if (clock64() - t0 > kSpinLimit) {
+        *abort_flag = 1;
+        atomicMax(status, kStatusTimeout);
+        atomicExch(status + 4, tag);
+        return false;
+      }
+    }
+  }
+}
+
+struct Ring {
+  int slot = 0;
+  uint32_t phase = 0;
+  __device__ __forceinline__ void next(int n) {
+    if (++slot == n) { slot = 0; phase ^= 1; }
+  }
+};
+
+struct Inflight {
+  uint32_t issued = 0, parity = 0;
+  __device__ __forceinline__ void mark(int slot, uint32_t phase) {
+    issued |= 1u << slot;
+    parity = (parity & ~(1u << slot)) | (phase << slot);
+  }
+  __device__ __forceinline__ void drain(uint64_t* bars, int n) const {
+    const long long t0 = clock64();
+    for (int s = 0; s < n; ++s) {
+      if (!(issued >> s & 1u)) continue;
+      while (!ptx::mbar_try_wait(&bars[s], (parity >> s) & 1u) && clock64() - t0 < kSpinLimit) {
+      }
+    }
+  }
+};
+
+// All `count` threads of named barrier `id` learn whether every one of them
+// passed v (bar.red.and): the epilogue warps leave their loop together.
+__device__ __forceinline__ bool group_all(uint32_t id, uint32_t count, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, %2, %3, p;\n"
+      " selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"(uint32_t(v)), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ uint32_t to_e4m3(float v) {
+  return uint32_t(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
+}
+__device__ __forceinline__ float from_e4m3(uint32_t b) {
+  return __half2float(__half(__nv_cvt_fp8_to_halfraw(__nv_fp8_storage_t(b), __NV_E4M3)));
+}
+
+// Per-launch geometry, the same on host and device.
+struct Geo {
+  int K, nsb, groups;        // reduction length, scale bytes per weight row, SF groups
+  int nbox_main, tail;       // 128-K boxes from the main map; K % 128 (0: no tail box)
+  int nbox, nstage;          // boxes per unit (main + tail), stages of 2 boxes
+  int NT, N;                 // B terms; MMA N = NT nb
+  int box_rows;              // A rows per TMA box: 64 (gate and up halves) or 128
+  int a_stage, b_stage;      // bytes per stage
+  int sc_a, sc_b, sc_buf;    // scale bytes per unit: A rows, one B table, buffer stride
+  int stages;                // ring depth
+  int off_b, off_sc, off_xch, off_bars, total;
+};
+
+template <Mode M>
+__host__ __device__ inline Geo geometry(int d, int W, int nb, int ld_sx, int stages) {
+  Geo g{};
+  g.K = (M == Mode::GateUp) ? d : W;
+  g.nsb = g.K / 32;
+  g.groups = (g.nsb + 3) / 4;
+  g.nbox_main = g.K / kBoxK;
+  g.tail = g.K % kBoxK;
+  g.nbox = g.nbox_main + (g.tail ? 1 : 0);
+  g.nstage = (g.nbox + 1) / 2;
+  g.NT = (M == Mode::GateUp) ? kXTerms : kHTerms;
+  g.N = g.NT * nb;
+  g.box_rows = (M == Mode::GateUp) ? kMW / 2 : kMW;
+  g.a_stage = 2 * kBoxBytesA;
+  g.b_stage = 2 * g.N * kBoxK;
+  g.sc_a = (kMW * g.nsb + 15) / 16 * 16;
+  g.sc_b = (M == Mode::GateUp) ? nb * ld_sx : 0;
+  g.sc_buf = g.sc_a + 2 * g.sc_b;
+  g.stages = stages;
+  int off = stages * g.a_stage;
+  g.off_b = off;
+  off += stages * g.b_stage;
+  g.off_sc = off;
+  off += 2 * g.sc_buf;
+  g.off_xch = off;
+  off += (M == Mode::GateUp) ? (kMW / 2) * kNB * 4 : 0;
+  off = (off + 7) & ~7;
+  g.off_bars = off;
+  off += kNumBars * 8 + 16;
+  g.total = off;
+  return g;
+}
+
+struct Unit {
+  int e, r0, n, mt;   // expert, first permuted row of the chunk, tokens in it, weight tile
+};
+
+__device__ __forceinline__ int expert_of_chunk(const int32_t* mtile_off, int E, int g) {
+  int lo = 0, hi = E;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(mtile_off + mid) <= g) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ Unit unit_of(const GemmArgs& a, int n_mt, int u) {
+  const int g = u / n_mt;
+  Unit w;
+  w.mt = u - g * n_mt;
+  w.e = expert_of_chunk(a.mtile_off, a.E, g);
+  w.r0 = __ldg(a.offsets + w.e) + (g - __ldg(a.mtile_off + w.e)) * a.nb;
+  w.n = min(a.nb, __ldg(a.offsets + w.e + 1) - w.r0);
+  return w;
+}
+
+// Scale bytes 4g..4g+3 of a row (bytes at or past nsb read as 0).
+__device__ __forceinline__ uint32_t scale_word(const uint8_t* row, int g, int nsb) {
+  uint32_t w = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    if (4 * g + j < nsb) w |= uint32_t(row[4 * g + j]) << (8 * j);
+  return w;
+}
+
+// ------------------------------------------------------------- kernel --
+
+template <Mode M>
+__global__ void __launch_bounds__(kThreads, 1)
+moe_expert_gemm_mx(const __grid_constant__ CUtensorMap map_w,     // main codes
+                   const __grid_constant__ CUtensorMap map_wt,    // tail codes
+                   const __grid_constant__ CUtensorMap map_b0,    // activation terms
+                   const __grid_constant__ CUtensorMap map_b1,
+                   const __grid_constant__ CUtensorMap map_b2,
+                   const __grid_constant__ CUtensorMap map_b3,
+                   const GemmArgs a, const int stages) {
+  constexpr bool kGateUp = (M == Mode::GateUp);
+  const Geo G = geometry<M>(a.d, a.W, a.nb, a.ld_sx, stages);
+  const int rpe = kGateUp ? 2 * a.W : a.d;           // weight rows per expert
+  const int n_out = kGateUp ? a.W : a.d;
+  const int rows_per_tile = kGateUp ? kMW / 2 : kMW;
+  const int n_mt = (n_out + rows_per_tile - 1) / rows_per_tile;
+  const int S = G.stages;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sa = smem;
+  uint8_t* sb = smem + G.off_b;
+  uint8_t* scb = smem + G.off_sc;
+  float* xch = reinterpret_cast<float*>(smem + G.off_xch);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + G.off_bars);
+  uint64_t* full = bars;
+  uint64_t* empty = full + kMaxStages;
+  uint64_t* sc_full = empty + kMaxStages;
+  uint64_t* sc_empty = sc_full + 2;
+  uint64_t* sf_full = sc_empty + 2;
+  uint64_t* sf_empty = sf_full + 2;
+  uint64_t* acc_full = sf_empty + 2;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* mma_done = acc_empty + 2;
+  uint32_t* tmem_base_p = reinterpret_cast<uint32_t*>(smem + G.off_bars + kNumBars * 8);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + G.off_bars + kNumBars * 8 + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kMaxStages; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      ptx::mbar_init(&sc_full[s], 1);
+      ptx::mbar_init(&sc_empty[s], 4);
+      ptx::mbar_init(&sf_full[s], 4);
+      ptx::mbar_init(&sf_empty[s], 1);
+      ptx::mbar_init(&acc_full[s], 1);
+      ptx::mbar_init(&acc_empty[s], 4);
+    }
+    ptx::mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == kWarpTmem) {
+    ptx::tmem_alloc(tmem_base_p, kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_base_p;
+  // TMEM columns: accumulators, then per SF set (2) the A and the B columns
+  const uint32_t sfa_col0 = 2 * kAccCols;
+  const uint32_t sfb_col0 = 2 * kAccCols + 2 * 4 * G.groups;
+  pdl_wait();
+  if (kGateUp) pdl_trigger();
+  const int units = __ldg(a.mtile_off + a.E) * n_mt;
+
+  if (warp == kWarpProd) {
+    // ------------------------------------------------------------ producer --
+    if (ptx::elect_one()) {
+      ptx::tma_prefetch_desc(&map_w);
+      if (G.tail) ptx::tma_prefetch_desc(&map_wt);
+      const CUtensorMap* mb[4] = {&map_b0, &map_b1, &map_b2, &map_b3};
+      for (int t = 0; t < G.NT; ++t) ptx::tma_prefetch_desc(mb[t]);
+      const uint8_t* wscale = kGateUp ? a.w_gu_scale : a.w_dn_scale;
+      Ring st;
+      Inflight in_st, in_sc;
+      bool ok = true;
+      int q = 0;
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++q) {
+        const Unit w = unit_of(a, n_mt, u);
+        const int sbuf = q & 1;
+        if (!wait_phase(&sc_empty[sbuf], ((q >> 1) & 1) ^ 1, abort_flag, a.status, 64, 5)) { ok = false; break; }
+        uint8_t* dst = scb + sbuf * G.sc_buf;
+        int row_a, row_b;
+        if constexpr (kGateUp) {
+          const int n0 = w.mt * (kMW / 2);
+          const int nrows = min(kMW / 2, a.W - n0);
+          row_a = w.e * rpe + n0;
+          row_b = w.e * rpe + a.W + n0;
+          const uint32_t bytes = uint32_t(nrows * G.nsb);
+          const uint32_t bbytes = uint32_t(G.sc_b);
+          ptx::mbar_arrive_expect_tx(&sc_full[sbuf], 2 * bytes + 2 * bbytes);
+          ptx::bulk_load(dst, wscale + size_t(row_a) * G.nsb, bytes, &sc_full[sbuf]);
+          ptx::bulk_load(dst + (kMW / 2) * G.nsb, wscale + size_t(row_b) * G.nsb, bytes, &sc_full[sbuf]);
+          ptx::bulk_load(dst + G.sc_a, a.sx_hi + size_t(w.r0) * a.ld_sx, bbytes, &sc_full[sbuf]);
+          ptx::bulk_load(dst + G.sc_a + G.sc_b, a.sx_lo + size_t(w.r0) * a.ld_sx, bbytes, &sc_full[sbuf]);
+        } else {
+          const int m0 = w.mt * kMW;
+          const int nrows = min(kMW, a.d - m0);
+          row_a = w.e * rpe + m0;
+          row_b = row_a;
+          const uint32_t bytes = uint32_t(nrows * G.nsb);
+          ptx::mbar_arrive_expect_tx(&sc_full[sbuf], bytes);
+          ptx::bulk_load(dst, wscale + size_t(row_a) * G.nsb, bytes, &sc_full[sbuf]);
+        }
+        in_sc.mark(sbuf, (q >> 1) & 1);
+        for (int s = 0; s < G.nstage; ++s) {
+          if (!wait_phase(&empty[st.slot], st.phase ^ 1, abort_flag, a.status, 64, 4)) { ok = false; break; }
+          const int i0 = 2 * s, i1 = min(2 * s + 2, G.nbox);
+          // the 4-bit TMA counts the packed bytes it reads (half of what it writes)
+          ptx::mbar_arrive_expect_tx(&full[st.slot],
+                                     uint32_t((i1 - i0) * (kBoxBytesA / 2 + G.N * kBoxK)));
+          uint8_t* da = sa + st.slot * G.a_stage;
+          uint8_t* db = sb + st.slot * G.b_stage;
+          for (int i = i0; i < i1; ++i) {
+            uint8_t* dai = da + (i - i0) * kBoxBytesA;
+            uint8_t* dbi = db + (i - i0) * G.N * kBoxK;
+            const bool main_box = i < G.nbox_main;
+            const CUtensorMap* mw = main_box ? &map_w : &map_wt;
+            const int xa = main_box ? i * kBoxK : 0;
+            ptx::tma_load_2d(dai, mw, &full[st.slot], xa, row_a);
+            if constexpr (kGateUp)
+              ptx::tma_load_2d(dai + (kMW / 2) * kBoxK, mw, &full[st.slot], xa, row_b);
+            const int xb = i * kBoxK;
+            for (int t = 0; t < G.NT; ++t)
+              ptx::tma_load_2d(dbi + t * a.nb * kBoxK, mb[t], &full[st.slot], xb, w.r0);
+          }
+          in_st.mark(st.slot, st.phase);
+          st.next(S);
+        }
+      }
+      if (!ok) {
+        in_st.drain(full, S);
+        in_sc.drain(sc_full, 2);
+      }
+    }
+  } else if (warp == kWarpMMA) {
+    // ------------------------------------------------------------ MMA issuer --
+    if (ptx::elect_one()) {
+      uint32_t idesc[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) idesc[j] = ptx::idesc_mx(kMW, G.N, j, j);
+      const int tail_off = kBoxK - G.tail;          // first tail code inside the tail box
+      Ring st;
+      bool ok = true;
+      int q = 0;
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++q) {
+        const int buf = q & 1;
+        if (!wait_phase(&acc_empty[buf], ((q >> 1) & 1) ^ 1, abort_flag, a.status, 0, 2)) { ok = false; break; }
+        if (!wait_phase(&sf_full[buf], (q >> 1) & 1, abort_flag, a.status, 0, 3)) { ok = false; break; }
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + buf * kAccCols;
+        const uint32_t sfa = tmem_base + sfa_col0 + buf * 4 * G.groups;
+        const uint32_t sfb = tmem_base + sfb_col0 + buf * 4 * G.groups;
+        uint32_t acc = 0;
+        for (int s = 0; s < G.nstage; ++s) {
+          if (!wait_phase(&full[st.slot], st.phase, abort_flag, a.status, 0, 1)) { ok = false; break; }
+          ptx::tc_fence_after();
+          const uint32_t a_addr = ptx::smem_u32(sa + st.slot * G.a_stage);
+          const uint32_t b_addr = ptx::smem_u32(sb + st.slot * G.b_stage);
+          const int i0 = 2 * s, i1 = min(2 * s + 2, G.nbox);
+          for (int i = i0; i < i1; ++i) {
+            const uint64_t adesc = ptx::desc_kmajor_sw128(a_addr + uint32_t((i - i0) * kBoxBytesA));
+            const uint64_t bdesc = ptx::desc_kmajor_sw128(b_addr + uint32_t((i - i0) * G.N * kBoxK));
+            const uint32_t sf_off = uint32_t(4 * i);     // SF group i: K blocks 4i..4i+3
+            if (i < G.nbox_main) {
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                ptx::mma_mx(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc[j], sfa + sf_off, sfb + sf_off, acc);
+                acc = 1;
+              }
+            } else {
+              for (int j = 0; j < G.tail / 32; ++j) {
+                ptx::mma_mx(d_tmem, adesc + uint64_t((tail_off + 32 * j) >> 4), bdesc + 2 * j, idesc[j],
+                            sfa + sf_off, sfb + sf_off, acc);
+                acc = 1;
+              }
+            }
+          }
+          ptx::mma_commit(&empty[st.slot]);
+          st.next(S);
+        }
+        if (!ok) break;
+        ptx::mma_commit(&acc_full[buf]);
+        ptx::mma_commit(&sf_empty[buf]);
+      }
+      ptx::mma_commit(mma_done);
+      const long long t0 = clock64();
+      while (!ptx::mbar_try_wait(mma_done, 0) && clock64() - t0 < kSpinLimit) {
+      }
+    }
+  } else if (warp >= kWarpSf0 && warp < kWarpSf0 + 4) {
+    // ------------------------------------------------------ scale writers --
+    const int quarter = warp & 3;
+    const uint32_t lane_addr = uint32_t(quarter * 32) << 16;
+    const int m = quarter * 32 + lane;             // weight row of the tile = TMEM lane
+    int q = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x, ++q) {
+      const int sbuf = q & 1;
+      const bool ok = wait_phase(&sc_full[sbuf], (q >> 1) & 1, abort_flag, a.status, 64, 6) &&
+                      wait_phase(&sf_empty[sbuf], ((q >> 1) & 1) ^ 1, abort_flag, a.status, 64, 7);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      const uint8_t* buf = scb + sbuf * G.sc_buf;
+      const uint32_t ta = tmem_base + lane_addr + sfa_col0 + sbuf * 4 * G.groups;
+      const uint32_t tb = tmem_base + lane_addr + sfb_col0 + sbuf * 4 * G.groups;
+      // A: row m's word of group g in all four columns 4g..4g+3 (the MMA reads
+      // column 4g + m / 32)
+      const uint8_t* ra = buf + m * G.nsb;
+      for (int g = 0; g < G.groups; ++g) {
+        const uint32_t wa = scale_word(ra, g, G.nsb);
+        ptx::tmem_st_32x32b_x4(ta + 4 * g, wa, wa, wa, wa);
+      }
+      // B: row n of B (term n / nb of token n % nb) at lane n % 32, column
+      // 4g + n / 32, in every lane quarter.  x terms: the scatter's block
+      // scales (hi table, lo table); h terms: 2^(h_exp - 4t) for every block.
+      const int n0 = lane, n1 = lane + 32;
+      const int t0 = n0 / a.nb, t1 = n1 / a.nb;
+      const uint32_t c0 = uint32_t(127 + a.h_exp - 4 * t0) * 0x01010101u;
+      const uint32_t c1 = uint32_t(127 + a.h_exp - 4 * t1) * 0x01010101u;
+      for (int g = 0; g < G.groups; ++g) {
+        uint32_t w0, w1 = 0;
+        if constexpr (kGateUp) {
+          const uint8_t* tab = buf + G.sc_a + t0 * G.sc_b;
+          w0 = scale_word(tab + (n0 % a.nb) * a.ld_sx, g, G.nsb);
+        } else {
+          w0 = c0;
+          w1 = c1;
+        }
+        if (G.N > 32) ptx::tmem_st_32x32b_x2(tb + 4 * g, w0, w1);
+        else ptx::tmem_st_32x32b_x1(tb + 4 * g, w0);
+      }
+      ptx::tmem_st_wait();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        ptx::mbar_arrive(&sc_empty[sbuf]);
+        ptx::mbar_arrive(&sf_full[sbuf]);
+      }
+    }
+  } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + 4) {
+    // ------------------------------------------------------------ epilogue --
+    const int quarter = warp & 3;
+    const int m = quarter * 32 + lane;             // TMEM lane = weight row of the tile
+    const float hscale = __int_as_float((127 - a.h_exp) << 23);   // 2^-h_exp
+    int q = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x, ++q) {
+      const Unit w = unit_of(a, n_mt, u);
+      const int buf = q & 1;
+      const bool ok0 = wait_phase(&acc_full[buf], (q >> 1) & 1, abort_flag, a.status, 256, 8);
+      if (!group_all(1, 128, ok0)) break;
+      ptx::tc_fence_after();
+      const uint32_t taddr = tmem_base + (uint32_t(quarter * 32) << 16) + buf * kAccCols;
+      // D column t nb + j holds term t of token j (nb = 16)
+      float z[kNB];
+      {
+        uint32_t v[kHTerms][16];
+        ptx::tmem_ld_32x32b_x16(taddr, v[0]);
+        ptx::tmem_ld_32x32b_x16(taddr + kNB, v[1]);
+        if (!kGateUp) {
+          ptx::tmem_ld_32x32b_x16(taddr + 2 * kNB, v[2]);
+          ptx::tmem_ld_32x32b_x16(taddr + 3 * kNB, v[3]);
+        }
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < kNB; ++j) {
+          float acc = __uint_as_float(v[0][j]) + __uint_as_float(v[1][j]);
+          if (!kGateUp) acc += __uint_as_float(v[2][j]) + __uint_as_float(v[3][j]);
+          z[j] = acc;
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&acc_empty[buf]);
+      if constexpr (kGateUp) {
+        const bool is_up = m >= kMW / 2;
+        const int n = w.mt * (kMW / 2) + (m & (kMW / 2 - 1));
+        const bool nvalid = n < a.W;
+        const float bias =
+            nvalid ? __bfloat162float(a.b_gu[size_t(w.e) * 2 * a.W + (is_up ? a.W : 0) + n]) : 0.f;
+        if (is_up) {
+#pragma unroll
+          for (int j = 0; j < kNB; ++j) xch[(m - kMW / 2) * kNB + j] = z[j] + bias;
+        }
+        ptx::named_barrier(2, 128);
+        if (!is_up && nvalid) {
+#pragma unroll
+          for (int j = 0; j < kNB; ++j) {
+            if (j < w.n) {
+              const float gg = fminf(z[j] + bias, a.limit);
+              const float uu = fminf(fmaxf(xch[m * kNB + j], -a.limit), a.limit);
+              const float hv = gg * (1.0f / (1.0f + expf(-a.alpha * gg))) * (uu + 1.0f);
+              float v = hv * hscale;
+              uint8_t* o = a.hq + size_t(w.r0 + j) * a.W + n;
+#pragma unroll
+              for (int t = 0; t < kHTerms; ++t) {         // v = t0 + t1/16 + t2/256 + t3/4096
+                const uint32_t b = to_e4m3(v);
+                o[size_t(t) * a.R * a.W] = uint8_t(b);
+                v = (v - from_e4m3(b)) * 16.f;
+              }
+            }
+          }
+        }
+        ptx::named_barrier(3, 128);              // xch is reused by the next unit
+      } else {
+        const int n = w.mt * kMW + m;
+        if (n < a.d) {
+          const float bias = __bfloat162float(a.b_dn[size_t(w.e) * a.d + n]);
+#pragma unroll
+          for (int j = 0; j < kNB; ++j)
+            if (j < w.n) a.y[size_t(w.r0 + j) * a.d + n] = z[j] + bias;
+        }
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpTmem) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ host --
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// [rows, cols] matrix, box {box_cols, box_rows}, 128-byte swizzle; cols and
+// box_cols count elements of type dt; row_bytes is the row stride.
+cudaError_t make_map(CUtensorMap* map, CUtensorMapDataType dt, const void* base, long long rows,
+                     long long cols, long long row_bytes, int box_cols, int box_rows) {
+  auto enc = get_encode();
+  if (!enc) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {cuuint64_t(cols), cuuint64_t(rows)};
+  const cuuint64_t strides[1] = {cuuint64_t(row_bytes)};
+  const cuuint32_t box[2] = {cuuint32_t(box_cols), cuuint32_t(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+int num_sms() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
+}
+
+template <Mode M>
+int plan_stages(const GemmArgs& a) {
+  const Geo g0 = geometry<M>(a.d, a.W, a.nb, a.ld_sx, 0);
+  const int per = g0.a_stage + g0.b_stage;
+  int s = (kMaxSmem - 1024 - g0.total) / per;
+  return s < kMaxStages ? s : kMaxStages;
+}
+
+// The four tensor maps of one launch.
+template <Mode M>
+cudaError_t make_maps(const GemmArgs& a, CUtensorMap* mw, CUtensorMap* mwt, CUtensorMap* mb) {
+  const bool gu = (M == Mode::GateUp);
+  const int K = gu ? a.d : a.W;
+  const uint8_t* w = gu ? a.w_gu : a.w_dn;
+  const long long rows = gu ? (long long)a.E * 2 * a.W : (long long)a.E * a.d;
+  const int box_rows = gu ? kMW / 2 : kMW;
+  const int kmain = K / kBoxK * kBoxK;
+  cudaError_t e = make_map(mw, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w, rows, kmain, K / 2, kBoxK,
+                           box_rows);
+  if (e == cudaSuccess) {
+    if (K % kBoxK) {
+      // the last 128 codes of each row: base at code K - 128 of row 0
+      e = make_map(mwt, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w + (K - kBoxK) / 2, rows, kBoxK,
+                   K / 2, kBoxK, box_rows);
+    } else {
+      *mwt = *mw;
+    }
+  }
+  const uint8_t* terms[4];
+  if (gu) {
+    terms[0] = terms[2] = a.xq_hi;
+    terms[1] = terms[3] = a.xq_lo;
+  } else {
+    for (int t = 0; t < 4; ++t) terms[t] = a.hq + size_t(t) * a.R * a.W;
+  }
+  for (int t = 0; t < 4 && e == cudaSuccess; ++t)
+    e = make_map(&mb[t], CU_TENSOR_MAP_DATA_TYPE_UINT8, terms[t], a.R, K, K, kBoxK, a.nb);
+  return e;
+}
+
+template <Mode M>
+bool fits_mode(const GemmArgs& a) {
+  const bool gu = (M == Mode::GateUp);
+  const int K = gu ? a.d : a.W;
+  const int nsb = K / 32;
+  if (K < kBoxK || K % 32 || (K / 2) % 16) return false;
+  if ((K % kBoxK) && ((K - kBoxK) / 2) % 32) return false;      // tail map base alignment
+  if ((nsb + 3) / 4 > kMaxGroups) return false;
+  // 1-D copies of scale rows: 16-byte sizes and starts
+  const int rpe = gu ? 2 * a.W : a.d;
+  if ((size_t(rpe) * nsb) % 16) return false;
+  if (gu) {
+    if ((64 * nsb) % 16 || ((a.W % 64) * nsb) % 16) return false;
+  } else {
+    if ((128 * nsb) % 16 || ((a.d % 128) * nsb) % 16) return false;
+  }
+  return plan_stages<M>(a) >= 2;
+}
+
+template <Mode M>
+cudaError_t launch(const GemmArgs& a, cudaStream_t s) {
+  if (a.nb != kNB || !fits_mode<M>(a)) return cudaErrorInvalidConfiguration;
+  const int stages = plan_stages<M>(a);
+  const Geo g = geometry<M>(a.d, a.W, a.nb, a.ld_sx, stages);
+  const size_t smem = size_t(g.total) + 1024;
+  if (smem > size_t(kMaxSmem)) return cudaErrorInvalidConfiguration;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(moe_expert_gemm_mx<M>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  CUtensorMap mw, mwt, mb[4];
+  cudaError_t e = make_maps<M>(a, &mw, &mwt, mb);
+  if (e != cudaSuccess) return e;
+  const int n_out = (M == Mode::GateUp) ? a.W : a.d;
+  const int rows_per_tile = (M == Mode::GateUp) ? kMW / 2 : kMW;
+  const long long n_mt = (n_out + rows_per_tile - 1) / rows_per_tile;
+  const long long units_bound = (long long)(a.R / a.nb + a.E) * n_mt;
+  const int grid = int(units_bound < num_sms() ? units_bound : num_sms());
+  return launch_pdl(moe_expert_gemm_mx<M>, dim3(grid), dim3(kThreads), smem, s, mw, mwt, mb[0], mb[1],
+                    mb[2], mb[3], a, stages);
+}
+
+}  // namespace
+
+int mx_chunk(int64_t, int) { return kNB; }
+
+int mx_hidden_exp(float limit) {
+  // |h| = |g sigmoid(alpha g) (u + 1)| <= limit (limit + 1) for the clamped g, u
+  const double bound = double(limit) * (double(limit) + 1.0);
+  int e = 0;
+  while (bound * std::ldexp(1.0, -e) > 448.0) ++e;
+  while (e > -20 && bound * std::ldexp(1.0, -(e - 1)) <= 448.0) --e;
+  return e;
+}
+
+bool mx_fits(const GemmArgs& args, float limit) {
+  // h is carried with a fixed scale, so the clamp must bound it, and tightly
+  // enough that typical values stay far above the E4M3 subnormals
+  if (!(limit > 0.f) || !std::isfinite(limit) || limit > 16.f) return false;
+  GemmArgs a = args;
+  a.nb = mx_chunk(a.R, a.E);
+  if (a.R / (a.E > 0 ? a.E : 1) > 8) return false;              // a decode-sized load
+  a.ld_sx = scale_row_bytes(a.d);
+  return fits_mode<Mode::GateUp>(a) && fits_mode<Mode::Down>(a);
+}
+
+cudaError_t launch_gateup_mx(const GemmArgs& a, cudaStream_t s) { return launch<Mode::GateUp>(a, s); }
+cudaError_t launch_down_mx(const GemmArgs& a, cudaStream_t s) { return launch<Mode::Down>(a, s); }
+
+}  // namespace moe

@@ -34,11 +34,15 @@
 //            largest scale byte of weight row n; B = x · 2^e_t in f16 (the
 //            permute stage scales each token so its largest |x| lies in
 //            [2^14, 2^15), which holds every bf16 value).  The epilogue
-//            multiplies by 2^(r_n - 127) · 2^(-e_t).  Exact while a row's scales
-//            lie within 2^23 of its largest.
-//   down:    A = E2M1 -> f16 bits moved into a bf16 field (a factor 2^-112)
-//            times 2^(s - 15), exact for every scale byte <= 142; B = h as two
-//            bf16 terms (hi + lo), two MMAs per K step.
+//            multiplies by 2^(r_n - 127) · 2^(-e_t).  Exact for scale bytes up
+//            to 240 whose block lies within 2^14 of its row's largest; a block
+//            further below contributes nothing (its factor would be an f16
+//            subnormal).
+//   down:    when the clamp bounds h inside the f16 range, as gate_up with
+//            B = h as two f16 terms (hi + lo); otherwise A = E2M1 -> f16 bits
+//            moved into a bf16 field (a factor 2^-112) times 2^(s - 15), exact
+//            for every scale byte <= 142, and B = h as two bf16 terms.  Two MMAs
+//            per K step (hi, lo).
 #include "common.cuh"
 #include "tc_ptx.cuh"
 
@@ -56,7 +60,7 @@ constexpr int kNBMax = kGemmBM;              // largest token chunk (MMA N)
 constexpr int kMW = 128;                     // weight rows per unit (MMA M, TMEM lanes)
 constexpr int kSK = 256;                     // K per stage: 128 B of codes per row, 128 TMEM columns of A
 constexpr int kACols = kSK / 2;              // TMEM columns per A stage
-constexpr int kMaxC = 8;                     // code-ring depth, most
+constexpr int kMaxC = 12;                    // code-ring depth, most
 constexpr int kMaxA = 3;                     // A-ring depth, most
 constexpr int kMaxB = 16;                    // activation-ring depth, most
 constexpr int kRing = 4;                     // per-unit row-factor ring
@@ -166,14 +170,16 @@ __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volat
                                            int32_t* status, uint32_t backoff_ns = 0) {
   if (ptx::mbar_try_wait_sleep(bar, parity, 20000u)) return true;
   const long long t0 = clock64();
-  while (true) {
+  for (uint32_t n = 1;; ++n) {
     if (backoff_ns) __nanosleep(backoff_ns);
     if (ptx::mbar_try_wait_sleep(bar, parity, 20000u)) return true;
-    if (*abort_flag) return false;
-    if (clock64() - t0 > kSpinLimit) {
-      *abort_flag = 1;
-      atomicMax(status, kStatusTimeout);
-      return false;
+    if ((n & 31) == 0) {                        // the abort flag and the clock, now and then
+      if (*abort_flag) return false;
+      if (clock64() - t0 > kSpinLimit) {
+        *abort_flag = 1;
+        atomicMax(status, kStatusTimeout);
+        return false;
+      }
     }
   }
 }
@@ -641,6 +647,7 @@ moe_expert_gemm_tmem(const __grid_constant__ CUtensorMap map_w,
       int rn = 0;
       if (F16 && valid)
         rn = row_max_byte(reinterpret_cast<const uint32_t*>(scb + sb * L.scbuf), uint32_t(sr * nsb), nsb);
+      const uint32_t rnb = uint32_t(rn) * 0x0101u;   // r_n in the two low bytes
       if (part == 0) {
         ok = __all_sync(0xffffffffu, wait_phase(&rf_empty[ring], ((q / kRing) & 1) ^ 1, abort_flag, a.status));
         if (!ok) break;
@@ -649,7 +656,7 @@ moe_expert_gemm_tmem(const __grid_constant__ CUtensorMap map_w,
         if (lane == 0) ptx::mbar_arrive(&rf_full[ring]);
       }
       for (int cs = 0; cs < nS; ++cs) {
-        ok = __all_sync(0xffffffffu, wait_phase(&code_full[cr.slot], cr.phase, abort_flag, a.status));
+        ok = __all_sync(0xffffffffu, wait_phase(&code_full[cr.slot], cr.phase, abort_flag, a.status, 32));
         if (!ok) break;
         const uint8_t* cst = codes + cr.slot * kCodeStageBytes;
         // this thread's 2 scale blocks: one 16-bit read when the row starts at
@@ -662,8 +669,20 @@ moe_expert_gemm_tmem(const __grid_constant__ CUtensorMap map_w,
           else if ((reinterpret_cast<uintptr_t>(sp) & 1u) == 0) s01 = *reinterpret_cast<const uint16_t*>(sp);
           else s01 = uint32_t(sp[0]) | (uint32_t(sp[1]) << 8);
         }
-        const uint32_t f0 = (valid && b0 < nsb) ? Dequant<DQ>::factor(int(s01 & 0xFF), rn) : 0u;
-        const uint32_t f1 = (valid && b0 + 1 < nsb) ? Dequant<DQ>::factor(int(s01 >> 8), rn) : 0u;
+        uint32_t f0, f1;
+        if (F16) {
+          // 2^(s - r_n) as f16x2 for both blocks at once: byte-wise s + 15 - r_n
+          // (s <= r_n; at most 15; 0 below the f16 normal range, where the
+          // factor becomes 0), moved into both halves' exponent fields
+          const uint32_t e2 = __vsubus4(__vaddus4(s01, 0x0F0Fu), rnb) & 0x1F1Fu;
+          f0 = (__byte_perm(e2, 0, 0x4040) << 10);
+          f1 = (__byte_perm(e2, 0, 0x4141) << 10);
+          if (!(valid && b0 < nsb)) f0 = 0u;
+          if (!(valid && b0 + 1 < nsb)) f1 = 0u;
+        } else {
+          f0 = (valid && b0 < nsb) ? Dequant<DQ>::factor(int(s01 & 0xFF), rn) : 0u;
+          f1 = (valid && b0 + 1 < nsb) ? Dequant<DQ>::factor(int(s01 >> 8), rn) : 0u;
+        }
         // 64 codes: 2 x 16 bytes of the 128-byte swizzled row
         const uint4 x0 = *reinterpret_cast<const uint4*>(cst + choff0);
         const uint4 x1 = *reinterpret_cast<const uint4*>(cst + choff1);
@@ -680,7 +699,7 @@ moe_expert_gemm_tmem(const __grid_constant__ CUtensorMap map_w,
         Dequant<DQ>::convert(x1.y, f1, &r[20]);
         Dequant<DQ>::convert(x1.z, f1, &r[24]);
         Dequant<DQ>::convert(x1.w, f1, &r[28]);
-        ok = __all_sync(0xffffffffu, wait_phase(&a_empty[ar.slot], ar.phase ^ 1, abort_flag, a.status));
+        ok = __all_sync(0xffffffffu, wait_phase(&a_empty[ar.slot], ar.phase ^ 1, abort_flag, a.status, 32));
         if (!ok) break;
         ptx::tmem_st_32x32b_x32(tmem_base + lane_addr + a_col0 + ar.slot * kACols + part * 32, r);
         ptx::tmem_st_wait();
@@ -746,17 +765,28 @@ int num_sms() {
   return n;
 }
 
-// Ring depths for one launch: deep code prefetch when the kernel streams
-// weights (small chunks), a deep activation ring in whatever shared memory is
-// left (at most kMaxB stages).
+// Ring depths for one launch.  The weight codes stream from HBM, whose
+// latency under load is several microseconds, so after a modest activation
+// ring (the activations are L2-resident) every remaining byte of shared memory
+// holds code stages in flight: about 10 x 16 KB at decode.
 template <Mode M>
 void plan(GemmArgs& a) {
   const int K = (M == Mode::GateUp) ? a.d : a.W;
-  a.stages_c = a.nb <= 32 ? 6 : 3;
-  const Lay base = layout<M>(K / 32, a.nb, a.stages_c, 0);
-  const int room = kMaxSmem - 1024 - base.total;
-  const int per = layout<M>(K / 32, a.nb, a.stages_c, 1).bstage;
-  a.stages_b = room / per < kMaxB ? room / per : kMaxB;
+  const int per_b = layout<M>(K / 32, a.nb, 0, 1).bstage;
+  int nbs;
+  if (a.nb <= 32) {
+    nbs = (48 * 1024) / per_b;                              // ~48 KB of activations
+  } else {
+    const Lay base = layout<M>(K / 32, a.nb, 3, 0);         // keep 3 code stages
+    nbs = (kMaxSmem - 1024 - base.total) / per_b;
+  }
+  nbs = nbs < 2 ? 2 : nbs;
+  nbs = nbs < kMaxB ? nbs : kMaxB;
+  const Lay base1 = layout<M>(K / 32, a.nb, 0, nbs);
+  int nc = (kMaxSmem - 1024 - base1.total) / kCodeStageBytes;
+  nc = nc < kMaxC ? nc : kMaxC;
+  a.stages_b = nbs;
+  a.stages_c = nc;
 }
 
 template <Mode M>
@@ -770,8 +800,8 @@ cudaError_t launch(const GemmArgs& args, cudaStream_t s) {
   GemmArgs a = args;
   plan<M>(a);
   const size_t smem = smem_bytes<M>(a);
-  if (a.stages_b < 2 || smem > size_t(kMaxSmem) || a.nb < 16 || a.nb > kNBMax || a.nb % 16 ||
-      a_stages(a.nb) < 2)
+  if (a.stages_b < 2 || a.stages_c < 2 || smem > size_t(kMaxSmem) || a.nb < 16 || a.nb > kNBMax ||
+      a.nb % 16 || a_stages(a.nb) < 2)
     return cudaErrorInvalidConfiguration;
   static bool configured = false;
   if (!configured) {
@@ -820,7 +850,8 @@ bool expert_gemm_tmem_fits(const GemmArgs& args) {
   GemmArgs g = a, d = a;
   plan<Mode::GateUp>(g);
   plan<Mode::Down>(d);
-  return g.stages_b >= 2 && d.stages_b >= 2 && smem_bytes<Mode::GateUp>(g) <= size_t(kMaxSmem) &&
+  return g.stages_b >= 2 && d.stages_b >= 2 && g.stages_c >= 2 && d.stages_c >= 2 &&
+         smem_bytes<Mode::GateUp>(g) <= size_t(kMaxSmem) &&
          smem_bytes<Mode::Down>(d) <= size_t(kMaxSmem);
 }
 cudaError_t launch_gateup_tmem(const GemmArgs& a, cudaStream_t s) { return launch<Mode::GateUp, true>(a, s); }

@@ -72,14 +72,25 @@ moe_status check_device() {
   return MOE_OK;
 }
 
-// Which grouped-GEMM design runs K3/K4.  The weight-in-TMEM kernels are the
-// default wherever their shared-memory plan fits; MOE_GEMM=smem selects the
-// kernels that stage dequantised weights in shared memory (a diagnostic and
-// tuning knob; both produce results within the same tolerances).
-bool use_tmem_gemm(const moe::GemmArgs& a) {
+// Which grouped-GEMM design runs K3/K4:
+//   Mx    block-scaled MMA on the E2M1 codes (expert_gemm_mx.cu): decode-sized
+//         loads (a few rows per expert) with a clamp that bounds h
+//   Tmem  dequantised weights as the MMA's A operand in tensor memory
+//   Smem  dequantised weights staged in shared memory
+// The first that fits is used; MOE_GEMM=tmem or MOE_GEMM=smem skips the ones
+// before it (a diagnostic and tuning knob; all meet the same tolerances).
+enum class Design { Smem, Tmem, Mx };
+
+moe::GemmArgs gemm_args(int64_t T, int d, int W, int E, int k);
+
+Design gemm_design(int64_t T, int d, int W, int E, int k, float limit) {
+  const moe::GemmArgs a = gemm_args(T, d, W, E, k);
   const char* s = getenv("MOE_GEMM");
-  if (s && strcmp(s, "smem") == 0) return false;
-  return moe::expert_gemm_tmem_fits(a);
+  const bool no_mx = s && (strcmp(s, "tmem") == 0 || strcmp(s, "smem") == 0);
+  const bool no_tmem = s && strcmp(s, "smem") == 0;
+  if (!no_mx && moe::mx_fits(a, limit)) return Design::Mx;
+  if (!no_tmem && moe::expert_gemm_tmem_fits(a)) return Design::Tmem;
+  return Design::Smem;
 }
 
 moe::GemmArgs gemm_args(int64_t T, int d, int W, int E, int k) {
@@ -111,6 +122,12 @@ struct RouteOut {
   int32_t* rowexp;
   void* x_perm;
   int32_t* status;
+  // block-scaled design: E4M3 pairs and their block scales
+  uint8_t* xq_hi;
+  uint8_t* xq_lo;
+  uint8_t* sx_hi;
+  uint8_t* sx_lo;
+  int ld_sx;
 };
 
 RouteOut route_tables(void* ws, const moe::Workspace& L, bool gather) {
@@ -128,6 +145,11 @@ RouteOut route_tables(void* ws, const moe::Workspace& L, bool gather) {
   r.rowexp = at<int32_t>(ws, L.rowexp);
   r.x_perm = gather ? at<void>(ws, L.x_perm) : nullptr;
   r.status = at<int32_t>(ws, L.status);
+  r.xq_hi = nullptr;
+  r.xq_lo = nullptr;
+  r.sx_hi = nullptr;
+  r.sx_lo = nullptr;
+  r.ld_sx = 0;
   return r;
 }
 
@@ -147,8 +169,13 @@ moe_status run_route(const void* x, int64_t T, int d, const float* rw, const flo
     if (e != cudaSuccess) return cuda_fail(e, "route_scan launch");
   }
   if ((e = trace(2, s)) != cudaSuccess) return cuda_fail(e, "trace event");
-  e = moe::launch_route_scatter(xb, int(T), d, E, k, r.topk_idx, r.rank, r.tile_base, r.perm,
-                                r.inv, r.x_perm, r.rowexp, r.status, s);
+  if (r.xq_hi) {
+    e = moe::launch_route_scatter_mx(xb, int(T), d, E, k, r.topk_idx, r.rank, r.tile_base, r.perm,
+                                     r.inv, r.xq_hi, r.xq_lo, r.sx_hi, r.sx_lo, r.ld_sx, r.status, s);
+  } else {
+    e = moe::launch_route_scatter(xb, int(T), d, E, k, r.topk_idx, r.rank, r.tile_base, r.perm,
+                                  r.inv, r.x_perm, r.rowexp, r.status, s);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "route_scatter launch");
   if ((e = trace(3, s)) != cudaSuccess) return cuda_fail(e, "trace event");
   return MOE_OK;
@@ -215,10 +242,25 @@ moe_status moe_forward(const void* x_bf16, int64_t T, int d, int W, const float*
   if (st != MOE_OK) return st;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const RouteOut r = route_tables(workspace, L, true);
+  RouteOut r = route_tables(workspace, L, true);
   moe::GemmArgs a = gemm_args(T, d, W, E, k);
-  const bool tmem = use_tmem_gemm(a);
+  Design design = gemm_design(T, d, W, E, k, limit);
+  // the block-scaled path reads the weights with 4-bit TMA maps, whose base
+  // addresses want 32-byte alignment (the tail map starts inside a row)
+  if (design == Design::Mx &&
+      ((reinterpret_cast<uintptr_t>(w_gu_fp4) | reinterpret_cast<uintptr_t>(w_dn_fp4)) & 31u))
+    design = moe::expert_gemm_tmem_fits(a) ? Design::Tmem : Design::Smem;
+  const bool tmem = design == Design::Tmem;
+  const bool mx = design == Design::Mx;
   if (tmem) a.nb = moe::expert_gemm_tmem_chunk(a.R, E);
+  if (mx) {
+    a.nb = moe::mx_chunk(a.R, E);
+    r.xq_hi = at<uint8_t>(workspace, L.x_perm);
+    r.xq_lo = at<uint8_t>(workspace, L.x_perm + size_t(a.R) * d);
+    r.sx_hi = at<uint8_t>(workspace, L.sx_hi);
+    r.sx_lo = at<uint8_t>(workspace, L.sx_lo);
+    r.ld_sx = moe::scale_row_bytes(d);
+  }
   cudaError_t e = trace(0, s);
   if (e != cudaSuccess) return cuda_fail(e, "trace event");
   st = run_route(x_bf16, T, d, router_w, router_b, E, k, a.nb, r, s);
@@ -241,10 +283,19 @@ moe_status moe_forward(const void* x_bf16, int64_t T, int d, int W, const float*
   a.h_lo = at<__nv_bfloat16>(workspace, L.h_lo);
   a.y = at<float>(workspace, L.y);
   a.status = r.status;
-  e = tmem ? moe::launch_gateup_tmem(a, s) : moe::launch_gateup(a, s);
+  if (mx) {
+    a.xq_hi = r.xq_hi;
+    a.xq_lo = r.xq_lo;
+    a.sx_hi = r.sx_hi;
+    a.sx_lo = r.sx_lo;
+    a.ld_sx = r.ld_sx;
+    a.hq = at<uint8_t>(workspace, L.h_hi);
+    a.h_exp = moe::mx_hidden_exp(limit);
+  }
+  e = mx ? moe::launch_gateup_mx(a, s) : tmem ? moe::launch_gateup_tmem(a, s) : moe::launch_gateup(a, s);
   if (e != cudaSuccess) return cuda_fail(e, "gate_up launch");
   if ((e = trace(4, s)) != cudaSuccess) return cuda_fail(e, "trace event");
-  e = tmem ? moe::launch_down_tmem(a, s) : moe::launch_down(a, s);
+  e = mx ? moe::launch_down_mx(a, s) : tmem ? moe::launch_down_tmem(a, s) : moe::launch_down(a, s);
   if (e != cudaSuccess) return cuda_fail(e, "down launch");
   if ((e = trace(5, s)) != cudaSuccess) return cuda_fail(e, "trace event");
   e = moe::launch_combine(a.y, r.topk_w, r.inv, int(T), d, k,
@@ -307,12 +358,21 @@ moe_status moe_poll_status(const void* workspace, void* stream) {
 
 const char* moe_last_error(void) { return g_last_error.c_str(); }
 
-moe_status moe_hidden_format(int64_t T, int d, int W, int E, int k, float limit, int* is_f16) {
+moe_status moe_hidden_format(int64_t T, int d, int W, int E, int k, float limit, int* format,
+                             int* exponent) {
   moe_status st = check_shape(T, d, W, E, k);
   if (st != MOE_OK) return st;
-  if (!is_f16) return fail(MOE_ERR_NULL, "is_f16 is NULL");
-  const moe::GemmArgs a = gemm_args(T, d, W, E, k);
-  *is_f16 = (T > 0 && use_tmem_gemm(a) && moe::hidden_fits_f16(limit)) ? 1 : 0;
+  if (!format) return fail(MOE_ERR_NULL, "format is NULL");
+  const Design design = T > 0 ? gemm_design(T, d, W, E, k, limit) : Design::Smem;
+  int f = MOE_HIDDEN_BF16_PAIR, x = 0;
+  if (design == Design::Mx) {
+    f = MOE_HIDDEN_E4M3_TERMS;
+    x = moe::mx_hidden_exp(limit);
+  } else if (design == Design::Tmem && moe::hidden_fits_f16(limit)) {
+    f = MOE_HIDDEN_F16_PAIR;
+  }
+  *format = f;
+  if (exponent) *exponent = x;
   return MOE_OK;
 }
 

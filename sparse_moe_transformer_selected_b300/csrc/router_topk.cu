@@ -46,6 +46,7 @@ router_logits_kernel(const __nv_bfloat16* __restrict__ x, const float* __restric
   if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && tid == 0) {
     status[0] = 0;                               // first kernel of a call
     status[1] = 0;                               // top-k tiles done (fused scan)
+    status[4] = 0;                               // which wait of a GEMM timed out, if one did
   }
 
   float acc[4][NPER];

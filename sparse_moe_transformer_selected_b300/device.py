@@ -101,10 +101,28 @@ class DeviceMoE:
                       inv, self.workspace, self.workspace.numel(), stream)
         return idx, w, off, perm, inv
 
+    def hidden_format(self) -> tuple:
+        """(format, exponent) of h on this shape and clamp (moe.HIDDEN_*)."""
+        return moe.moe_hidden_format(self.T, self.d, self.W, self.E, self.k, self.limit)
+
     def hidden_dtype(self) -> torch.dtype:
-        """The 16-bit type of the h_hi / h_lo tables on this shape and clamp."""
-        f16 = moe.moe_hidden_format(self.T, self.d, self.W, self.E, self.k, self.limit)
-        return torch.float16 if f16 else torch.bfloat16
+        """The element type of the h_hi / h_lo tables on this shape and clamp."""
+        fmt, _ = self.hidden_format()
+        return {moe.HIDDEN_F16_PAIR: torch.float16, moe.HIDDEN_BF16_PAIR: torch.bfloat16,
+                moe.HIDDEN_E4M3_TERMS: torch.float8_e4m3fn}[fmt]
+
+    def hidden(self) -> torch.Tensor:
+        """h of every permuted row as fp32 [T*k, W], rebuilt from its stored terms."""
+        fmt, ex = self.hidden_format()
+        R = self.T * self.k
+        if fmt == moe.HIDDEN_E4M3_TERMS:
+            off, _ = moe.moe_workspace_region(self.T, self.d, self.W, self.E, self.k, "h_hi")
+            q = self.workspace[off:off + 4 * R * self.W].view(torch.float8_e4m3fn).view(4, R, self.W)
+            h = torch.zeros((R, self.W), dtype=torch.float64, device=q.device)
+            for t in range(4):
+                h += q[t].double() / 16.0 ** t
+            return (h * 2.0 ** ex).float()
+        return self.region("h_hi").float() + self.region("h_lo").float()
 
     def region(self, which: str) -> torch.Tensor:
         """A view of an intermediate table inside the workspace (after forward)."""
@@ -116,6 +134,7 @@ class DeviceMoE:
             "offsets": (torch.int32, (self.E + 1,)), "perm": (torch.int32, (R,)),
             "inv": (torch.int32, (self.T, self.k)), "x_perm": (torch.float16, (R, self.d)),
             "h_hi": (self.hidden_dtype(), (R, self.W)), "h_lo": (self.hidden_dtype(), (R, self.W)),
+            # (in the E4M3 terms format the four tables start at h_hi; see hidden())
             "y": (torch.float32, (R, self.d)),
         }[which]
         return raw.view(dtype).view(shape)

@@ -71,7 +71,8 @@ def load() -> ctypes.CDLL:
     lib.moe_forward_noalloc.argtypes = [P, I64, I32, I32, P, P, P, P, P, P, P, P, I32, I32, F32,
                                         F32, P, P]
     lib.moe_forward_noalloc.restype = I32
-    lib.moe_hidden_format.argtypes = [I64, I32, I32, I32, I32, F32, ctypes.POINTER(I32)]
+    lib.moe_hidden_format.argtypes = [I64, I32, I32, I32, I32, F32, ctypes.POINTER(I32),
+                                      ctypes.POINTER(I32)]
     lib.moe_hidden_format.restype = I32
     _lib = lib
     return lib
@@ -135,11 +136,20 @@ def moe_poll_status(workspace, stream=None) -> int:
     return _check(load().moe_poll_status(_ptr(workspace), _stream(stream)))
 
 
-def moe_hidden_format(T: int, d: int, W: int, E: int, k: int, limit: float) -> bool:
-    """True when moe_forward carries h as an f16 pair on this shape, else bf16."""
-    v = ctypes.c_int(0)
-    _check(load().moe_hidden_format(T, d, W, E, k, limit, ctypes.byref(v)))
-    return bool(v.value)
+# Number formats of h between the two GEMMs (moe_hidden_format).
+HIDDEN_BF16_PAIR, HIDDEN_F16_PAIR, HIDDEN_E4M3_TERMS = 0, 1, 2
+
+
+def moe_hidden_format(T: int, d: int, W: int, E: int, k: int, limit: float) -> tuple:
+    """(format, exponent): how moe_forward carries h on this shape and clamp.
+
+    HIDDEN_BF16_PAIR / HIDDEN_F16_PAIR: h = hi + lo; HIDDEN_E4M3_TERMS:
+    h = (t0 + t1/16 + t2/256 + t3/4096) * 2**exponent.
+    """
+    f = ctypes.c_int(0)
+    x = ctypes.c_int(0)
+    _check(load().moe_hidden_format(T, d, W, E, k, limit, ctypes.byref(f), ctypes.byref(x)))
+    return f.value, x.value
 
 
 def moe_set_trace_events(events) -> int:

@@ -95,7 +95,7 @@ def test_forward_tiny_with_intermediates():
     rel, worst = _check_full(dev, out, ref, 4)
     # hidden activations h (carried as hi + lo bf16) and expert outputs y
     perm = dev.region("perm").cpu().numpy()
-    h = (dev.region("h_hi").float() + dev.region("h_lo").float()).cpu().numpy().astype(np.float64)
+    h = dev.hidden().cpu().numpy().astype(np.float64)
     y = dev.region("y").cpu().numpy().astype(np.float64)
     for row, q in enumerate(perm):
         t, j = divmod(int(q), 4)
