@@ -299,36 +299,52 @@ moe_expert_gemm_mx(const __grid_constant__ CUtensorMap map_w,     // main codes
       const uint8_t* wscale = kGateUp ? a.w_gu_scale : a.w_dn_scale;
       Ring st;
       Inflight in_st, in_sc;
-      bool ok = true;
-      int q = 0;
-      for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++q) {
-        const Unit w = unit_of(a, n_mt, u);
-        const int sbuf = q & 1;
-        if (!wait_phase(&sc_empty[sbuf], ((q >> 1) & 1) ^ 1, abort_flag, a.status, 64, 5)) { ok = false; break; }
-        uint8_t* dst = scb + sbuf * G.sc_buf;
-        int row_a, row_b;
+      // weight rows of a unit: gate and up halves (gate_up) or one block (down)
+      auto rows_of = [&](const Unit& w, int& ra, int& rb, int& nrows) {
         if constexpr (kGateUp) {
           const int n0 = w.mt * (kMW / 2);
-          const int nrows = min(kMW / 2, a.W - n0);
-          row_a = w.e * rpe + n0;
-          row_b = w.e * rpe + a.W + n0;
-          const uint32_t bytes = uint32_t(nrows * G.nsb);
+          nrows = min(kMW / 2, a.W - n0);
+          ra = w.e * rpe + n0;
+          rb = w.e * rpe + a.W + n0;
+        } else {
+          const int m0 = w.mt * kMW;
+          nrows = min(kMW, a.d - m0);
+          ra = w.e * rpe + m0;
+          rb = ra;
+        }
+      };
+      // The scale rows of unit number qq (its index in this CTA's sequence) go
+      // to buffer qq & 1 one unit ahead of its stages, so the scale writers
+      // have them in TMEM before the MMA reaches the unit.
+      auto load_scales = [&](int uu, int qq) -> bool {
+        const Unit w = unit_of(a, n_mt, uu);
+        const int sbuf = qq & 1;
+        if (!wait_phase(&sc_empty[sbuf], ((qq >> 1) & 1) ^ 1, abort_flag, a.status, 64, 5)) return false;
+        uint8_t* dst = scb + sbuf * G.sc_buf;
+        int ra, rb, nrows;
+        rows_of(w, ra, rb, nrows);
+        const uint32_t bytes = uint32_t(nrows * G.nsb);
+        if constexpr (kGateUp) {
           const uint32_t bbytes = uint32_t(G.sc_b);
           ptx::mbar_arrive_expect_tx(&sc_full[sbuf], 2 * bytes + 2 * bbytes);
-          ptx::bulk_load(dst, wscale + size_t(row_a) * G.nsb, bytes, &sc_full[sbuf]);
-          ptx::bulk_load(dst + (kMW / 2) * G.nsb, wscale + size_t(row_b) * G.nsb, bytes, &sc_full[sbuf]);
+          ptx::bulk_load(dst, wscale + size_t(ra) * G.nsb, bytes, &sc_full[sbuf]);
+          ptx::bulk_load(dst + (kMW / 2) * G.nsb, wscale + size_t(rb) * G.nsb, bytes, &sc_full[sbuf]);
           ptx::bulk_load(dst + G.sc_a, a.sx_hi + size_t(w.r0) * a.ld_sx, bbytes, &sc_full[sbuf]);
           ptx::bulk_load(dst + G.sc_a + G.sc_b, a.sx_lo + size_t(w.r0) * a.ld_sx, bbytes, &sc_full[sbuf]);
         } else {
-          const int m0 = w.mt * kMW;
-          const int nrows = min(kMW, a.d - m0);
-          row_a = w.e * rpe + m0;
-          row_b = row_a;
-          const uint32_t bytes = uint32_t(nrows * G.nsb);
           ptx::mbar_arrive_expect_tx(&sc_full[sbuf], bytes);
-          ptx::bulk_load(dst, wscale + size_t(row_a) * G.nsb, bytes, &sc_full[sbuf]);
+          ptx::bulk_load(dst, wscale + size_t(ra) * G.nsb, bytes, &sc_full[sbuf]);
         }
-        in_sc.mark(sbuf, (q >> 1) & 1);
+        in_sc.mark(sbuf, (qq >> 1) & 1);
+        return true;
+      };
+      bool ok = blockIdx.x >= units || load_scales(blockIdx.x, 0);
+      int q = 0;
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++q) {
+        const Unit w = unit_of(a, n_mt, u);
+        if (u + int(gridDim.x) < units && !load_scales(u + int(gridDim.x), q + 1)) { ok = false; break; }
+        int row_a, row_b, nrows;
+        rows_of(w, row_a, row_b, nrows);
         for (int s = 0; s < G.nstage; ++s) {
           if (!wait_phase(&empty[st.slot], st.phase ^ 1, abort_flag, a.status, 64, 4)) { ok = false; break; }
           const int i0 = 2 * s, i1 = min(2 * s + 2, G.nbox);
