@@ -37,13 +37,26 @@ from sparse_moe_transformer_selected_b300 import inputs as gen  # noqa: E402
 
 METRIC = "MoE-layer tokens/s at 20b/120b shapes; % of HBM or tensor-pipe roofline"
 STAGES = ["router_topk", "route_scan", "route_scatter", "gate_up", "down", "combine"]
-# kernels one moe_forward launches: router logits, router top-k, scan, scatter,
+# kernels one moe_forward launches: router logits, router top-k, scan (run by
+# the last top-k CTA when T has at most 8 router tiles of 32 tokens), scatter,
 # gate_up, down, combine
-KERNELS_PER_STEP = 7
+FUSE_SCAN_TILES = 8
+
+
+def kernels_per_step(T: int) -> int:
+    return 6 if (T + 31) // 32 <= FUSE_SCAN_TILES else 7
+
+
 KERNEL_SOURCES = {
     "router_topk": "router_topk.cu", "route_scan": "permute.cu", "route_scatter": "permute.cu",
     "gate_up": "expert_gemm_tmem.cu", "down": "expert_gemm_tmem.cu", "combine": "combine.cu",
 }
+# the grouped GEMMs of the block-scaled design (E4M3-term activations)
+MX_SOURCES = {"gate_up": "expert_gemm_mx.cu", "down": "expert_gemm_mx.cu"}
+
+
+def kernel_source(kernel: str, mx: bool) -> str:
+    return (MX_SOURCES if mx else KERNEL_SOURCES).get(kernel, KERNEL_SOURCES.get(kernel, ""))
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 
 
@@ -146,11 +159,11 @@ def stage_work(wl: gen.Workload, counts: np.ndarray):
     }
 
 
-def kernel_traffic(kernel: str, workload: str):
+def kernel_traffic(kernel: str, workload: str, mx: bool = False):
     """DRAM bytes per launch from a committed ncu capture, if the kernel's source
     is unchanged since (profiles/dram_traffic.txt: kernel workload sha bytes)."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
-    src = os.path.join(ROOT, "sparse_moe_transformer_selected_b300", "csrc", KERNEL_SOURCES[kernel])
+    src = os.path.join(ROOT, "sparse_moe_transformer_selected_b300", "csrc", kernel_source(kernel, mx))
     if not os.path.exists(path) or not os.path.exists(src):
         return None
     sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
@@ -371,7 +384,10 @@ def run_ours(args, wl):
                 "unit": "TFLOP/s"}
         peak_note = (f"bf16 dense {'sustained' if long_step else 'burst'} ({peak_src})")
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = kernel_traffic(top, wl.name)
+    fmt, _ = dev.hidden_format()
+    mx = fmt == moe.HIDDEN_E4M3_TERMS
+    roof["traffic"] = kernel_traffic(top, wl.name, mx)
+    roof["kernel_source"] = kernel_source(top, mx)
     roof["kernel"] = top
     roof["peak_source"] = peak_note
     roof["algorithmic"] = {"bytes": wk["bytes"], "flops": wk["flops"], "per": wk.get("unit", "")}
@@ -381,14 +397,16 @@ def run_ours(args, wl):
         "metric": METRIC, "value": whole_job_tokens_per_s(wl.T, world, ms), "unit": "tokens/s",
         "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": ("e2m1 x e4m3 block-scaled MMA, fp32 accumulation" if mx
+                  else "f16 x f16 MMA on exactly dequantised MXFP4, fp32 accumulation"),
         "data": "synthetic (seeded PCG64: x~N(0,1) bf16, random MXFP4 experts)",
         "config": config_block(wl, world),
         "clocks": clk.summary(),
         "e2e": {"value": whole_job_tokens_per_s(wl.T, world, e2e), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(dev.x.numel() * 2),
                 "d2h_bytes_per_step": int(dev.out.numel() * 2)},
-        "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "gpu_launches": kernels_per_step(wl.T) * args.steps,
         "roofline": roof,
         "stages_ms": {k_: round(v, 5) for k_, v in mean_stage.items()},
         "active_experts": work["_active"],
