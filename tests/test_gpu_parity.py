@@ -218,8 +218,8 @@ def test_edge_shapes_smem_staged_gemm(name, monkeypatch):
 
 
 def test_both_gemm_designs_agree_on_decode(monkeypatch):
-    """The two designs round differently only in fp32 summation order, so on
-    the 20b decode layer they agree to well inside the oracle tolerance."""
+    """The default (block-scaled) and the shared-memory-staged designs agree on
+    the 20b decode layer to well inside the oracle tolerance."""
     inp = gen.make_inputs(gen.WORKLOADS["gptoss20b_decode"])
     dev = DeviceMoE.upload(inp)
     a = bf16_to_f64(dev.forward().clone())
@@ -246,3 +246,56 @@ def test_cuda_graph_replay_matches_eager_call():
     second = dev.out.clone()
     assert torch.equal(second.view(torch.int16), dev.forward().view(torch.int16))
     moe.moe_poll_status(dev.workspace)
+
+
+# ------------------------------------------------ the block-scaled design --
+
+def test_block_scaled_path_intermediates():
+    """A decode-sized load with K % 128 = 64 on both GEMMs (the tail box read
+    through the second tensor map) and a partial down tile (d % 128 = 64) runs
+    on the block-scaled design; its h (four E4M3 terms) and y match the oracle
+    row by row."""
+    wl = gen.Workload("mx_tail", T=24, d=448, W=320, E=16, router_bias="normal", seed=21)
+    inp = gen.make_inputs(wl)
+    dev, out, ref = _run(inp, keep_hidden=True)
+    fmt, ex = dev.hidden_format()
+    assert fmt == moe.HIDDEN_E4M3_TERMS and ex == -3
+    _check_full(dev, out, ref, 4)
+    perm = dev.region("perm").cpu().numpy()
+    h = dev.hidden().cpu().numpy().astype(np.float64)
+    y = dev.region("y").cpu().numpy().astype(np.float64)
+    for row, q in enumerate(perm):
+        t, j = divmod(int(q), 4)
+        z_ref, h_ref, y_ref = ref["hidden"][(t, j)]
+        assert np.allclose(h[row], h_ref, rtol=1e-4, atol=1e-4 * np.abs(h_ref).max()), (t, j)
+        assert np.allclose(y[row], y_ref, rtol=1e-4, atol=1e-4 * np.abs(y_ref).max()), (t, j)
+
+
+def test_block_scaled_and_tmem_designs_agree_on_decode(monkeypatch):
+    """MOE_GEMM=tmem forces the dequantise-into-TMEM design on the 20b decode
+    layer; it and the default block-scaled design agree within the oracle bar."""
+    inp = gen.make_inputs(gen.WORKLOADS["gptoss20b_decode"])
+    dev = DeviceMoE.upload(inp)
+    assert dev.hidden_format()[0] == moe.HIDDEN_E4M3_TERMS
+    a = bf16_to_f64(dev.forward().clone())
+    monkeypatch.setenv("MOE_GEMM", "tmem")
+    assert dev.hidden_format()[0] == moe.HIDDEN_F16_PAIR
+    b = bf16_to_f64(dev.forward().clone())
+    moe.moe_poll_status(dev.workspace)
+    parity.check_output(a, b, what="block-scaled vs tmem design")
+
+
+@pytest.mark.parametrize("case", ["k_tail_32", "wide_clamp"])
+def test_block_scaled_design_falls_back(case):
+    """Decode-sized loads the block-scaled design cannot take run on the TMEM
+    design: a reduction length with K % 128 = 32 (the 4-bit tail map's base
+    would not be 32-byte aligned) and a clamp too wide for a fixed h scale."""
+    if case == "k_tail_32":
+        wl = gen.Workload("k_tail_32", T=16, d=416, W=256, E=8, router_bias="normal", seed=22)
+        inp = gen.make_inputs(wl)
+    else:
+        wl = gen.Workload("wide_clamp", T=16, d=256, W=256, E=8, router_bias="normal", seed=23)
+        inp = gen.make_inputs(wl, limit=20.0)
+    dev, out, ref = _run(inp)
+    assert dev.hidden_format()[0] != moe.HIDDEN_E4M3_TERMS
+    _check_full(dev, out, ref, 4)
