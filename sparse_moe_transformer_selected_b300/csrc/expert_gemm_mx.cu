@@ -175,7 +175,7 @@ __host__ __device__ inline Geo geometry(int d, int W, int nb, int ld_sx, int sta
   g.off_b = off;
   off += stages * g.b_stage;
   g.off_sc = off;
-  off += 2 * g.sc_buf;
+  off += g.sc_buf;
   g.off_xch = off;
   off += (M == Mode::GateUp) ? (kMW / 2) * kNB * 4 : 0;
   off = (off + 7) & ~7;
@@ -313,39 +313,41 @@ moe_expert_gemm_mx(const __grid_constant__ CUtensorMap map_w,     // main codes
           rb = ra;
         }
       };
-      // The scale rows of unit number qq (its index in this CTA's sequence) go
-      // to buffer qq & 1 one unit ahead of its stages, so the scale writers
-      // have them in TMEM before the MMA reaches the unit.
+      // The scale rows of unit number qq (its index in this CTA's sequence)
+      // are loaded while unit qq - 1 streams, into the one staging buffer the
+      // scale writers have emptied (they copy a unit's scales into TMEM during
+      // the unit before it), so the MMA finds them in TMEM.
       auto load_scales = [&](int uu, int qq) -> bool {
         const Unit w = unit_of(a, n_mt, uu);
-        const int sbuf = qq & 1;
-        if (!wait_phase(&sc_empty[sbuf], ((qq >> 1) & 1) ^ 1, abort_flag, a.status, 64, 5)) return false;
-        uint8_t* dst = scb + sbuf * G.sc_buf;
+        if (!wait_phase(&sc_empty[0], (qq & 1) ^ 1, abort_flag, a.status, 64, 5)) return false;
+        uint8_t* dst = scb;
         int ra, rb, nrows;
         rows_of(w, ra, rb, nrows);
         const uint32_t bytes = uint32_t(nrows * G.nsb);
         if constexpr (kGateUp) {
           const uint32_t bbytes = uint32_t(G.sc_b);
-          ptx::mbar_arrive_expect_tx(&sc_full[sbuf], 2 * bytes + 2 * bbytes);
-          ptx::bulk_load(dst, wscale + size_t(ra) * G.nsb, bytes, &sc_full[sbuf]);
-          ptx::bulk_load(dst + (kMW / 2) * G.nsb, wscale + size_t(rb) * G.nsb, bytes, &sc_full[sbuf]);
-          ptx::bulk_load(dst + G.sc_a, a.sx_hi + size_t(w.r0) * a.ld_sx, bbytes, &sc_full[sbuf]);
-          ptx::bulk_load(dst + G.sc_a + G.sc_b, a.sx_lo + size_t(w.r0) * a.ld_sx, bbytes, &sc_full[sbuf]);
+          ptx::mbar_arrive_expect_tx(&sc_full[0], 2 * bytes + 2 * bbytes);
+          ptx::bulk_load(dst, wscale + size_t(ra) * G.nsb, bytes, &sc_full[0]);
+          ptx::bulk_load(dst + (kMW / 2) * G.nsb, wscale + size_t(rb) * G.nsb, bytes, &sc_full[0]);
+          ptx::bulk_load(dst + G.sc_a, a.sx_hi + size_t(w.r0) * a.ld_sx, bbytes, &sc_full[0]);
+          ptx::bulk_load(dst + G.sc_a + G.sc_b, a.sx_lo + size_t(w.r0) * a.ld_sx, bbytes, &sc_full[0]);
         } else {
-          ptx::mbar_arrive_expect_tx(&sc_full[sbuf], bytes);
-          ptx::bulk_load(dst, wscale + size_t(ra) * G.nsb, bytes, &sc_full[sbuf]);
+          ptx::mbar_arrive_expect_tx(&sc_full[0], bytes);
+          ptx::bulk_load(dst, wscale + size_t(ra) * G.nsb, bytes, &sc_full[0]);
         }
-        in_sc.mark(sbuf, (qq >> 1) & 1);
+        in_sc.mark(0, qq & 1);
         return true;
       };
       bool ok = blockIdx.x >= units || load_scales(blockIdx.x, 0);
       int q = 0;
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++q) {
         const Unit w = unit_of(a, n_mt, u);
-        if (u + int(gridDim.x) < units && !load_scales(u + int(gridDim.x), q + 1)) { ok = false; break; }
         int row_a, row_b, nrows;
         rows_of(w, row_a, row_b, nrows);
         for (int s = 0; s < G.nstage; ++s) {
+          // the next unit's scales, once this unit's first stages are out
+          if (s == min(1, G.nstage - 1) && u + int(gridDim.x) < units &&
+              !load_scales(u + int(gridDim.x), q + 1)) { ok = false; break; }
           if (!wait_phase(&empty[st.slot], st.phase ^ 1, abort_flag, a.status, 64, 4)) { ok = false; break; }
           const int i0 = 2 * s, i1 = min(2 * s + 2, G.nbox);
           // the 4-bit TMA counts the packed bytes it reads (half of what it writes)
@@ -372,7 +374,7 @@ moe_expert_gemm_mx(const __grid_constant__ CUtensorMap map_w,     // main codes
       }
       if (!ok) {
         in_st.drain(full, S);
-        in_sc.drain(sc_full, 2);
+        in_sc.drain(sc_full, 1);
       }
     }
   } else if (warp == kWarpMMA) {
@@ -437,11 +439,11 @@ moe_expert_gemm_mx(const __grid_constant__ CUtensorMap map_w,     // main codes
     const int m = quarter * 32 + lane;             // weight row of the tile = TMEM lane
     int q = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x, ++q) {
-      const int sbuf = q & 1;
-      const bool ok = wait_phase(&sc_full[sbuf], (q >> 1) & 1, abort_flag, a.status, 64, 6) &&
+      const int sbuf = q & 1;                      // TMEM scale set
+      const bool ok = wait_phase(&sc_full[0], q & 1, abort_flag, a.status, 64, 6) &&
                       wait_phase(&sf_empty[sbuf], ((q >> 1) & 1) ^ 1, abort_flag, a.status, 64, 7);
       if (!__all_sync(0xffffffffu, ok)) break;
-      const uint8_t* buf = scb + sbuf * G.sc_buf;
+      const uint8_t* buf = scb;
       const uint32_t ta = tmem_base + lane_addr + sfa_col0 + sbuf * 4 * G.groups;
       const uint32_t tb = tmem_base + lane_addr + sfb_col0 + sbuf * 4 * G.groups;
       // A: row m's word of group g in all four columns 4g..4g+3 (the MMA reads
@@ -474,7 +476,7 @@ moe_expert_gemm_mx(const __grid_constant__ CUtensorMap map_w,     // main codes
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        ptx::mbar_arrive(&sc_empty[sbuf]);
+        ptx::mbar_arrive(&sc_empty[0]);
         ptx::mbar_arrive(&sf_full[sbuf]);
       }
     }
