@@ -41,6 +41,7 @@
 //   warps 8-11  scale writers, TMEM lane quarter = warp % 4
 // Work unit = (token chunk of one expert, weight tile of 128 rows), chunk-major.
 #include "common.cuh"
+#include "map_cache.cuh"
 #include "tc_ptx.cuh"
 
 #include <cudaTypedefs.h>
@@ -680,9 +681,30 @@ cudaError_t launch(const GemmArgs& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  CUtensorMap mw, mwt, mb[4];
-  cudaError_t e = make_maps<M>(a, &mw, &mwt, mb);
-  if (e != cudaSuccess) return e;
+  // the six maps, from the cache when this layer's buffers were seen before
+  struct Key {
+    const void* p[7];
+    int R, d, W, E, nb;
+  } key;
+  memset(&key, 0, sizeof(key));
+  key.p[0] = (M == Mode::GateUp) ? a.w_gu : a.w_dn;
+  key.p[1] = a.xq_hi;
+  key.p[2] = a.xq_lo;
+  key.p[3] = a.hq;
+  key.R = a.R;
+  key.d = a.d;
+  key.W = a.W;
+  key.E = a.E;
+  key.nb = a.nb;
+  static MapCache<Key, 6> cache;
+  CUtensorMap maps[6];
+  if (!cache.find(key, maps)) {
+    cudaError_t e = make_maps<M>(a, &maps[0], &maps[1], &maps[2]);
+    if (e != cudaSuccess) return e;
+    cache.put(key, maps);
+  }
+  const CUtensorMap &mw = maps[0], &mwt = maps[1];
+  const CUtensorMap* mb = &maps[2];
   const int n_out = (M == Mode::GateUp) ? a.W : a.d;
   const int rows_per_tile = (M == Mode::GateUp) ? kMW / 2 : kMW;
   const long long n_mt = (n_out + rows_per_tile - 1) / rows_per_tile;

@@ -44,6 +44,7 @@
 //            for every scale byte <= 142, and B = h as two bf16 terms.  Two MMAs
 //            per K step (hi, lo).
 #include "common.cuh"
+#include "map_cache.cuh"
 #include "tc_ptx.cuh"
 
 #include <cudaTypedefs.h>
@@ -810,25 +811,49 @@ cudaError_t launch(const GemmArgs& args, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  CUtensorMap mw, m0, m1;
-  cudaError_t e;
-  if (M == Mode::GateUp) {
-    e = make_map(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.w_gu, (long long)a.E * 2 * a.W, a.d / 2,
-                 kSK / 2, kCodeBoxRows);
-    if (e == cudaSuccess)
-      e = make_map(&m0, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.x_perm, a.R, a.d, 64, a.nb);
-    m1 = m0;
-  } else {
-    e = make_map(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.w_dn, (long long)a.E * a.d, a.W / 2,
-                 kSK / 2, kCodeBoxRows);
-    if (e == cudaSuccess)
-      e = make_map(&m0, F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-                   a.h_hi, a.R, a.W, 64, a.nb);
-    if (e == cudaSuccess)
-      e = make_map(&m1, F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-                   a.h_lo, a.R, a.W, 64, a.nb);
+  // the three maps, from the cache when this layer's buffers were seen before
+  struct Key {
+    const void* p[4];
+    int R, d, W, E, nb;
+  } key;
+  memset(&key, 0, sizeof(key));
+  key.p[0] = (M == Mode::GateUp) ? a.w_gu : a.w_dn;
+  key.p[1] = a.x_perm;
+  key.p[2] = a.h_hi;
+  key.p[3] = a.h_lo;
+  key.R = a.R;
+  key.d = a.d;
+  key.W = a.W;
+  key.E = a.E;
+  key.nb = a.nb;
+  static MapCache<Key, 3> cache;
+  CUtensorMap maps[3];
+  cudaError_t e = cudaSuccess;
+  if (!cache.find(key, maps)) {
+    CUtensorMap mw, m0, m1;
+    if (M == Mode::GateUp) {
+      e = make_map(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.w_gu, (long long)a.E * 2 * a.W, a.d / 2,
+                   kSK / 2, kCodeBoxRows);
+      if (e == cudaSuccess)
+        e = make_map(&m0, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.x_perm, a.R, a.d, 64, a.nb);
+      m1 = m0;
+    } else {
+      e = make_map(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.w_dn, (long long)a.E * a.d, a.W / 2,
+                   kSK / 2, kCodeBoxRows);
+      if (e == cudaSuccess)
+        e = make_map(&m0, F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                     a.h_hi, a.R, a.W, 64, a.nb);
+      if (e == cudaSuccess)
+        e = make_map(&m1, F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                     a.h_lo, a.R, a.W, 64, a.nb);
+    }
+    if (e != cudaSuccess) return e;
+    maps[0] = mw;
+    maps[1] = m0;
+    maps[2] = m1;
+    cache.put(key, maps);
   }
-  if (e != cudaSuccess) return e;
+  const CUtensorMap &mw = maps[0], &m0 = maps[1], &m1 = maps[2];
   const int n_out = (M == Mode::GateUp) ? a.W : a.d;
   const int rows_per_tile = (M == Mode::GateUp) ? kMW / 2 : kMW;
   const long long n_mt = (n_out + rows_per_tile - 1) / rows_per_tile;
