@@ -428,13 +428,14 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="gptoss20b_decode", choices=sorted(gen.WORKLOADS))
+    ap.add_argument("--workload", default="gptoss20b_decode",
+                    choices=sorted({**gen.WORKLOADS, **gen.STRESS_WORKLOADS}))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-sample", type=int, default=0, help="oracle tokens per CPU sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)      # at least 3 untimed warm-up steps
-    wl = gen.WORKLOADS[args.workload]
+    wl = {**gen.WORKLOADS, **gen.STRESS_WORKLOADS}[args.workload]
     if args.impl == "reference":
         run_reference(args, wl)
     else:

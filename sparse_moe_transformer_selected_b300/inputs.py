@@ -60,6 +60,15 @@ WORKLOADS = {
                                   router_bias="zipf"),
 }
 
+# A second MoE shape as a stress of the same kernels (another model's layer:
+# d = 2048, expert width 768, 128 experts, top-8); not a pages' configuration.
+STRESS_WORKLOADS = {
+    "qwen3_30b_a3b_decode": Workload("qwen3_30b_a3b_decode", T=32, d=2048, W=768, E=128, k=8,
+                                     seed=31),
+    "qwen3_30b_a3b_prefill": Workload("qwen3_30b_a3b_prefill", T=2048, d=2048, W=768, E=128,
+                                      k=8, seed=32),
+}
+
 
 def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
     """Round float32 values to the nearest bf16 (ties to even); return uint16 bits.

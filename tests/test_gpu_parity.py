@@ -299,3 +299,29 @@ def test_block_scaled_design_falls_back(case):
     dev, out, ref = _run(inp)
     assert dev.hidden_format()[0] != moe.HIDDEN_E4M3_TERMS
     _check_full(dev, out, ref, 4)
+
+
+# ------------------------------------------------ a second MoE shape (stress) --
+
+@pytest.mark.parametrize("name", sorted(gen.STRESS_WORKLOADS))
+def test_stress_shape_d2048_w768_e128_top8(name):
+    """Another model's MoE layer shape (d 2048, expert width 768, 128 experts,
+    top-8) through the same kernels: the decode size takes the block-scaled
+    design, the prefill size the TMEM design; all tokens at decode, a seeded
+    sample at prefill."""
+    wl = gen.STRESS_WORKLOADS[name]
+    inp = gen.make_inputs(wl)
+    tokens = None
+    if wl.T > 64:
+        rng = np.random.Generator(np.random.PCG64(4321))
+        tokens = np.unique(np.concatenate([[0, wl.T - 1], rng.choice(wl.T, size=10, replace=False)]))
+    dev, out, ref = _run(inp, tokens=tokens)
+    fmt = dev.hidden_format()[0]
+    assert (fmt == moe.HIDDEN_E4M3_TERMS) == (wl.T <= 64)
+    idx = dev.region("topk_idx").cpu().numpy()
+    if tokens is None:
+        _check_full(dev, out, ref, wl.k)
+    else:
+        excused = parity.check_routing(ref, idx, dev.region("topk_w").cpu().numpy(), wl.k)
+        keep = np.array([i for i, t in enumerate(tokens) if int(t) not in excused])
+        parity.check_output(out[tokens[keep]], ref["out"][keep])
