@@ -37,17 +37,35 @@ __device__ __forceinline__ void scan_tiles(const int32_t* tile_counts, int ntile
     total[tid] = run;
   }
   __syncthreads();
-  if (tid == 0) {
-    int32_t run = 0, mrun = 0;
-    for (int q = 0; q < E; ++q) {
-      off[q] = run;
-      offsets[q] = run;
-      mtile_off[q] = mrun;
-      run += total[q];
-      mrun += (total[q] + chunk - 1) / chunk;
+  // exclusive scans over experts of the counts and of their token chunks:
+  // inclusive scans inside each warp (shuffles), then the warps' totals in
+  // order (E <= 256: at most 8 warps)
+  {
+    const int lane = tid & 31, wid = tid >> 5;
+    const int32_t v = tid < E ? total[tid] : 0;
+    const int32_t c = tid < E ? (v + chunk - 1) / chunk : 0;
+    int32_t iv = v, ic = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t pv = __shfl_up_sync(0xffffffffu, iv, o);
+      const int32_t pc = __shfl_up_sync(0xffffffffu, ic, o);
+      if (lane >= o) { iv += pv; ic += pc; }
     }
-    offsets[E] = run;
-    mtile_off[E] = mrun;
+    __shared__ int32_t wsum_v[8], wsum_c[8];
+    if (lane == 31 && wid < 8) { wsum_v[wid] = iv; wsum_c[wid] = ic; }
+    __syncthreads();
+    if (tid < E) {
+      int32_t bv = 0, bc = 0;
+      for (int w = 0; w < wid; ++w) { bv += wsum_v[w]; bc += wsum_c[w]; }
+      const int32_t ev = bv + iv - v, ec = bc + ic - c;     // exclusive
+      off[tid] = ev;
+      offsets[tid] = ev;
+      mtile_off[tid] = ec;
+      if (tid == E - 1) {
+        offsets[E] = ev + v;
+        mtile_off[E] = ec + c;
+      }
+    }
   }
   __syncthreads();
   if (active) {
