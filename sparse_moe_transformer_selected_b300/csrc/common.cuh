@@ -63,6 +63,8 @@ inline int router_split_len(int64_t T, int d, int E) {
   return int(len < d ? len : (d + 31) / 32 * 32);
 }
 inline int router_splits(int64_t T, int d, int E) {
+  // at most 8 router tiles: whole dot products, one slab (router_topk.cu)
+  if ((T + kRouterTile - 1) / kRouterTile <= 8) return 1;
   const int len = router_split_len(T, d, E);
   return (d + len - 1) / len;
 }

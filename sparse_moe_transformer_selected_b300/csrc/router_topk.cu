@@ -151,6 +151,75 @@ router_logits_kernel(const __nv_bfloat16* __restrict__ x, const float* __restric
   }
 }
 
+// Decode-sized batches (at most 8 router tiles): whole dot products, no
+// partial slabs.  A CTA takes one token and 4 experts; its 8 warps split d
+// into 8 ranges, so each lane has at most kRowIt 4-element pieces and loads all
+// of them (token row and the 4 expert rows) before it multiplies: one round of
+// memory latency.  Each warp adds its lanes in a fixed shuffle tree and warp 0
+// adds the 8 ranges in order.  The result is the logits without bias, the one
+// partial slab the top-k kernel adds the bias to.
+constexpr int kRowExp = 4, kRowParts = kThreads / 32, kRowIt = 4;
+
+__global__ void __launch_bounds__(kThreads)
+router_logits_rows_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__ rw,
+                          int T, int d, int E, float* __restrict__ part,
+                          int32_t* __restrict__ status) {
+  __shared__ float red[kRowParts][kRowExp];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x;
+  const int e0 = blockIdx.y * kRowExp;
+  pdl_wait();
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
+    status[0] = 0;                               // first kernel of a call
+    status[1] = 0;                               // top-k tiles done (fused scan)
+    status[4] = 0;                               // which wait of a GEMM timed out, if one did
+  }
+  const int np = d / 4;                          // 4-element pieces of a row
+  const int per = (np + kRowParts - 1) / kRowParts;
+  const int p0 = warp * per, p1 = min(np, p0 + per);
+  const uint2* xr = reinterpret_cast<const uint2*>(x + (size_t)t * d);
+  float acc[kRowExp] = {0.f, 0.f, 0.f, 0.f};
+  for (int base = p0; base < p1; base += 32 * kRowIt) {
+    uint2 xv[kRowIt];
+    float4 wv[kRowExp][kRowIt];
+#pragma unroll
+    for (int it = 0; it < kRowIt; ++it) {
+      const int pc = base + lane + 32 * it;
+      const bool in = pc < p1;
+      xv[it] = in ? __ldg(xr + pc) : make_uint2(0, 0);
+#pragma unroll
+      for (int j = 0; j < kRowExp; ++j)
+        wv[j][it] = (in && e0 + j < E)
+                        ? __ldg(reinterpret_cast<const float4*>(rw + (size_t)(e0 + j) * d) + pc)
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int it = 0; it < kRowIt; ++it) {
+      const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&xv[it].x);
+      const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&xv[it].y);
+      const float x0 = __low2float(a), x1 = __high2float(a), x2 = __low2float(b), x3 = __high2float(b);
+#pragma unroll
+      for (int j = 0; j < kRowExp; ++j)
+        acc[j] = fmaf(x3, wv[j][it].w, fmaf(x2, wv[j][it].z, fmaf(x1, wv[j][it].y, fmaf(x0, wv[j][it].x, acc[j]))));
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < kRowExp; ++j)
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc[j] += __shfl_xor_sync(0xffffffffu, acc[j], off);
+  if (lane == 0) {
+#pragma unroll
+    for (int j = 0; j < kRowExp; ++j) red[warp][j] = acc[j];
+  }
+  __syncthreads();
+  if (warp == 0 && lane < kRowExp && e0 + lane < E) {
+    float v = 0.f;
+#pragma unroll
+    for (int q = 0; q < kRowParts; ++q) v += red[q][lane];
+    part[(size_t)t * E + e0 + lane] = v;
+  }
+}
+
 template <int NPER>
 __global__ void __launch_bounds__(kThreads)
 router_topk_kernel(const float* __restrict__ part, int nks, const float* __restrict__ rb, int T,
@@ -279,7 +348,8 @@ cudaError_t launch_router_topk(const __nv_bfloat16* x, const float* router_w,
                                int32_t* tile_base, int32_t* offsets, int32_t* mtile_off,
                                bool* scanned, cudaStream_t s) {
   const int ntiles = (T + kTT - 1) / kTT;
-  const int nks = router_splits(T, d, E);
+  const bool rows = ntiles <= kFuseScanTiles;   // decode-sized: whole dot products
+  const int nks = rows ? 1 : router_splits(T, d, E);
   const int kc = router_split_len(T, d, E);
   const int eg = router_expert_group(T, E);
   const dim3 g1(ntiles, nks, (E + eg - 1) / eg);
@@ -287,12 +357,15 @@ cudaError_t launch_router_topk(const __nv_bfloat16* x, const float* router_w,
   const int nper = (E + 31) / 32;                // ... and in the top-k kernel
   if (nper_g < 1 || nper_g > 8 || nper > 8) return cudaErrorInvalidValue;
   cudaError_t e = cudaSuccess;
+  if (rows)
+    e = launch_pdl(router_logits_rows_kernel, dim3(T, (E + kRowExp - 1) / kRowExp), dim3(kThreads), 0,
+                   s, x, router_w, T, d, E, logit_part, status);
 #define MOE_LOGITS_CASE(N)                                                                   \
   case N:                                                                                    \
     e = launch_pdl(router_logits_kernel<N>, g1, dim3(kThreads), 0, s, x, router_w, T, d, E,   \
                    kc, eg, logit_part, status);                                              \
     break;
-  switch (nper_g) {
+  switch (rows ? 0 : nper_g) {
     MOE_LOGITS_CASE(1)
     MOE_LOGITS_CASE(2)
     MOE_LOGITS_CASE(3)
