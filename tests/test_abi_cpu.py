@@ -116,3 +116,37 @@ def test_binding_raises_on_error(lib):
         moe.moe_forward(0, 64, 256, 256, 16, 16, 16, 16, 16, 16, 16, 16, 8, 4, 7.0, 1.702,
                         16, 16, 1 << 30, stream=0)
     assert ei.value.status == 1
+
+
+# ------------------------------------------------- GEMM design selection --
+# moe_hidden_format reports how h is carried, which names the design moe_forward
+# picks for a shape and clamp; the choice is host logic, checked here without a GPU.
+
+@pytest.mark.parametrize("shape,limit,want", [
+    # decode-sized loads (at most 8 routed rows per expert) with a bounded clamp:
+    # block-scaled MXFP4 GEMMs, h as four E4M3 terms scaled by 2^-3 at limit 7
+    ((32, 2880, 2880, 32, 4), 7.0, (moe.HIDDEN_E4M3_TERMS, -3)),
+    ((64, 2880, 2880, 128, 4), 7.0, (moe.HIDDEN_E4M3_TERMS, -3)),
+    ((32, 2048, 768, 128, 8), 7.0, (moe.HIDDEN_E4M3_TERMS, -3)),
+    ((24, 448, 320, 16, 4), 7.0, (moe.HIDDEN_E4M3_TERMS, -3)),      # K % 128 = 64 tails
+    ((32, 2880, 2880, 32, 4), 1.0, (moe.HIDDEN_E4M3_TERMS, -7)),    # |h| <= 2: 2^7 scale
+    # more rows per expert: TMEM-dequantised GEMMs with an f16 pair
+    ((8192, 2880, 2880, 32, 4), 7.0, (moe.HIDDEN_F16_PAIR, 0)),
+    ((64, 256, 256, 8, 4), 7.0, (moe.HIDDEN_F16_PAIR, 0)),
+    # block-scaled design excluded: a clamp too wide for a fixed scale, no clamp,
+    # a reduction length whose 4-bit tail map would be misaligned, K < 128
+    ((32, 2880, 2880, 32, 4), 20.0, (moe.HIDDEN_F16_PAIR, 0)),
+    ((32, 2880, 2880, 32, 4), float("inf"), (moe.HIDDEN_BF16_PAIR, 0)),
+    ((16, 416, 256, 8, 4), 7.0, (moe.HIDDEN_F16_PAIR, 0)),
+    ((45, 96, 160, 5, 4), 7.0, (moe.HIDDEN_F16_PAIR, 0)),
+])
+def test_gemm_design_selection(lib, shape, limit, want):
+    assert moe.moe_hidden_format(*shape, limit) == want
+
+
+def test_gemm_design_override(lib, monkeypatch):
+    decode = (32, 2880, 2880, 32, 4)
+    monkeypatch.setenv("MOE_GEMM", "tmem")
+    assert moe.moe_hidden_format(*decode, 7.0)[0] == moe.HIDDEN_F16_PAIR
+    monkeypatch.setenv("MOE_GEMM", "smem")
+    assert moe.moe_hidden_format(*decode, 7.0)[0] == moe.HIDDEN_BF16_PAIR
