@@ -325,3 +325,31 @@ def test_stress_shape_d2048_w768_e128_top8(name):
         excused = parity.check_routing(ref, idx, dev.region("topk_w").cpu().numpy(), wl.k)
         keep = np.array([i for i, t in enumerate(tokens) if int(t) not in excused])
         parity.check_output(out[tokens[keep]], ref["out"][keep])
+
+
+def test_block_scaled_design_with_16_byte_aligned_weights():
+    """Weight buffers aligned to 16 but not 32 bytes: the 4-bit TMA maps want
+    32-byte bases, so the call takes the TMEM design instead and still meets
+    the oracle bar (same layer, same result up to rounding)."""
+    wl = gen.Workload("aligned16", T=16, d=256, W=256, E=8, router_bias="normal", seed=24)
+    inp = gen.make_inputs(wl)
+    dev = DeviceMoE.upload(inp)
+    assert dev.hidden_format()[0] == moe.HIDDEN_E4M3_TERMS
+    ref = O.moe_forward_inputs(inp)
+
+    def shifted(t):
+        buf = torch.empty(t.numel() + 16, dtype=torch.uint8, device=t.device)
+        view = buf[16:16 + t.numel()]
+        view.copy_(t.view(-1))
+        assert view.data_ptr() % 32 == 16
+        return view
+
+    w_gu, w_dn = shifted(dev.w_gu), shifted(dev.w_dn)
+    out = torch.empty_like(dev.out)
+    moe.moe_forward(dev.x, dev.T, dev.d, dev.W, dev.router_w, dev.router_b, w_gu, dev.w_gu_scale,
+                    dev.b_gu, w_dn, dev.w_dn_scale, dev.b_dn, dev.E, dev.k, dev.limit, dev.alpha,
+                    out, dev.workspace, dev.workspace.numel())
+    moe.moe_poll_status(dev.workspace)
+    _check_full(dev, bf16_to_f64(out), ref, 4)
+    # the aligned call (block-scaled design) agrees with it
+    parity.check_output(bf16_to_f64(dev.forward()), bf16_to_f64(out), what="aligned vs 16-byte-aligned weights")
