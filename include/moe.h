@@ -103,11 +103,12 @@ size_t moe_workspace_bytes(int64_t T, int d, int W, int E, int k);
  * Precision: router logits, softmax and all accumulation in fp32.  The
  * weights enter the products exactly (code x 2^(scale - 127)).  Two number
  * formats carry the activations, chosen per call (moe_hidden_format says which):
- *  - decode-sized loads (at most 16 routed rows per expert on average) with a
+ *  - decode-sized loads (at most 8 routed rows per expert on average) with a
  *    clamp 0 < limit <= 16, weight buffers 32-byte aligned: x and h as sums
  *    of E4M3 terms fed to the tensor cores' block-scaled MXFP4 x MXFP8
  *    products: x = hi + lo/16 with a power-of-two scale per 32-element block
- *    (exact for bf16 x), h = t0 + t1/16 + t2/256 + t3/4096 with one fixed
+ *    (exact for bf16 x within 2^-7 of its block's largest |x|, else within
+ *    2^-13 of it), h = t0 + t1/16 + t2/256 + t3/4096 with one fixed
  *    scale 2^e that keeps |h| <= limit·(limit+1) inside the E4M3 range
  *    (about 16 significant bits);
  *  - otherwise x exactly (f16 after a per-token power-of-two scaling) and h

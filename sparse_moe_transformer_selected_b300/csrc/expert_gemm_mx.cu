@@ -12,7 +12,8 @@
 // activations are the B side as sums of E4M3 terms, each term with its own
 // block scales, stacked along N: rows t nb .. t nb + nb - 1 of B are term t of
 // the chunk's nb tokens, and the epilogue adds accumulator columns t nb + j.
-//   gate_up: x = hi + lo / 16 (2 terms; a bf16 value splits exactly)
+//   gate_up: x = hi + lo / 16 (2 terms; exact for bf16 values within 2^-7
+//            of their 32-block's largest)
 //   down:    h = (t0 + t1 / 16 + t2 / 256 + t3 / 4096) 2^h_exp (4 terms,
 //            about 16 significant bits)
 // One MMA covers M = 128 weight rows, N = terms x nb, K = 32.
