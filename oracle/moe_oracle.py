@@ -23,6 +23,10 @@ Sources (web pages about the gpt-oss architecture, cited by title and section):
 * [P4] Xin Zhiyuan report (dreamgost.com .../564), GLU discussion around
   Figure 6: a gated FFN has three weight matrices instead of two; the
   parameter arithmetic FC1+FC2 = 8,388,608 vs 3 x 1,048,576 = 3,145,728.
+* The step before the block (rms_norm, moe_block_forward): [P3] 2.7.1 and
+  [P5] "RMSNorm 替换 LayerNorm" — RMSNorm divides the activations by their root
+  mean square, with no mean subtraction and no bias term; [P5] "更深对比更宽"
+  — residual connections around the sub-layers.
 
 Facts the pages leave open, and the reading taken here:
 
@@ -41,6 +45,10 @@ Facts the pages leave open, and the reading taken here:
   bias is scaled by the routing weight.
 * Permuted ("expert-contiguous") row order: rows sorted by (expert, token,
   slot) ascending.
+* RMSNorm keeps the usual learned per-feature scale g and a small eps inside
+  the square root (the pages name neither): x / sqrt(mean(x²) + eps) · g.  The
+  block is pre-norm: the MoE reads RMSNorm(x) and its output is added to the
+  un-normalised x, out = x + MoE(RMSNorm(x)).
 
 The oracle rounds nothing: every intermediate stays fp64.
 """
@@ -205,7 +213,7 @@ def expert_ffn(x_rows, w_gu, b_gu, w_dn, b_dn, limit, alpha):
 
 def moe_forward(x_bits, router_w, router_b, w_gu, w_gu_scale, b_gu_bits,
                 w_dn, w_dn_scale, b_dn_bits, k=4, limit=7.0, alpha=1.702,
-                tokens=None, keep_hidden=False):
+                tokens=None, keep_hidden=False, workers=1):
     """The MoE MLP block on fp64: router -> top-k -> selected softmax -> experts
     -> weighted sum ([P5] MoE bullet; [P3] 2.4.1).  No shared expert is added
     ([P5] "更少的大专家 vs 更多的小专家").
@@ -213,9 +221,20 @@ def moe_forward(x_bits, router_w, router_b, w_gu, w_gu_scale, b_gu_bits,
     Routing (logits, top-k, weights, permutation) is computed for all T tokens.
     The expert FFN runs for `tokens` only (default: all), so large layers can be
     checked on a sample.  Returns a dict; "out" has one row per entry of
-    `tokens` in that order.
+    `tokens` in that order.  `workers` > 1 runs the experts on that many threads
+    (numpy releases the interpreter lock inside its loops); each expert's rows
+    are computed exactly as with one thread and added in expert order.
     """
-    x = bf16_bits_to_f64(x_bits)
+    return moe_forward_f64(bf16_bits_to_f64(x_bits), router_w, router_b, w_gu, w_gu_scale,
+                           b_gu_bits, w_dn, w_dn_scale, b_dn_bits, k=k, limit=limit,
+                           alpha=alpha, tokens=tokens, keep_hidden=keep_hidden, workers=workers)
+
+
+def moe_forward_f64(x, router_w, router_b, w_gu, w_gu_scale, b_gu_bits,
+                    w_dn, w_dn_scale, b_dn_bits, k=4, limit=7.0, alpha=1.702,
+                    tokens=None, keep_hidden=False, workers=1):
+    """moe_forward on activations already in fp64 (the block's normalised x)."""
+    x = np.asarray(x, np.float64)
     T = x.shape[0]
     E = router_w.shape[0]
     logits = router_logits(x, router_w, router_b)
@@ -229,11 +248,21 @@ def moe_forward(x_bits, router_w, router_b, w_gu, w_gu_scale, b_gu_bits,
     b_gu = bf16_bits_to_f64(b_gu_bits)
     b_dn = bf16_bits_to_f64(b_dn_bits)
     sel = idx[tok]                               # [n, k]
-    for e in np.unique(sel):
+
+    def one_expert(e):
         pos, slot = np.nonzero(sel == e)         # sampled position, slot
         wg = dequant_mxfp4(w_gu[e], w_gu_scale[e])
         wd = dequant_mxfp4(w_dn[e], w_dn_scale[e])
-        z, h, y = expert_ffn(x[tok[pos]], wg, b_gu[e], wd, b_dn[e], limit, alpha)
+        return pos, slot, expert_ffn(x[tok[pos]], wg, b_gu[e], wd, b_dn[e], limit, alpha)
+
+    experts = np.unique(sel)
+    if workers > 1:
+        from concurrent.futures import ThreadPoolExecutor
+        with ThreadPoolExecutor(max_workers=workers) as pool:
+            results = list(pool.map(one_expert, experts))
+    else:
+        results = [one_expert(e) for e in experts]
+    for pos, slot, (z, h, y) in results:         # expert order
         out[pos] += w[tok[pos], slot][:, None] * y   # each (pos, e) occurs once
         if keep_hidden:
             for r, (p, j) in enumerate(zip(pos, slot)):
@@ -245,9 +274,47 @@ def moe_forward(x_bits, router_w, router_b, w_gu, w_gu_scale, b_gu_bits,
     return res
 
 
-def moe_forward_inputs(inp, tokens=None, keep_hidden=False):
+def moe_forward_inputs(inp, tokens=None, keep_hidden=False, workers=1):
     """moe_forward on a MoEInputs bundle."""
     return moe_forward(inp.x, inp.router_w, inp.router_b, inp.w_gu, inp.w_gu_scale,
                        inp.b_gu, inp.w_dn, inp.w_dn_scale, inp.b_dn, k=inp.wl.k,
                        limit=inp.limit, alpha=inp.alpha, tokens=tokens,
-                       keep_hidden=keep_hidden)
+                       keep_hidden=keep_hidden, workers=workers)
+
+
+# --------------------------------------------------------- the step before --
+
+def rms_norm(x, weight, eps):
+    """RMSNorm ([P3] 2.7.1; [P5] "RMSNorm 替换 LayerNorm"): each row divided by
+    its root mean square, with no mean subtracted and no bias added, then
+    scaled by the per-feature weight: x / sqrt(mean(x²) + eps) · weight."""
+    x = np.asarray(x, np.float64)
+    ms = np.mean(x * x, axis=-1, keepdims=True)
+    return x / np.sqrt(ms + eps) * np.asarray(weight, np.float64)
+
+
+def moe_block_forward(x_bits, norm_w, eps, router_w, router_b, w_gu, w_gu_scale, b_gu_bits,
+                      w_dn, w_dn_scale, b_dn_bits, k=4, limit=7.0, alpha=1.702,
+                      tokens=None, keep_hidden=False, workers=1):
+    """The MoE sub-layer of a pre-norm block with its residual connection:
+    out = x + MoE(RMSNorm(x)), x the un-normalised residual stream ([P5]
+    "更深对比更宽": residual connections; "RMSNorm 替换 LayerNorm").  Returns the
+    moe_forward dict with "out" replaced by the block output and "normed"
+    holding RMSNorm(x) for every token.
+    """
+    x = bf16_bits_to_f64(x_bits)
+    xn = rms_norm(x, norm_w, eps)
+    res = moe_forward_f64(xn, router_w, router_b, w_gu, w_gu_scale, b_gu_bits, w_dn,
+                          w_dn_scale, b_dn_bits, k=k, limit=limit, alpha=alpha, tokens=tokens,
+                          keep_hidden=keep_hidden, workers=workers)
+    res["out"] = x[res["tokens"]] + res["out"]
+    res["normed"] = xn
+    return res
+
+
+def moe_block_forward_inputs(inp, tokens=None, keep_hidden=False, workers=1):
+    """moe_block_forward on a MoEInputs bundle that carries norm_w and eps."""
+    return moe_block_forward(inp.x, inp.norm_w, inp.eps, inp.router_w, inp.router_b, inp.w_gu,
+                             inp.w_gu_scale, inp.b_gu, inp.w_dn, inp.w_dn_scale, inp.b_dn,
+                             k=inp.wl.k, limit=inp.limit, alpha=inp.alpha, tokens=tokens,
+                             keep_hidden=keep_hidden, workers=workers)

@@ -108,6 +108,10 @@ class MoEInputs:
     b_dn: np.ndarray
     limit: float = 7.0
     alpha: float = 1.702
+    # the step before the block (make_block_inputs): RMSNorm weight [d] and eps;
+    # x is then the un-normalised residual stream
+    norm_w: np.ndarray | None = None
+    eps: float = 1e-5
 
 
 def _router_bias(rng: np.random.Generator, wl: Workload) -> np.ndarray:
@@ -167,3 +171,24 @@ def make_router_inputs(wl: Workload):
                 * np.float32(1.0 / math.sqrt(d))).astype(np.float32)
     router_b = _router_bias(rng, wl)
     return x, router_w, router_b
+
+
+def make_block_inputs(wl: Workload, limit: float = 7.0, alpha: float = 1.702,
+                      eps: float = 1e-5) -> MoEInputs:
+    """Inputs of the pre-norm block (RMSNorm, the MoE, the residual add).
+
+    The router and expert arguments are those of make_inputs(wl); a second
+    stream, PCG64([seed, 1]), then draws the residual stream and the RMSNorm
+    weight, in this order:
+      s_t    per-token magnitude, exp(N(0, 0.5))  (tokens of unequal RMS)
+      x      bf16 of s_t times N(0, 1)            [T, d], replaces make_inputs' x
+      norm_w float32, 1 + N(0, 0.1)               [d]
+    """
+    inp = make_inputs(wl, limit=limit, alpha=alpha)
+    rng = np.random.Generator(np.random.PCG64([wl.seed, 1]))
+    s_t = np.exp(rng.normal(0.0, 0.5, size=(wl.T, 1))).astype(np.float32)
+    z = rng.standard_normal((wl.T, wl.d), dtype=np.float32)
+    inp.x = f32_to_bf16_bits((z * s_t).astype(np.float32))
+    inp.norm_w = (1.0 + rng.normal(0.0, 0.1, size=wl.d)).astype(np.float32)
+    inp.eps = float(eps)
+    return inp

@@ -322,4 +322,105 @@ def check_sampled_tokens(O):
     assert np.allclose(sub, full[[13, 2, 7]], rtol=1e-13, atol=1e-13)
 
 
+def check_threaded_experts(O):
+    """Running the experts on several threads changes nothing, bit for bit."""
+    inp = _tiny_inputs(T=24, d=64, W=32, E=8, seed=27)
+    a = O.moe_forward_inputs(inp)["out"]
+    b = O.moe_forward_inputs(inp, workers=4)["out"]
+    assert np.array_equal(a, b)
+
+
+# --------------------------------------------------------- the step before --
+
+def _decimal_rms_norm(row, weight, eps):
+    """x / sqrt(mean(x²) + eps) · g in 50-digit decimal arithmetic from the exact
+    binary values: an independent brute force of RMSNorm ([P3] 2.7.1)."""
+    from decimal import Decimal, getcontext
+    getcontext().prec = 50
+    xs = [Fraction(float(v)) for v in row]
+    ms = sum(v * v for v in xs) / len(xs) + Fraction(float(eps))
+    rms = (Decimal(ms.numerator) / Decimal(ms.denominator)).sqrt()
+    return [float(Decimal(v.numerator) / Decimal(v.denominator) / rms * Decimal(float(g)))
+            for v, g in zip(xs, weight)]
+
+
+def _bf16_value(bits):
+    """A bf16 bit pattern's value, through the float32 byte layout (struct)."""
+    import struct
+    return struct.unpack(">f", struct.pack(">I", int(bits) << 16))[0]
+
+
+def check_rms_norm_decimal(O):
+    rng = np.random.Generator(np.random.PCG64(31))
+    cases = [(rng.normal(0, 1, 16), rng.normal(1, 0.1, 16), 1e-5),
+             (rng.normal(0, 30, 48), rng.normal(1, 0.5, 48), 0.5),
+             (np.concatenate([rng.normal(0, 1e-3, 31), [250.0]]), np.ones(32), 0.0),
+             (np.full(8, -3.0), rng.normal(0, 2, 8), 1e-5)]
+    for row, g, eps in cases:
+        got = O.rms_norm(row[None, :], g, eps)[0]
+        want = _decimal_rms_norm(row, g, eps)
+        for i in range(len(row)):
+            assert abs(got[i] - want[i]) <= 1e-14 * max(1e-300, abs(want[i])), (i, got[i], want[i])
+
+
+def check_rms_norm_no_mean_no_bias(O):
+    """RMSNorm subtracts no mean and adds no bias ([P3] 2.7.1; [P5] "RMSNorm 替换
+    LayerNorm"): a constant row maps to ±1 (a mean-subtracting norm gives 0), a
+    zero row stays zero, scaling a row by a power of two changes nothing, and
+    with g = 1 and eps = 0 every output row has RMS 1."""
+    d = 24
+    for c in (2.5, -0.75):
+        assert np.array_equal(O.rms_norm(np.full((1, d), c), np.ones(d), 0.0)[0],
+                              np.full(d, math.copysign(1.0, c)))
+    assert np.array_equal(O.rms_norm(np.zeros((1, d)), np.ones(d), 1e-5)[0], np.zeros(d))
+    rng = np.random.Generator(np.random.PCG64(32))
+    x = rng.normal(0, 1, (5, d))
+    g = rng.normal(1, 0.2, d)
+    assert np.array_equal(O.rms_norm(8.0 * x, g, 0.0), O.rms_norm(x, g, 0.0))
+    y = O.rms_norm(x, np.ones(d), 0.0)
+    assert np.allclose(np.sqrt(np.mean(y * y, axis=1)), 1.0, rtol=1e-15, atol=0)
+
+
+def _block_inputs(T, d, W, E, seed, k=4):
+    wl = gen.Workload("pin", T=T, d=d, W=W, E=E, k=k, router_bias="normal", seed=seed)
+    return gen.make_block_inputs(wl)
+
+
+def check_block_residual(O):
+    """The block adds the MoE output to the un-normalised input: with every
+    expert's output zero (down codes 0, down bias 0) the block returns x
+    exactly; with rows of RMS 1 (entries ±1), g = 1 and eps = 0 the norm is the
+    identity and the block is x plus the MoE of x."""
+    inp = _block_inputs(T=5, d=64, W=32, E=6, seed=33)
+    inp.w_dn[:] = 0
+    inp.b_dn[:] = 0
+    out = O.moe_block_forward_inputs(inp)["out"]
+    for t in range(5):
+        for i in range(64):
+            assert out[t, i] == _bf16_value(inp.x[t, i]), (t, i)
+    inp = _block_inputs(T=6, d=64, W=32, E=6, seed=34)
+    signs = np.random.Generator(np.random.PCG64(35)).integers(0, 2, size=(6, 64))
+    inp.x = np.where(signs == 1, 0x3F80, 0xBF80).astype(np.uint16)      # +1.0 / -1.0
+    inp.norm_w = np.ones(64, dtype=np.float32)
+    inp.eps = 0.0
+    blk = O.moe_block_forward_inputs(inp)["out"]
+    moe = O.moe_forward_inputs(inp)["out"]
+    xv = np.where(signs == 1, 1.0, -1.0)
+    assert np.allclose(blk, xv + moe, rtol=1e-13, atol=1e-13)
+
+
+def check_block_scale_invariance(O):
+    """With eps = 0, scaling the input by 4 scales the residual part only: the
+    MoE reads RMSNorm(x), which does not change, so block(4x) - 4x equals
+    block(x) - x."""
+    inp = _block_inputs(T=6, d=64, W=32, E=6, seed=36)
+    inp.eps = 0.0
+    a = O.moe_block_forward_inputs(inp)
+    xa = np.array([[_bf16_value(b) for b in row] for row in inp.x])
+    inp.x = (inp.x.astype(np.int64) + (2 << 7)).astype(np.uint16)   # exponent + 2: times 4
+    b = O.moe_block_forward_inputs(inp)
+    assert np.allclose(b["out"] - 4.0 * xa, a["out"] - xa, rtol=1e-12, atol=1e-12)
+    assert np.array_equal(a["topk_idx"], b["topk_idx"])
+
+
 ALL_CHECKS = [v for k, v in sorted(globals().items()) if k.startswith("check_")]

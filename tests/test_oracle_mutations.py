@@ -43,6 +43,20 @@ MUTANTS = {
     "mx_bits": [("n_params * 4 / 8 + n_params / MX_BLOCK", "n_params * 4 / 8 + n_params / 16")],
     "glu_two_matrices": [("return 3 * d_model * hidden", "return 2 * d_model * hidden")],
     "sigmoid_sign": [("1.0 / (1.0 + np.exp(-v))", "1.0 / (1.0 + np.exp(v))")],
+    "rms_mean_subtracted": [("return x / np.sqrt(ms + eps) * np.asarray(weight, np.float64)",
+                             "return (x - x.mean(axis=-1, keepdims=True)) / np.sqrt(ms + eps)"
+                             " * np.asarray(weight, np.float64)")],
+    "rms_weight_dropped": [("return x / np.sqrt(ms + eps) * np.asarray(weight, np.float64)",
+                            "return x / np.sqrt(ms + eps)")],
+    "rms_eps_outside": [("np.sqrt(ms + eps)", "(np.sqrt(ms) + eps)")],
+    "rms_sum_not_mean": [("ms = np.mean(x * x, axis=-1, keepdims=True)",
+                          "ms = np.sum(x * x, axis=-1, keepdims=True)")],
+    "rms_bias_added": [("return x / np.sqrt(ms + eps) * np.asarray(weight, np.float64)",
+                        "return x / np.sqrt(ms + eps) * np.asarray(weight, np.float64) + 0.01")],
+    "residual_dropped": [('res["out"] = x[res["tokens"]] + res["out"]', 'res["out"] = res["out"] + 0.0')],
+    "residual_of_normed": [('res["out"] = x[res["tokens"]] + res["out"]',
+                            'res["out"] = xn[res["tokens"]] + res["out"]')],
+    "moe_reads_raw_x": [("res = moe_forward_f64(xn, router_w", "res = moe_forward_f64(x, router_w")],
 }
 
 
