@@ -48,9 +48,13 @@ Facts the pages leave open, and the reading taken here:
 * RMSNorm keeps the usual learned per-feature scale g and a small eps inside
   the square root (the pages name neither): x / sqrt(mean(x²) + eps) · g.  The
   block is pre-norm: the MoE reads RMSNorm(x) and its output is added to the
-  un-normalised x, out = x + MoE(RMSNorm(x)).
+  un-normalised x, out = x + MoE(RMSNorm(x)).  The MoE's input is bf16 (its x
+  is a bf16 tensor), so RMSNorm's output enters it rounded to the nearest bf16,
+  ties to even: the one rounding this oracle performs, because it is part of
+  what the block computes.
 
-The oracle rounds nothing: every intermediate stays fp64.
+Apart from that input rounding of the block, the oracle rounds nothing: every
+intermediate stays fp64.
 """
 from __future__ import annotations
 
@@ -293,17 +297,25 @@ def rms_norm(x, weight, eps):
     return x / np.sqrt(ms + eps) * np.asarray(weight, np.float64)
 
 
+def round_bf16(v):
+    """Nearest bf16 value (8 significant bits), ties to even, for finite v in
+    the normal range: v = m·2^e with 0.5 <= |m| < 1, m rounded to a multiple of
+    2^-8 (numpy's rint rounds halves to even)."""
+    m, e = np.frexp(np.asarray(v, np.float64))
+    return np.ldexp(np.rint(np.ldexp(m, 8)), e - 8)
+
+
 def moe_block_forward(x_bits, norm_w, eps, router_w, router_b, w_gu, w_gu_scale, b_gu_bits,
                       w_dn, w_dn_scale, b_dn_bits, k=4, limit=7.0, alpha=1.702,
                       tokens=None, keep_hidden=False, workers=1):
     """The MoE sub-layer of a pre-norm block with its residual connection:
-    out = x + MoE(RMSNorm(x)), x the un-normalised residual stream ([P5]
-    "更深对比更宽": residual connections; "RMSNorm 替换 LayerNorm").  Returns the
-    moe_forward dict with "out" replaced by the block output and "normed"
-    holding RMSNorm(x) for every token.
+    out = x + MoE(bf16(RMSNorm(x))), x the un-normalised residual stream ([P5]
+    "更深对比更宽": residual connections; "RMSNorm 替换 LayerNorm"); the MoE's
+    input is bf16.  Returns the moe_forward dict with "out" replaced by the block
+    output and "normed" holding the MoE input bf16(RMSNorm(x)) of every token.
     """
     x = bf16_bits_to_f64(x_bits)
-    xn = rms_norm(x, norm_w, eps)
+    xn = round_bf16(rms_norm(x, norm_w, eps))
     res = moe_forward_f64(xn, router_w, router_b, w_gu, w_gu_scale, b_gu_bits, w_dn,
                           w_dn_scale, b_dn_bits, k=k, limit=limit, alpha=alpha, tokens=tokens,
                           keep_hidden=keep_hidden, workers=workers)

@@ -190,5 +190,5 @@ def make_block_inputs(wl: Workload, limit: float = 7.0, alpha: float = 1.702,
     z = rng.standard_normal((wl.T, wl.d), dtype=np.float32)
     inp.x = f32_to_bf16_bits((z * s_t).astype(np.float32))
     inp.norm_w = (1.0 + rng.normal(0.0, 0.1, size=wl.d)).astype(np.float32)
-    inp.eps = float(eps)
+    inp.eps = float(np.float32(eps))       # the value a float32 argument carries
     return inp

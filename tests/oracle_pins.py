@@ -381,6 +381,58 @@ def check_rms_norm_no_mean_no_bias(O):
     assert np.allclose(np.sqrt(np.mean(y * y, axis=1)), 1.0, rtol=1e-15, atol=0)
 
 
+def _bf16_round_bits(v):
+    """Nearest bf16 of a float64 by integer arithmetic on its IEEE bits: keep
+    the sign, exponent and top 7 fraction bits, and round the 45 dropped bits
+    half to even (normal range only)."""
+    import struct
+    b = struct.unpack(">Q", struct.pack(">d", float(v)))[0]
+    keep, drop = b >> 45, b & ((1 << 45) - 1)
+    half = 1 << 44
+    if drop > half or (drop == half and keep & 1):
+        keep += 1
+    return struct.unpack(">d", struct.pack(">Q", keep << 45))[0]
+
+
+def check_round_bf16(O):
+    """bf16 rounding against integer rounding of the IEEE bits, at random
+    values and at constructed midpoints (ties go to the even neighbour)."""
+    rng = np.random.Generator(np.random.PCG64(37))
+    vals = np.concatenate([rng.normal(0, 1, 400), rng.normal(0, 1e3, 100),
+                           [1.0, -2.5, 1 + 2.0 ** -8, 1 + 3 * 2.0 ** -8, -(1 + 2.0 ** -8),
+                            1 + 2.0 ** -8 + 2.0 ** -40, 0.0]])
+    got = O.round_bf16(vals)
+    for v, r in zip(vals, got):
+        assert r == _bf16_round_bits(v), (v, r)
+    assert O.round_bf16(1 + 2.0 ** -8) == 1.0                     # tie, even below
+    assert O.round_bf16(1 + 3 * 2.0 ** -8) == 1 + 2.0 ** -6       # tie, even above
+
+
+def check_block_rounds_moe_input(O):
+    """E = 1, k = 1 block on a tiny layer against a brute force: RMSNorm in
+    50-digit decimal, rounded to bf16 by integer bit arithmetic, then the dense
+    gated FFN in plain Python; block - x must equal it."""
+    inp = _block_inputs(T=3, d=32, W=32, E=1, seed=38, k=1)
+    res = O.moe_block_forward_inputs(inp)
+    xb = [[_bf16_value(b) for b in row] for row in inp.x]
+    bgu = [_bf16_value(b) for b in inp.b_gu[0]]
+    bdn = [_bf16_value(b) for b in inp.b_dn[0]]
+    wgu = [_decode_row(O, inp.w_gu[0, n], inp.w_gu_scale[0, n]) for n in range(64)]
+    wdn = [_decode_row(O, inp.w_dn[0, n], inp.w_dn_scale[0, n]) for n in range(32)]
+    for t in range(3):
+        xn = [_bf16_round_bits(v) for v in _decimal_rms_norm(xb[t], inp.norm_w, inp.eps)]
+        z = [sum(wgu[n][i] * xn[i] for i in range(32)) + bgu[n] for n in range(64)]
+        h = []
+        for n in range(32):
+            g = min(z[n], 7.0)
+            u = max(-7.0, min(7.0, z[32 + n]))
+            h.append(g / (1 + math.exp(-1.702 * g)) * (u + 1))
+        for o in range(32):
+            y = sum(wdn[o][n] * h[n] for n in range(32)) + bdn[o]
+            got = res["out"][t, o] - xb[t][o]
+            assert abs(got - y) <= 1e-12 * max(1.0, abs(y)), (t, o, got, y)
+
+
 def _block_inputs(T, d, W, E, seed, k=4):
     wl = gen.Workload("pin", T=T, d=d, W=W, E=E, k=k, router_bias="normal", seed=seed)
     return gen.make_block_inputs(wl)

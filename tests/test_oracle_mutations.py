@@ -57,6 +57,10 @@ MUTANTS = {
     "residual_of_normed": [('res["out"] = x[res["tokens"]] + res["out"]',
                             'res["out"] = xn[res["tokens"]] + res["out"]')],
     "moe_reads_raw_x": [("res = moe_forward_f64(xn, router_w", "res = moe_forward_f64(x, router_w")],
+    "moe_input_not_rounded": [("xn = round_bf16(rms_norm(x, norm_w, eps))",
+                               "xn = rms_norm(x, norm_w, eps)")],
+    "bf16_round_truncates": [("np.rint(np.ldexp(m, 8))", "np.trunc(np.ldexp(m, 8))")],
+    "bf16_round_7_bits": [("np.rint(np.ldexp(m, 8)), e - 8)", "np.rint(np.ldexp(m, 7)), e - 7)")],
 }
 
 
