@@ -13,8 +13,8 @@
  *   "【LLM】GPT-OSS架构变化详解", section 2.4: the MoE replaces the single FFN
  *     and a router picks the experts of each token.
  *
- * For token t with input x[t] (already normalised; the RMSNorm before the block
- * is not part of this library):
+ * For token t with input x[t] (already normalised; moe_block_forward below
+ * adds the RMSNorm before the block and the residual add after it):
  *   logits[e] = x[t]·router_w[e] + router_b[e]                    (fp32)
  *   S         = the k largest logits, ordered by (logit desc, index asc)
  *   w_j       = exp(l_j - l_max) / Σ_{j'∈S} exp(l_j' - l_max)
@@ -124,6 +124,34 @@ moe_status moe_forward(const void* x_bf16, int64_t T, int d, int W,
                        void* out_bf16, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * The MoE sub-layer of a pre-norm transformer block, with the step before it
+ * and the residual add after it:
+ *   out = x + MoE(RMSNorm(x)),   RMSNorm(x) = x / sqrt(mean(x²) + eps) · norm_w
+ * x is the un-normalised residual stream.  RMSNorm divides each token by its
+ * root mean square, with no mean subtracted and no bias ("【LLM】GPT-OSS架构变化详解"
+ * 2.7.1; "OpenAI 最新开源模型 gpt-oss 架构与训练解析", section RMSNorm 替换
+ * LayerNorm); the residual connection is the one the latter page names in
+ * section 更深对比更宽.  The learned per-feature scale norm_w and eps are not on
+ * the pages (gpt-oss uses eps = 1e-5).
+ *   norm_w   [d]  fp32
+ *   eps      >= 0, finite
+ * Every other argument is as for moe_forward.  The MoE's input is bf16, so it
+ * reads RMSNorm(x) rounded to the nearest bf16 (ties to even); 1/rms is kept in
+ * fp64 so that rounding is decided as for the exact value.  The normalisation
+ * runs in the router kernel at decode sizes (a separate pass over x for more
+ * than 256 tokens); the residual add runs in the combine, which rounds
+ * x + Σ_j w_j·y_j once to bf16.  out may be the same buffer as x (an in-place
+ * residual update).
+ */
+moe_status moe_block_forward(const void* x_bf16, int64_t T, int d, int W, const float* norm_w,
+                             float eps, const float* router_w, const float* router_b,
+                             const uint8_t* w_gu_fp4, const uint8_t* w_gu_scale,
+                             const void* b_gu_bf16, const uint8_t* w_dn_fp4,
+                             const uint8_t* w_dn_scale, const void* b_dn_bf16, int E, int k,
+                             float limit, float alpha, void* out_bf16, void* workspace,
+                             size_t workspace_bytes, void* stream);
+
+/*
  * Routing only (the first two stages of moe_forward), with its tables returned:
  *   topk_idx  [T, k]  int32   selected experts, slot order (logit desc, index asc)
  *   topk_w    [T, k]  fp32    softmax over the selected logits
@@ -188,17 +216,64 @@ moe_status moe_hidden_format(int64_t T, int d, int W, int E, int k, float limit,
                              int* exponent);
 
 /*
- * Tracing aid: make moe_forward calls from the calling thread record CUDA
- * events at its stage boundaries, on the call's stream.  `events` holds n = 7
- * cudaEvent_t handles (as void*) created by the caller:
+ * Tracing aid: make moe_forward / moe_block_forward calls from the calling
+ * thread record CUDA events at its stage boundaries, on the call's stream.
+ * `events` holds n = 7 cudaEvent_t handles (as void*) created by the caller:
  *   [0] before the router   [1] after router/top-k   [2] after the scan
- *   [3] after the permute   [4] after gate_up        [5] after down
- *   [6] after the combine
+ *   [3] after the permute   [4] after gate_up        [5] after down and the
+ *   combine (which runs in the down kernel's epilogue)   [6] = [5]
  * n = 0 (or events = NULL) turns tracing off.  The handles are used by every
  * later moe_forward on this thread until replaced; the caller keeps them alive.
  * Returns MOE_ERR_SHAPE for any other n.
  */
 moe_status moe_set_trace_events(void* const* events, int n);
+
+/*
+ * Failure detection.  Every wait inside the grouped GEMMs is bounded: after
+ * the wait limit (2 s by default) the waiting role records MOE_ERR_TIMEOUT in
+ * the status word, the CTA's other roles stop at their next wait, copies and
+ * tensor-core work already issued are waited for (up to about 2 s more), and
+ * the kernel returns; moe_poll_status then reports the timeout.
+ * moe_set_wait_limit sets the limit, in seconds within [1e-4, 60], for later
+ * calls from the calling thread; 0 restores the default.  Returns
+ * MOE_ERR_SHAPE otherwise.  No counterpart on the pages.
+ */
+moe_status moe_set_wait_limit(double seconds);
+
+/*
+ * Test hooks for the failure paths (no counterpart on the pages; not for
+ * production use).
+ * moe_set_fault_injection(mode), per calling thread, for later calls:
+ *   0  none (the default)
+ *   1  the gate_up GEMM's weight producer issues nothing, so the MMA's wait
+ *      for its first stage runs out: the call completes with MOE_ERR_TIMEOUT
+ *      in the status word and out holding no meaningful values.
+ * moe_debug_combine runs the weighted combine that the down GEMM runs in its
+ * epilogue on caller tables (device memory): y [T·k, d] fp32, perm [T·k]
+ * (permuted row -> t·k + j), inv [T, k], topk_w [T, k]; out [T, d] bf16.  The
+ * workspace needs 256 + 4·T·ceil(d/128) bytes; its first word is the status
+ * word (read it with moe_poll_status).  An inv entry outside [0, T·k) is left
+ * out of its token's sum and recorded as MOE_ERR_DEVICE_BOUNDS.  perm must be
+ * a permutation of [0, T·k).
+ */
+moe_status moe_set_fault_injection(int mode);
+moe_status moe_debug_combine(const float* y, const int32_t* perm, const int32_t* inv,
+                             const float* topk_w, int64_t T, int d, int k, void* out_bf16,
+                             void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Measurement aid: the dense rate, in TFLOP/s, of the tensor-core MMA kind the
+ * grouped GEMMs issue, with their instruction forms and tile shape (M = 128,
+ * N = 256, operands in shared memory, fp32 accumulators in tensor memory):
+ *   kind 0   tcgen05.mma kind::f16 on bf16 operands (the TMEM design)
+ *   kind 1   tcgen05.mma kind::mxf8f6f4.block_scale, E2M1 x E4M3 with UE8M0
+ *            scales (the block-scaled design)
+ * One CTA per SM issues iters x 4 MMAs back to back; the launch is timed with
+ * CUDA events on `stream` (synchronises it).  workspace: 4 bytes of device
+ * memory for a status word.  Returns MOE_ERR_SHAPE for another kind or iters
+ * outside [1, 2^24].  No counterpart on the pages.
+ */
+moe_status moe_mma_peak(int kind, int iters, double* tflops, void* workspace, void* stream);
 
 /*
  * Size of the scratch array built into the library for moe_forward_noalloc:
@@ -226,8 +301,11 @@ moe_status moe_set_trace_events(void* const* events, int n);
  *   - All calls share the one array and it keeps the last call's contents.
  *     Every call rewrites all of it that it reads, so nothing needs clearing,
  *     but calls that overlap on the GPU (two streams, two threads) race on it:
- *     issue them one after another.  moe_poll_status cannot read this array's
- *     status word; errors from argument checks are returned as usual.
+ *     issue them one after another.  Errors from argument checks are returned
+ *     as usual (T = 0 included); device-side failures of the last call are
+ *     read with moe_poll_status_noalloc.
+ *   - The array's address is looked up once per device and kept: do not call
+ *     this entry point again on a device after cudaDeviceReset.
  */
 moe_status moe_forward_noalloc(const void* x_bf16, int64_t T, int d, int W,
                                const float* router_w, const float* router_b,
@@ -235,6 +313,14 @@ moe_status moe_forward_noalloc(const void* x_bf16, int64_t T, int d, int W,
                                const void* b_gu_bf16, const uint8_t* w_dn_fp4,
                                const uint8_t* w_dn_scale, const void* b_dn_bf16, int E, int k,
                                float limit, float alpha, void* out_bf16, void* stream);
+
+/*
+ * moe_poll_status for moe_forward_noalloc: synchronises `stream`, then reads
+ * the status word at the start of the built-in scratch array on the current
+ * device (MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_DEVICE_BOUNDS from the last
+ * no-alloc call there).  Allocates nothing.  No counterpart on the pages.
+ */
+moe_status moe_poll_status_noalloc(void* stream);
 
 #ifdef __cplusplus
 }

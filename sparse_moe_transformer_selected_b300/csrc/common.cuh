@@ -35,6 +35,14 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
+// Host helpers shared by the launchers (defined in moe_abi.cu).
+// Sets `kernel`'s dynamic shared-memory limit to `bytes` once per device: the
+// attribute belongs to each device's context, so a process that drives
+// several GPUs sets it on each.  Thread-safe.
+cudaError_t set_smem_limit_once(const void* kernel, int bytes);
+// Number of SMs of the current device (cached per device).
+int device_sm_count();
+
 // Router tile: tokens per CTA of the router kernel.  Also the granularity of
 // the per-tile expert histogram the permutation is built from.
 constexpr int kRouterTile = 32;
@@ -87,14 +95,21 @@ struct Workspace {
   size_t perm;         // int32[R]
   size_t inv;          // int32[R]
   size_t rowexp;       // int32[R]   e_t of the token of each permuted row
-  size_t x_perm;       // f16[R, d]  x[t] * 2^e_t; block-scaled design: E4M3 hi [R, d] then lo [R, d]
+  size_t x_perm;       // f16[R, d]  x[t] * 2^e_t; block-scaled design: E4M3 hi [T, d] then lo [T, d]
   size_t h_hi;         // bf16[R, W]; block-scaled design: 4 E4M3 term tables [R, W] over h_hi and h_lo
   size_t h_lo;         // bf16[R, W]
   size_t y;            // float[R, d]
-  size_t sx_hi;        // uint8[R + kGemmBM, ld_sx]  UE8M0 block scales of x hi (block-scaled design)
-  size_t sx_lo;        // uint8[R + kGemmBM, ld_sx]  ... of x lo
+  size_t sx_hi;        // uint8[T, ld_sx]  UE8M0 block scales of x hi (block-scaled design)
+  size_t sx_lo;        // uint8[T, ld_sx]  ... of x lo
+  size_t cnt;          // int32[T, ceil(d/128)]  combine counts per (token, output column tile)
+  size_t rnorm;        // float[T]  1/rms of each token (the block's RMSNorm)
+  // The block's MoE input bf16(RMSNorm(x)) [T, d] lives at the start of the y
+  // region: it is read only by the routing stages, before K4 writes y.
   size_t total;
 };
+
+// Output column tiles of the down GEMM (its weight tile is 128 rows of d).
+inline int down_col_tiles(int d) { return (d + 127) / 128; }
 
 // Row stride of the activation block-scale tables: d/32 bytes rounded up to a
 // multiple of 16 (the rows of a chunk are copied with 1-D bulk copies).
@@ -128,8 +143,10 @@ inline Workspace workspace_layout(int64_t T, int d, int W, int E, int k) {
   ws.h_hi = take(size_t(R) * W * 2);
   ws.h_lo = take(size_t(R) * W * 2);
   ws.y = take(size_t(R) * d * 4);
-  ws.sx_hi = take(size_t(R + kGemmBM) * scale_row_bytes(d));
-  ws.sx_lo = take(size_t(R + kGemmBM) * scale_row_bytes(d));
+  ws.sx_hi = take(size_t(T) * scale_row_bytes(d));
+  ws.sx_lo = take(size_t(T) * scale_row_bytes(d));
+  ws.cnt = take(size_t(T) * down_col_tiles(d) * 4);
+  ws.rnorm = take(size_t(T) * 4);
   ws.total = off;
   return ws;
 }
@@ -137,18 +154,71 @@ inline Workspace workspace_layout(int64_t T, int d, int W, int E, int k) {
 // ---------------------------------------------------------------- kernels --
 // Host-side launchers, one per stage.  All return the launch's cudaError_t.
 
+// Arguments of K1 (router_topk.cu).
+struct RouteArgs {
+  const __nv_bfloat16* x;      // [T, d] the MoE input (for the block: the xn table below)
+  const float* router_w;       // [E, d]
+  const float* router_b;       // [E]
+  // The pre-norm block: x_pre is the residual stream and K1 writes the MoE
+  // input xn = bf16(RMSNorm(x_pre)) = bf16(x_pre / sqrt(mean(x_pre²) + eps) · g)
+  // into the table x points at.  Null x_pre: x is given as is.
+  const __nv_bfloat16* x_pre;  // [T, d] or null
+  __nv_bfloat16* xn;           // [T, d] the table x points at (written when x_pre is given)
+  const float* norm_w;         // [d]
+  float eps;
+  int T, d, E, k;
+  int chunk;                   // token chunk of the grouped GEMMs (for mtile_off)
+  float* logit_part;           // [splits, T, E]
+  int32_t* topk_idx;           // [T, k]
+  float* topk_w;               // [T, k]
+  int32_t* rank;               // [T, k]  rank of (t, j) among its tile's rows of expert e
+  int32_t* tile_counts;        // [ntiles, E]
+  int32_t* tile_base;          // [ntiles, E]
+  int32_t* offsets;            // [E + 1]
+  int32_t* mtile_off;          // [E + 1]
+  int32_t* status;             // status word (cleared by the first kernel)
+  float* rnorm;                // [T] 1 / rms of each token, written with xn
+  int32_t* cnt;                // combine counts, zeroed by the first kernel
+  int64_t ncnt;
+  // Block-scaled design: the MoE input of every token as two E4M3 term tables
+  // [T, d] with UE8M0 block scales [T, ld_sx] (quantize.cuh), or null.
+  uint8_t* xq_hi;
+  uint8_t* xq_lo;
+  uint8_t* sx_hi;
+  uint8_t* sx_lo;
+  int ld_sx;
+  // perm [R] / inv [T k]: written by the last top-k CTA when it runs the scan
+  // (null: left to the scatter kernel)
+  int32_t* perm;
+  int32_t* inv;
+};
+
+// bf16 (nearest, ties to even) of x·g·r for a bf16 value x, an fp32 g and
+// r = 1/rms held in fp64 (r32 = (float)r), decided as for the exact product:
+// the fp32 product lies within 2 ulps of it, so its own rounding is the
+// exact one unless its low 16 bits are within 4 ulps of the halfway point;
+// then the product is recomputed in fp64 (exact for x·g) and rounded there.
+__device__ __forceinline__ float rms_scaled_bf16(float x, float g, float r32, double r64) {
+  const float p = (x * g) * r32;
+  const uint32_t low = __float_as_uint(p) & 0xFFFFu;
+  if (low - 0x7FFCu > 8u) return __bfloat162float(__float2bfloat16_rn(p));
+  const double v = double(x) * double(g) * r64;
+  if (v == 0.0) return 0.f;
+  int e;
+  const double m = frexp(v, &e);                           // v = m 2^e, 0.5 <= |m| < 1
+  return float(ldexp(rint(ldexp(m, 8)), e - 8));           // 8 significant bits, ties to even
+}
+
 // K1: logits (K-split partial sums, then summed in order with the bias), top-k,
 // selected softmax, per-tile histogram and in-tile ranks.  The first kernel
-// also clears the status word.
+// also clears the status word and the combine counts.  With norm_w, the
+// logits are those of RMSNorm(x) = x / sqrt(mean(x²) + eps) · norm_w.
 // When T has at most kFuseScanTiles tiles and tile_base is given, the last
 // top-k CTA also runs the expert scan (tile_base, offsets, mtile_off for
-// `chunk`) and *scanned is set; otherwise the caller launches the scan.
-cudaError_t launch_router_topk(const __nv_bfloat16* x, const float* router_w,
-                               const float* router_b, int T, int d, int E, int k,
-                               float* logit_part, int32_t* topk_idx, float* topk_w,
-                               int32_t* rank, int32_t* tile_counts, int32_t* status, int chunk,
-                               int32_t* tile_base, int32_t* offsets, int32_t* mtile_off,
-                               bool* scanned, cudaStream_t s);
+// `chunk`) and, when r.perm is given, writes perm and inv; *scanned is set.
+// Otherwise the caller launches the scan and the scatter.  With r.xq_hi the
+// token tables of the block-scaled design are written too.
+cudaError_t launch_router_topk(const RouteArgs& r, bool* scanned, cudaStream_t s);
 
 // K2a: expert offsets, per-(tile, expert) bases, prefix of chunks of `chunk` rows.
 cudaError_t launch_route_scan(const int32_t* tile_counts, int ntiles, int E, int chunk,
@@ -183,22 +253,40 @@ struct GemmArgs {
   // block-scaled design (expert_gemm_mx.cu): activations as sums of E4M3
   // terms, x = (hi + lo / 16) * 2^(s - 127) with s the hi block's UE8M0 byte
   // (the lo table holds s - 4), h = (t0 + t1 / 16 + t2 / 256 + t3 / 4096) * 2^h_exp
-  const uint8_t* xq_hi; const uint8_t* xq_lo;   // [R, d]
-  const uint8_t* sx_hi; const uint8_t* sx_lo;   // [R + kGemmBM, ld_sx]
+  const uint8_t* xq_hi; const uint8_t* xq_lo;   // [T, d], one row per token
+  const uint8_t* sx_hi; const uint8_t* sx_lo;   // [T, ld_sx]
   int ld_sx;
   uint8_t* hq;                                  // 4 tables [R, W], term t at hq + t R W
   int h_exp;
+  // K5, run by K4's epilogue (combine.cuh): out[t] = bf16(Σ_j w[t,j] y[inv[t,j]]
+  // (+ resid[t])), counted per (token, output column tile) in cnt
+  int k;
+  const int32_t* perm;        // [R]   permuted row -> t k + j
+  const int32_t* inv;         // [T k] (t, j) -> permuted row
+  const float* topk_w;        // [T k]
+  int32_t* cnt;               // [T, n_mt_dn], zero when K4 starts
+  int n_mt_dn;
+  __nv_bfloat16* out;         // [T, d]
+  const __nv_bfloat16* resid; // [T, d] or null
+  // failure detection: a bounded wait gives up after wait_ns nanoseconds
+  // (status word MOE_ERR_TIMEOUT); inject = 1 (a test hook) makes gate_up's
+  // weight producer issue nothing, so the waits for its stages run out
+  long long wait_ns;
+  int inject;
 };
 
-// K3: h = swiglu(x_perm · W_gu^T + b_gu), per expert segment.
-cudaError_t launch_gateup(const GemmArgs& a, cudaStream_t s);
-// K4: y = (h_hi + h_lo) · W_dn^T + b_dn, per expert segment.
-cudaError_t launch_down(const GemmArgs& a, cudaStream_t s);
+// Nanoseconds of the GPU's global timer (for wait limits).
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
 
-// K3 / K4 with the dequantised weights as the MMA's A operand in tensor memory
-// (expert_gemm_tmem.cu).  Same arguments and results as launch_gateup /
-// launch_down; usable when its shared-memory plan fits (the reduction length
-// sets the size of the per-unit scale buffers).
+// K3: h = swiglu(x_perm · W_gu^T + b_gu), per expert segment, and
+// K4: y = (h_hi + h_lo) · W_dn^T + b_dn with the combine in its epilogue,
+// with the dequantised weights as the MMA's A operand in tensor memory
+// (expert_gemm_tmem.cu); usable when its shared-memory plan fits (the
+// reduction length sets the size of the per-unit scale buffers).
 bool expert_gemm_tmem_fits(const GemmArgs& a);
 // Token chunk of the TMEM design for R routed rows over E experts: small
 // chunks (N = 16) when experts get few tokens, so an activation stage is a
@@ -222,19 +310,5 @@ int mx_hidden_exp(float limit);
 cudaError_t launch_gateup_mx(const GemmArgs& a, cudaStream_t s);
 cudaError_t launch_down_mx(const GemmArgs& a, cudaStream_t s);
 
-// K2b, block-scaled design: perm / inv and x[t] as E4M3 hi / lo pairs with
-// one UE8M0 scale per 32-element block (hi: 2^(e_b) with e_b putting the
-// block's largest |x| in [128, 256); lo: the remainder times 16).
-cudaError_t launch_route_scatter_mx(const __nv_bfloat16* x, int T, int d, int E, int k,
-                                    const int32_t* topk_idx, const int32_t* rank,
-                                    const int32_t* tile_base, int32_t* perm, int32_t* inv,
-                                    uint8_t* xq_hi, uint8_t* xq_lo, uint8_t* sx_hi,
-                                    uint8_t* sx_lo, int ld_sx, int32_t* status, cudaStream_t s);
-
-// K5: out[t] = bf16(Σ_j w[t,j] · y[inv[t,j]]); a row index outside [0, T·k)
-// is skipped and recorded in the status word.
-cudaError_t launch_combine(const float* y, const float* topk_w, const int32_t* inv,
-                           int T, int d, int k, __nv_bfloat16* out, int32_t* status,
-                           cudaStream_t s);
 
 }  // namespace moe

@@ -10,13 +10,13 @@
 // codes, each 32-element K block with a UE8M0 scale held in tensor memory, so
 // the weights go from HBM to the tensor core without being converted.  The
 // activations are the B side as sums of E4M3 terms, each term with its own
-// block scales, stacked along N: rows t nb .. t nb + nb - 1 of B are term t of
-// the chunk's nb tokens, and the epilogue adds accumulator columns t nb + j.
+// block scales, stacked along N, and the epilogue adds a token's term columns.
+// A work unit is a chunk of up to 8 tokens of one expert.
 //   gate_up: x = hi + lo / 16 (2 terms; exact for bf16 values within 2^-7
 //            of their 32-block's largest)
 //   down:    h = (t0 + t1 / 16 + t2 / 256 + t3 / 4096) 2^h_exp (4 terms,
 //            about 16 significant bits)
-// One MMA covers M = 128 weight rows, N = terms x nb, K = 32.
+// One MMA covers M = 128 weight rows, N = 32, K = 32.
 //
 //   D[weight row, j] = Σ_k A[row, k] 2^(sa - 127) · B[j, k] 2^(sb - 127)
 //
@@ -27,20 +27,29 @@
 //      type wants the tensor's row length a multiple of 128, so the map covers
 //      the first K - K % 128 codes of each row and a second map, whose base
 //      is the row's last 128 codes, serves the tail.
-//   B  TMA of E4M3 bytes, one box of 128 K x nb rows per operand (hi, lo).
+//   B  gate_up: the chunk's token rows of the per-token E4M3 tables (the router
+//      quantises each token once), gathered by TMA tile::gather4: four token
+//      rows of 128 K land in the first four rows of a 1024-byte swizzle atom,
+//      so term t holds tokens 0-3 in rows 16t .. 16t + 3 and tokens 4-7 in
+//      rows 16t + 8 .. 16t + 11 (B row of token j: 16t + 8 (j / 4) + j % 4);
+//      the other rows only feed accumulator columns the epilogue ignores.
+//      down: TMA boxes of 128 K x 8 rows of the h term tables (permuted rows,
+//      written by gate_up), term t in rows 8t .. 8t + 7.
 // Scales in tensor memory, written once per unit by four warps with tcgen05.st
 // (a row's 4 scale bytes of 4 consecutive K blocks share a 32-bit column; the
 // MMA picks the byte with the descriptor's scale-factor ID).
 //
 // Persistent kernel, one CTA per SM, 12 warps:
-//   warp 0      producer: per unit the scale rows (1-D bulk copies), per stage
-//               A and B (TMA); one ring of stages of 256 K
+//   warp 0      producer: per unit the weight scale rows (1-D bulk copies),
+//               per stage A and B (TMA); one ring of stages of 256 K
 //   warp 1      MMA issuer (one elected thread)
 //   warp 2      TMEM allocator: 512 columns (2 accumulators of 64, then two
 //               sets of A and B scale columns)
 //   warps 4-7   epilogue, TMEM lane quarter = warp % 4
-//   warps 8-11  scale writers, TMEM lane quarter = warp % 4
+//   warps 8-11  scale writers, TMEM lane quarter = warp % 4 (gate_up's
+//               activation scales read from L2, one token row per lane)
 // Work unit = (token chunk of one expert, weight tile of 128 rows), chunk-major.
+#include "combine.cuh"
 #include "common.cuh"
 #include "map_cache.cuh"
 #include "tc_ptx.cuh"
@@ -58,7 +67,8 @@ namespace {
 constexpr int kMW = 128;                      // weight rows per unit (MMA M)
 constexpr int kBoxK = 128;                    // K per box: one 128-byte swizzle row
 constexpr int kBoxBytesA = kMW * kBoxK;       // 16 KB, one byte per code in shared memory
-constexpr int kNB = 16;                       // token chunk
+constexpr int kNB = 8;                        // token chunk
+constexpr int kBRows = 32;                    // MMA N: B rows of a box
 constexpr int kHTerms = 4;                    // E4M3 terms of h
 constexpr int kXTerms = 2;                    // E4M3 terms of x
 constexpr int kAccCols = 64;                  // TMEM columns per accumulator
@@ -67,7 +77,7 @@ constexpr int kThreads = 384;
 constexpr int kWarpProd = 0, kWarpMMA = 1, kWarpTmem = 2, kWarpEpi0 = 4, kWarpSf0 = 8;
 constexpr int kTmemCols = 512;
 constexpr int kMaxGroups = (kTmemCols - 2 * kAccCols) / 16;   // SF groups (4 K blocks each)
-constexpr long long kSpinLimit = 4000000000ll;
+constexpr long long kSpinLimit = 4000000000ll;   // clock cycles: the final drains
 constexpr int kMaxSmem = 232448;
 // stage ring (full + empty), scales (2 + 2), scale columns (2 + 2),
 // accumulators (2 + 2), final drain
@@ -75,19 +85,20 @@ constexpr int kNumBars = 2 * kMaxStages + 4 + 4 + 4 + 1;
 
 enum class Mode { GateUp, Down };
 
-// Bounded wait: true when the phase completed; false after a timeout (code in
-// status[0], the waiting role's tag in status[4]) or when another thread of
-// the CTA gave up.
+// Bounded wait: true when the phase completed; false after limit_ns
+// nanoseconds (code in status[0], the waiting role's tag in status[4]) or when
+// another thread of the CTA gave up.
 __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                           int32_t* status, uint32_t backoff_ns = 0, int tag = 0) {
+                                           int32_t* status, long long limit_ns,
+                                           uint32_t backoff_ns = 0, int tag = 0) {
   if (ptx::mbar_try_wait_sleep(bar, parity, 20000u)) return true;
-  const long long t0 = clock64();
+  const unsigned long long t0 = global_ns();
   for (uint32_t n = 1;; ++n) {
     if (backoff_ns) __nanosleep(backoff_ns);
     if (ptx::mbar_try_wait_sleep(bar, parity, 20000u)) return true;
     if ((n & 31) == 0) {
       if (*abort_flag) return false;
-      if (clock64() - t0 > kSpinLimit) {
+      if ((long long)(global_ns() - t0) > limit_ns) {
         *abort_flag = 1;
         atomicMax(status, kStatusTimeout);
         atomicExch(status + 4, tag);
@@ -121,19 +132,6 @@ struct Inflight {
   }
 };
 
-// All `count` threads of named barrier `id` learn whether every one of them
-// passed v (bar.red.and): the epilogue warps leave their loop together.
-__device__ __forceinline__ bool group_all(uint32_t id, uint32_t count, bool v) {
-  uint32_t r;
-  asm volatile(
-      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, %2, %3, p;\n"
-      " selp.u32 %0, 1, 0, q;\n}\n"
-      : "=r"(r)
-      : "r"(uint32_t(v)), "r"(id), "r"(count)
-      : "memory");
-  return r != 0;
-}
-
 __device__ __forceinline__ uint32_t to_e4m3(float v) {
   return uint32_t(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
 }
@@ -146,7 +144,7 @@ struct Geo {
   int K, nsb, groups;        // reduction length, scale bytes per weight row, SF groups
   int nbox_main, tail;       // 128-K boxes from the main map; K % 128 (0: no tail box)
   int nbox, nstage;          // boxes per unit (main + tail), stages of 2 boxes
-  int NT, N;                 // B terms; MMA N = NT nb
+  int NT, rpt, N;            // B terms, B rows per term, MMA N = NT rpt
   int box_rows;              // A rows per TMA box: 64 (gate and up halves) or 128
   int a_stage, b_stage;      // bytes per stage
   int sc_a, sc_b, sc_buf;    // scale bytes per unit: A rows, one B table, buffer stride
@@ -165,12 +163,13 @@ __host__ __device__ inline Geo geometry(int d, int W, int nb, int ld_sx, int sta
   g.nbox = g.nbox_main + (g.tail ? 1 : 0);
   g.nstage = (g.nbox + 1) / 2;
   g.NT = (M == Mode::GateUp) ? kXTerms : kHTerms;
-  g.N = g.NT * nb;
+  g.rpt = kBRows / g.NT;                   // gate_up: two atoms of 4 tokens; down: 8 rows
+  g.N = kBRows;
   g.box_rows = (M == Mode::GateUp) ? kMW / 2 : kMW;
   g.a_stage = 2 * kBoxBytesA;
   g.b_stage = 2 * g.N * kBoxK;
   g.sc_a = (kMW * g.nsb + 15) / 16 * 16;
-  g.sc_b = (M == Mode::GateUp) ? nb * ld_sx : 0;
+  g.sc_b = 0;                               // (activation scales are read from L2)
   g.sc_buf = g.sc_a + 2 * g.sc_b;
   g.stages = stages;
   int off = stages * g.a_stage;
@@ -182,7 +181,8 @@ __host__ __device__ inline Geo geometry(int d, int W, int nb, int ld_sx, int sta
   off += (M == Mode::GateUp) ? (kMW / 2) * kNB * 4 : 0;
   off = (off + 7) & ~7;
   g.off_bars = off;
-  off += kNumBars * 8 + 16;
+  off += kNumBars * 8 + 16;           // barriers, TMEM base, abort flag
+  off += (M == Mode::Down) ? combine_smem_bytes(kNB) : 0;
   g.total = off;
   return g;
 }
@@ -256,6 +256,7 @@ moe_expert_gemm_mx(const __grid_constant__ CUtensorMap map_w,     // main codes
   uint64_t* mma_done = acc_empty + 2;
   uint32_t* tmem_base_p = reinterpret_cast<uint32_t*>(smem + G.off_bars + kNumBars * 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + G.off_bars + kNumBars * 8 + 4);
+  uint8_t* comb = smem + G.off_bars + kNumBars * 8 + 16;         // combine lists (down)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -293,7 +294,7 @@ moe_expert_gemm_mx(const __grid_constant__ CUtensorMap map_w,     // main codes
 
   if (warp == kWarpProd) {
     // ------------------------------------------------------------ producer --
-    if (ptx::elect_one()) {
+    if (ptx::elect_one() && !(kGateUp && a.inject == 1)) {
       ptx::tma_prefetch_desc(&map_w);
       if (G.tail) ptx::tma_prefetch_desc(&map_wt);
       const CUtensorMap* mb[4] = {&map_b0, &map_b1, &map_b2, &map_b3};
@@ -321,18 +322,16 @@ moe_expert_gemm_mx(const __grid_constant__ CUtensorMap map_w,     // main codes
       // the unit before it), so the MMA finds them in TMEM.
       auto load_scales = [&](int uu, int qq) -> bool {
         const Unit w = unit_of(a, n_mt, uu);
-        if (!wait_phase(&sc_empty[0], (qq & 1) ^ 1, abort_flag, a.status, 64, 5)) return false;
+        if (!wait_phase(&sc_empty[0], (qq & 1) ^ 1, abort_flag, a.status, a.wait_ns, 64, 5)) return false;
         uint8_t* dst = scb;
         int ra, rb, nrows;
         rows_of(w, ra, rb, nrows);
         const uint32_t bytes = uint32_t(nrows * G.nsb);
         if constexpr (kGateUp) {
-          const uint32_t bbytes = uint32_t(G.sc_b);
-          ptx::mbar_arrive_expect_tx(&sc_full[0], 2 * bytes + 2 * bbytes);
+          // the weight scale rows (the activations' are read by the writers)
+          ptx::mbar_arrive_expect_tx(&sc_full[0], 2 * bytes);
           ptx::bulk_load(dst, wscale + size_t(ra) * G.nsb, bytes, &sc_full[0]);
           ptx::bulk_load(dst + (kMW / 2) * G.nsb, wscale + size_t(rb) * G.nsb, bytes, &sc_full[0]);
-          ptx::bulk_load(dst + G.sc_a, a.sx_hi + size_t(w.r0) * a.ld_sx, bbytes, &sc_full[0]);
-          ptx::bulk_load(dst + G.sc_a + G.sc_b, a.sx_lo + size_t(w.r0) * a.ld_sx, bbytes, &sc_full[0]);
         } else {
           ptx::mbar_arrive_expect_tx(&sc_full[0], bytes);
           ptx::bulk_load(dst, wscale + size_t(ra) * G.nsb, bytes, &sc_full[0]);
@@ -346,15 +345,22 @@ moe_expert_gemm_mx(const __grid_constant__ CUtensorMap map_w,     // main codes
         const Unit w = unit_of(a, n_mt, u);
         int row_a, row_b, nrows;
         rows_of(w, row_a, row_b, nrows);
+        // gate_up: the chunk's tokens (rows past the chunk repeat its first)
+        int tok[kNB];
+        if constexpr (kGateUp) {
+#pragma unroll
+          for (int j = 0; j < kNB; ++j) tok[j] = __ldg(a.perm + w.r0 + (j < w.n ? j : 0)) / a.k;
+        }
         for (int s = 0; s < G.nstage; ++s) {
           // the next unit's scales, once this unit's first stages are out
           if (s == min(1, G.nstage - 1) && u + int(gridDim.x) < units &&
               !load_scales(u + int(gridDim.x), q + 1)) { ok = false; break; }
-          if (!wait_phase(&empty[st.slot], st.phase ^ 1, abort_flag, a.status, 64, 4)) { ok = false; break; }
+          if (!wait_phase(&empty[st.slot], st.phase ^ 1, abort_flag, a.status, a.wait_ns, 64, 4)) { ok = false; break; }
           const int i0 = 2 * s, i1 = min(2 * s + 2, G.nbox);
-          // the 4-bit TMA counts the packed bytes it reads (half of what it writes)
-          ptx::mbar_arrive_expect_tx(&full[st.slot],
-                                     uint32_t((i1 - i0) * (kBoxBytesA / 2 + G.N * kBoxK)));
+          // the 4-bit TMA counts the packed bytes it reads (half of what it
+          // writes); gate_up's B is two gathers of 4 rows per term
+          const uint32_t b_box = kGateUp ? uint32_t(G.NT * 2 * 4 * kBoxK) : uint32_t(G.N * kBoxK);
+          ptx::mbar_arrive_expect_tx(&full[st.slot], uint32_t(i1 - i0) * (kBoxBytesA / 2 + b_box));
           uint8_t* da = sa + st.slot * G.a_stage;
           uint8_t* db = sb + st.slot * G.b_stage;
           for (int i = i0; i < i1; ++i) {
@@ -364,11 +370,19 @@ moe_expert_gemm_mx(const __grid_constant__ CUtensorMap map_w,     // main codes
             const CUtensorMap* mw = main_box ? &map_w : &map_wt;
             const int xa = main_box ? i * kBoxK : 0;
             ptx::tma_load_2d(dai, mw, &full[st.slot], xa, row_a);
-            if constexpr (kGateUp)
-              ptx::tma_load_2d(dai + (kMW / 2) * kBoxK, mw, &full[st.slot], xa, row_b);
             const int xb = i * kBoxK;
-            for (int t = 0; t < G.NT; ++t)
-              ptx::tma_load_2d(dbi + t * a.nb * kBoxK, mb[t], &full[st.slot], xb, w.r0);
+            if constexpr (kGateUp) {
+              ptx::tma_load_2d(dai + (kMW / 2) * kBoxK, mw, &full[st.slot], xa, row_b);
+              for (int t = 0; t < G.NT; ++t) {
+                ptx::tma_gather4(dbi + t * G.rpt * kBoxK, mb[t], &full[st.slot], xb, tok[0], tok[1],
+                                 tok[2], tok[3]);
+                ptx::tma_gather4(dbi + t * G.rpt * kBoxK + 1024, mb[t], &full[st.slot], xb, tok[4],
+                                 tok[5], tok[6], tok[7]);
+              }
+            } else {
+              for (int t = 0; t < G.NT; ++t)
+                ptx::tma_load_2d(dbi + t * G.rpt * kBoxK, mb[t], &full[st.slot], xb, w.r0);
+            }
           }
           in_st.mark(st.slot, st.phase);
           st.next(S);
@@ -391,15 +405,15 @@ moe_expert_gemm_mx(const __grid_constant__ CUtensorMap map_w,     // main codes
       int q = 0;
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++q) {
         const int buf = q & 1;
-        if (!wait_phase(&acc_empty[buf], ((q >> 1) & 1) ^ 1, abort_flag, a.status, 0, 2)) { ok = false; break; }
-        if (!wait_phase(&sf_full[buf], (q >> 1) & 1, abort_flag, a.status, 0, 3)) { ok = false; break; }
+        if (!wait_phase(&acc_empty[buf], ((q >> 1) & 1) ^ 1, abort_flag, a.status, a.wait_ns, 0, 2)) { ok = false; break; }
+        if (!wait_phase(&sf_full[buf], (q >> 1) & 1, abort_flag, a.status, a.wait_ns, 0, 3)) { ok = false; break; }
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + buf * kAccCols;
         const uint32_t sfa = tmem_base + sfa_col0 + buf * 4 * G.groups;
         const uint32_t sfb = tmem_base + sfb_col0 + buf * 4 * G.groups;
         uint32_t acc = 0;
         for (int s = 0; s < G.nstage; ++s) {
-          if (!wait_phase(&full[st.slot], st.phase, abort_flag, a.status, 0, 1)) { ok = false; break; }
+          if (!wait_phase(&full[st.slot], st.phase, abort_flag, a.status, a.wait_ns, 0, 1)) { ok = false; break; }
           ptx::tc_fence_after();
           const uint32_t a_addr = ptx::smem_u32(sa + st.slot * G.a_stage);
           const uint32_t b_addr = ptx::smem_u32(sb + st.slot * G.b_stage);
@@ -442,8 +456,8 @@ moe_expert_gemm_mx(const __grid_constant__ CUtensorMap map_w,     // main codes
     int q = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x, ++q) {
       const int sbuf = q & 1;                      // TMEM scale set
-      const bool ok = wait_phase(&sc_full[0], q & 1, abort_flag, a.status, 64, 6) &&
-                      wait_phase(&sf_empty[sbuf], ((q >> 1) & 1) ^ 1, abort_flag, a.status, 64, 7);
+      const bool ok = wait_phase(&sc_full[0], q & 1, abort_flag, a.status, a.wait_ns, 64, 6) &&
+                      wait_phase(&sf_empty[sbuf], ((q >> 1) & 1) ^ 1, abort_flag, a.status, a.wait_ns, 64, 7);
       if (!__all_sync(0xffffffffu, ok)) break;
       const uint8_t* buf = scb;
       const uint32_t ta = tmem_base + lane_addr + sfa_col0 + sbuf * 4 * G.groups;
@@ -455,24 +469,29 @@ moe_expert_gemm_mx(const __grid_constant__ CUtensorMap map_w,     // main codes
         const uint32_t wa = scale_word(ra, g, G.nsb);
         ptx::tmem_st_32x32b_x4(ta + 4 * g, wa, wa, wa, wa);
       }
-      // B: row n of B (term n / nb of token n % nb) at lane n % 32, column
-      // 4g + n / 32, in every lane quarter.  x terms: the scatter's block
-      // scales (hi table, lo table); h terms: 2^(h_exp - 4t) for every block.
-      const int n0 = lane, n1 = lane + 32;
-      const int t0 = n0 / a.nb, t1 = n1 / a.nb;
-      const uint32_t c0 = uint32_t(127 + a.h_exp - 4 * t0) * 0x01010101u;
-      const uint32_t c1 = uint32_t(127 + a.h_exp - 4 * t1) * 0x01010101u;
-      for (int g = 0; g < G.groups; ++g) {
-        uint32_t w0, w1 = 0;
-        if constexpr (kGateUp) {
-          const uint8_t* tab = buf + G.sc_a + t0 * G.sc_b;
-          w0 = scale_word(tab + (n0 % a.nb) * a.ld_sx, g, G.nsb);
-        } else {
-          w0 = c0;
-          w1 = c1;
-        }
-        if (G.N > 32) ptx::tmem_st_32x32b_x2(tb + 4 * g, w0, w1);
-        else ptx::tmem_st_32x32b_x1(tb + 4 * g, w0);
+      // B: row n = lane of B at lane n of every lane quarter, column 4g
+      // (N = 32).  x terms: row n is term n / 16, token 4 ((n % 16) / 8) +
+      // n % 4 of the chunk (rows with n % 8 >= 4 are unused), whose scale row
+      // of that term's table this lane reads from L2; h terms: row n is term
+      // n / 8, scale 2^(h_exp - 4t) for every block.
+      const int t0 = lane / G.rpt;
+      if constexpr (kGateUp) {
+        const Unit w = unit_of(a, n_mt, u);
+        const int jx = 4 * ((lane % 16) / 8) + (lane % 4);
+        const int tk = __ldg(a.perm + w.r0 + (jx < w.n ? jx : 0)) / a.k;
+        const uint32_t* srow =
+            reinterpret_cast<const uint32_t*>((t0 ? a.sx_lo : a.sx_hi) + size_t(tk) * a.ld_sx);
+        // the row's scale words, all loads in flight before the first store
+        uint32_t sw[kMaxGroups];
+#pragma unroll
+        for (int g = 0; g < kMaxGroups; ++g)
+          if (g < G.groups) sw[g] = __ldg(srow + g);
+#pragma unroll
+        for (int g = 0; g < kMaxGroups; ++g)
+          if (g < G.groups) ptx::tmem_st_32x32b_x1(tb + 4 * g, sw[g]);
+      } else {
+        const uint32_t c0 = uint32_t(127 + a.h_exp - 4 * t0) * 0x01010101u;
+        for (int g = 0; g < G.groups; ++g) ptx::tmem_st_32x32b_x1(tb + 4 * g, c0);
       }
       ptx::tmem_st_wait();
       ptx::tc_fence_before();
@@ -491,26 +510,27 @@ moe_expert_gemm_mx(const __grid_constant__ CUtensorMap map_w,     // main codes
     for (int u = blockIdx.x; u < units; u += gridDim.x, ++q) {
       const Unit w = unit_of(a, n_mt, u);
       const int buf = q & 1;
-      const bool ok0 = wait_phase(&acc_full[buf], (q >> 1) & 1, abort_flag, a.status, 256, 8);
-      if (!group_all(1, 128, ok0)) break;
+      const bool ok0 = wait_phase(&acc_full[buf], (q >> 1) & 1, abort_flag, a.status, a.wait_ns, 256, 8);
+      if (!ptx::group_all(1, 128, ok0)) break;
       ptx::tc_fence_after();
       const uint32_t taddr = tmem_base + (uint32_t(quarter * 32) << 16) + buf * kAccCols;
-      // D column t nb + j holds term t of token j (nb = 16)
+      // D column n holds B row n: gate_up term n / 16 of token
+      // 4 ((n % 16) / 8) + n % 4; down term n / 8 of token n % 8
       float z[kNB];
       {
-        uint32_t v[kHTerms][16];
+        uint32_t v[2][16];
         ptx::tmem_ld_32x32b_x16(taddr, v[0]);
-        ptx::tmem_ld_32x32b_x16(taddr + kNB, v[1]);
-        if (!kGateUp) {
-          ptx::tmem_ld_32x32b_x16(taddr + 2 * kNB, v[2]);
-          ptx::tmem_ld_32x32b_x16(taddr + 3 * kNB, v[3]);
-        }
+        ptx::tmem_ld_32x32b_x16(taddr + 16, v[1]);
         ptx::tmem_ld_wait();
 #pragma unroll
         for (int j = 0; j < kNB; ++j) {
-          float acc = __uint_as_float(v[0][j]) + __uint_as_float(v[1][j]);
-          if (!kGateUp) acc += __uint_as_float(v[2][j]) + __uint_as_float(v[3][j]);
-          z[j] = acc;
+          if constexpr (kGateUp) {
+            const int c = 8 * (j / 4) + j % 4;
+            z[j] = __uint_as_float(v[0][c]) + __uint_as_float(v[1][c]);
+          } else {
+            z[j] = (__uint_as_float(v[0][j]) + __uint_as_float(v[0][8 + j])) +
+                   (__uint_as_float(v[1][j]) + __uint_as_float(v[1][8 + j]));
+          }
         }
       }
       ptx::tc_fence_before();
@@ -548,12 +568,15 @@ moe_expert_gemm_mx(const __grid_constant__ CUtensorMap map_w,     // main codes
         ptx::named_barrier(3, 128);              // xch is reused by the next unit
       } else {
         const int n = w.mt * kMW + m;
-        if (n < a.d) {
+        const bool nvalid = n < a.d;
+        if (nvalid) {
           const float bias = __bfloat162float(a.b_dn[size_t(w.e) * a.d + n]);
 #pragma unroll
           for (int j = 0; j < kNB; ++j)
             if (j < w.n) a.y[size_t(w.r0 + j) * a.d + n] = z[j] + bias;
         }
+        // K5: the weighted sum of each token whose k rows are now all stored
+        combine_tile<4>(a, w.r0, w.n, w.mt, m, comb, kNB, 2);
       }
     }
   }
@@ -598,17 +621,6 @@ cudaError_t make_map(CUtensorMap* map, CUtensorMapDataType dt, const void* base,
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-int num_sms() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 148;
-  }
-  return n;
-}
-
 template <Mode M>
 int plan_stages(const GemmArgs& a) {
   const Geo g0 = geometry<M>(a.d, a.W, a.nb, a.ld_sx, 0);
@@ -637,15 +649,14 @@ cudaError_t make_maps(const GemmArgs& a, CUtensorMap* mw, CUtensorMap* mwt, CUte
       *mwt = *mw;
     }
   }
-  const uint8_t* terms[4];
-  if (gu) {
-    terms[0] = terms[2] = a.xq_hi;
-    terms[1] = terms[3] = a.xq_lo;
-  } else {
-    for (int t = 0; t < 4; ++t) terms[t] = a.hq + size_t(t) * a.R * a.W;
+  // B: gate_up's token tables [T, d] (a one-row box per gather4 coordinate),
+  // down's h term tables [R, W] (boxes of a chunk's 8 rows)
+  const long long T = a.R / a.k;
+  for (int t = 0; t < 4 && e == cudaSuccess; ++t) {
+    const uint8_t* base = gu ? ((t & 1) ? a.xq_lo : a.xq_hi) : a.hq + size_t(t) * a.R * a.W;
+    e = make_map(&mb[t], CU_TENSOR_MAP_DATA_TYPE_UINT8, base, gu ? T : a.R, K, K, kBoxK,
+                 gu ? 1 : a.nb);
   }
-  for (int t = 0; t < 4 && e == cudaSuccess; ++t)
-    e = make_map(&mb[t], CU_TENSOR_MAP_DATA_TYPE_UINT8, terms[t], a.R, K, K, kBoxK, a.nb);
   return e;
 }
 
@@ -675,17 +686,14 @@ cudaError_t launch(const GemmArgs& a, cudaStream_t s) {
   const Geo g = geometry<M>(a.d, a.W, a.nb, a.ld_sx, stages);
   const size_t smem = size_t(g.total) + 1024;
   if (smem > size_t(kMaxSmem)) return cudaErrorInvalidConfiguration;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(moe_expert_gemm_mx<M>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
+  {
+    cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(moe_expert_gemm_mx<M>), kMaxSmem);
     if (e != cudaSuccess) return e;
-    configured = true;
   }
   // the six maps, from the cache when this layer's buffers were seen before
   struct Key {
     const void* p[7];
-    int R, d, W, E, nb;
+    int R, d, W, E, nb, k;
   } key;
   memset(&key, 0, sizeof(key));
   key.p[0] = (M == Mode::GateUp) ? a.w_gu : a.w_dn;
@@ -697,6 +705,7 @@ cudaError_t launch(const GemmArgs& a, cudaStream_t s) {
   key.W = a.W;
   key.E = a.E;
   key.nb = a.nb;
+  key.k = a.k;
   static MapCache<Key, 6> cache;
   CUtensorMap maps[6];
   if (!cache.find(key, maps)) {
@@ -710,7 +719,7 @@ cudaError_t launch(const GemmArgs& a, cudaStream_t s) {
   const int rows_per_tile = (M == Mode::GateUp) ? kMW / 2 : kMW;
   const long long n_mt = (n_out + rows_per_tile - 1) / rows_per_tile;
   const long long units_bound = (long long)(a.R / a.nb + a.E) * n_mt;
-  const int grid = int(units_bound < num_sms() ? units_bound : num_sms());
+  const int grid = int(units_bound < device_sm_count() ? units_bound : device_sm_count());
   return launch_pdl(moe_expert_gemm_mx<M>, dim3(grid), dim3(kThreads), smem, s, mw, mwt, mb[0], mb[1],
                     mb[2], mb[3], a, stages);
 }

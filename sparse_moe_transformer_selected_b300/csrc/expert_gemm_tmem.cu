@@ -34,15 +34,19 @@
 //            largest scale byte of weight row n; B = x · 2^e_t in f16 (the
 //            permute stage scales each token so its largest |x| lies in
 //            [2^14, 2^15), which holds every bf16 value).  The epilogue
-//            multiplies by 2^(r_n - 127) · 2^(-e_t).  Exact for scale bytes up
-//            to 240 whose block lies within 2^14 of its row's largest; a block
+//            multiplies by 2^(r_n - 127) · 2^(-e_t).  Exact for every scale
+//            byte whose block lies within 2^14 of its row's largest; a block
 //            further below contributes nothing (its factor would be an f16
-//            subnormal).
+//            subnormal): each of its terms is below 2^-14 of the largest
+//            weights of the row.
 //   down:    when the clamp bounds h inside the f16 range, as gate_up with
 //            B = h as two f16 terms (hi + lo); otherwise A = E2M1 -> f16 bits
-//            moved into a bf16 field (a factor 2^-112) times 2^(s - 15), exact
-//            for every scale byte <= 142, and B = h as two bf16 terms.  Two MMAs
+//            moved into a bf16 field (a factor 2^-112) times 2^(s - c_n) with
+//            c_n = max(15, r_n - 127), exact for every scale byte (blocks more
+//            than 2^253 below the row's largest aside), the epilogue
+//            multiplying by 2^(c_n - 15); B = h as two bf16 terms.  Two MMAs
 //            per K step (hi, lo).
+#include "combine.cuh"
 #include "common.cuh"
 #include "map_cache.cuh"
 #include "tc_ptx.cuh"
@@ -79,7 +83,7 @@ constexpr int kCodeBoxRows = 64;
 // code, A and B rings (full + empty each), scales and accumulators (2 + 2
 // each), the row-factor ring, and the final MMA drain
 constexpr int kNumBars = 2 * kMaxC + 2 * kMaxA + 2 * kMaxB + 4 + 4 + 2 * kRing + 1;
-constexpr long long kSpinLimit = 4000000000ll;   // clock cycles before a wait gives up
+constexpr long long kSpinLimit = 4000000000ll;   // clock cycles: the final drains
 constexpr int kMaxSmem = 232448;                 // 227 KB opt-in per CTA
 
 // K of one activation stage: 256 for small chunks (a stage is a few KB and
@@ -99,12 +103,10 @@ struct Cfg;
 template <>
 struct Cfg<Mode::GateUp> {
   static constexpr int NOPS = 1;      // B operands per K step: x
-  static constexpr bool kBf16 = false;
 };
 template <>
 struct Cfg<Mode::Down> {
   static constexpr int NOPS = 2;      // h_hi, h_lo
-  static constexpr bool kBf16 = true;
 };
 
 struct Lay {
@@ -131,7 +133,8 @@ __host__ __device__ inline Lay layout(int nsb, int nb, int nc, int nbs) {
   l.bars = off;
   off += kNumBars * 8;
   l.misc = off;
-  off += 16;
+  off += 16;                          // TMEM base, abort flag
+  off += (M == Mode::Down) ? combine_smem_bytes(kNBMax) : 0;   // combine lists
   l.total = off;
   return l;
 }
@@ -159,8 +162,9 @@ __device__ __forceinline__ Unit unit_of(const GemmArgs& a, int n_mt, int u) {
   return w;
 }
 
-// Bounded wait: true when the phase completed; false after a timeout (recorded
-// in the status word) or when another thread of the CTA gave up.
+// Bounded wait: true when the phase completed; false after limit_ns
+// nanoseconds (recorded in the status word) or when another thread of the CTA
+// gave up.
 // The thread sleeps inside the wait instruction (woken when the phase
 // completes) and wakes at least every 20 us to check the abort flag and the
 // time limit.  `backoff_ns` > 0 also sleeps that long between polls: for
@@ -168,15 +172,16 @@ __device__ __forceinline__ Unit unit_of(const GemmArgs& a, int n_mt, int u) {
 // ahead (the producers), so polling does not take issue slots from the
 // dequantisers that share the SM partition.
 __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                           int32_t* status, uint32_t backoff_ns = 0) {
+                                           int32_t* status, long long limit_ns,
+                                           uint32_t backoff_ns = 0) {
   if (ptx::mbar_try_wait_sleep(bar, parity, 20000u)) return true;
-  const long long t0 = clock64();
+  const unsigned long long t0 = global_ns();
   for (uint32_t n = 1;; ++n) {
     if (backoff_ns) __nanosleep(backoff_ns);
     if (ptx::mbar_try_wait_sleep(bar, parity, 20000u)) return true;
     if ((n & 31) == 0) {                        // the abort flag and the clock, now and then
       if (*abort_flag) return false;
-      if (clock64() - t0 > kSpinLimit) {
+      if ((long long)(global_ns() - t0) > limit_ns) {
         *abort_flag = 1;
         atomicMax(status, kStatusTimeout);
         return false;
@@ -224,9 +229,9 @@ __device__ __forceinline__ uint32_t f16x2_pow2(int delta) {
   return b | (b << 16);
 }
 
-// 2^p as a bf16x2 pair, -126 <= p <= 127.
+// 2^p as a bf16x2 pair for p <= 127; 0 below the bf16 normal range.
 __device__ __forceinline__ uint32_t bf16x2_pow2(int p) {
-  const uint32_t b = uint32_t(p + 127) << 7;
+  const uint32_t b = uint32_t(max(p + 127, 0)) << 7;
   return b | (b << 16);
 }
 
@@ -276,10 +281,17 @@ struct Dequant<Mode::GateUp> {
   }
 };
 
+// The bf16 form's row offset c_n = max(15, r_n - 127): weights scale by
+// 2^(s - c_n) in bf16 (the bit move left a factor 2^-112, so the product is
+// the weight times 2^(15 - c_n)), at most 2^127 for every scale byte, and the
+// epilogue multiplies by 2^(c_n - 15) (1 unless r_n > 142).
+__device__ __forceinline__ int bf16_row_offset(int rn) { return max(15, rn - 127); }
+
 template <>
 struct Dequant<Mode::Down> {
-  // 2^(s - 15) in bf16 (the bit move left a factor 2^-112); r_n unused.
-  __device__ __forceinline__ static uint32_t factor(int s, int) { return bf16x2_pow2(min(s - 15, 127)); }
+  __device__ __forceinline__ static uint32_t factor(int s, int rn) {
+    return bf16x2_pow2(s - bf16_row_offset(rn));
+  }
   __device__ __forceinline__ static void convert(uint32_t w, uint32_t f, uint32_t* out) {
     const uint4 v = e2m1x8_to_f16(w);
     out[0] = hmul2_bf16(f16x2_to_bf16x2_scaled(v.x), f);
@@ -357,6 +369,7 @@ moe_expert_gemm_tmem(const __grid_constant__ CUtensorMap map_w,
   uint64_t* mma_done = rf_empty + kRing;
   uint32_t* tmem_base_p = reinterpret_cast<uint32_t*>(smem + L.misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc + 4);
+  uint8_t* comb = smem + L.misc + 16;                // combine lists (down)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -404,7 +417,7 @@ moe_expert_gemm_tmem(const __grid_constant__ CUtensorMap map_w,
 
   if (warp == kWarpProd) {
     // ------------------------------------------- producer: scales and codes --
-    if (ptx::elect_one()) {
+    if (ptx::elect_one() && !(kGateUp && a.inject == 1)) {
       ptx::tma_prefetch_desc(&map_w);
       Ring cr;
       Inflight c_in, s_in;
@@ -414,7 +427,7 @@ moe_expert_gemm_tmem(const __grid_constant__ CUtensorMap map_w,
         const Unit w = unit_of(a, n_mt, u);
         // the unit's scale rows (1-D bulk copies of contiguous rows)
         const int sb = q & 1;
-        if (!wait_phase(&sc_empty[sb], ((q >> 1) & 1) ^ 1, abort_flag, a.status, 64)) { ok = false; break; }
+        if (!wait_phase(&sc_empty[sb], ((q >> 1) & 1) ^ 1, abort_flag, a.status, a.wait_ns, 64)) { ok = false; break; }
         const uint8_t* wscale = kGateUp ? a.w_gu_scale : a.w_dn_scale;
         int row_a, row_b;
         if constexpr (kGateUp) {
@@ -438,7 +451,7 @@ moe_expert_gemm_tmem(const __grid_constant__ CUtensorMap map_w,
         }
         s_in.mark(sb, (q >> 1) & 1);
         for (int cs = 0; cs < nS; ++cs) {
-          if (!wait_phase(&code_empty[cr.slot], cr.phase ^ 1, abort_flag, a.status, 64)) { ok = false; break; }
+          if (!wait_phase(&code_empty[cr.slot], cr.phase ^ 1, abort_flag, a.status, a.wait_ns, 64)) { ok = false; break; }
           uint8_t* cdst = codes + cr.slot * kCodeStageBytes;
           ptx::mbar_arrive_expect_tx(&code_full[cr.slot], kCodeStageBytes);
           ptx::tma_load_2d(cdst, &map_w, &code_full[cr.slot], cs * (kSK / 2), row_a);
@@ -464,7 +477,7 @@ moe_expert_gemm_tmem(const __grid_constant__ CUtensorMap map_w,
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
         const Unit w = unit_of(a, n_mt, u);
         for (int jb = 0; jb < nKB; ++jb) {
-          if (!wait_phase(&b_empty[br.slot], br.phase ^ 1, abort_flag, a.status, 64)) { ok = false; break; }
+          if (!wait_phase(&b_empty[br.slot], br.phase ^ 1, abort_flag, a.status, a.wait_ns, 64)) { ok = false; break; }
           // one box of nb rows x 64 K per sub-tile and operand (rows past the
           // chunk are other experts' tokens or zero fill, and only feed
           // accumulator columns the epilogue ignores); sub-tiles past K are
@@ -499,17 +512,17 @@ moe_expert_gemm_tmem(const __grid_constant__ CUtensorMap map_w,
         const int N = (w.n + 15) & ~15;
         const uint32_t idesc = ptx::idesc_f16(kMW, N, !F16);
         const int buf = q & 1;
-        if (!wait_phase(&acc_empty[buf], ((q >> 1) & 1) ^ 1, abort_flag, a.status)) { ok = false; break; }
+        if (!wait_phase(&acc_empty[buf], ((q >> 1) & 1) ^ 1, abort_flag, a.status, a.wait_ns)) { ok = false; break; }
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + buf * a.nb;
         uint32_t accumulate = 0;
         int jb = 0;                                  // activation stage of the unit
         for (int ja = 0; ja < nS && ok; ++ja) {
-          if (!wait_phase(&a_full[ar.slot], ar.phase, abort_flag, a.status)) { ok = false; break; }
+          if (!wait_phase(&a_full[ar.slot], ar.phase, abort_flag, a.status, a.wait_ns)) { ok = false; break; }
           const uint32_t a_stage = tmem_base + a_col0 + ar.slot * kACols;
           // the activation stages inside this A stage
           for (int kb = ja * kSK; kb < min(K, (ja + 1) * kSK); kb += bk, ++jb) {
-            if (!wait_phase(&b_full[br.slot], br.phase, abort_flag, a.status)) { ok = false; break; }
+            if (!wait_phase(&b_full[br.slot], br.phase, abort_flag, a.status, a.wait_ns)) { ok = false; break; }
             ptx::tc_fence_after();
             const uint32_t bsm = ptx::smem_u32(bt + br.slot * L.bstage);
             const int nk = min(bk, K - kb) / 16;         // K16 steps in this stage
@@ -552,9 +565,11 @@ moe_expert_gemm_tmem(const __grid_constant__ CUtensorMap map_w,
     for (int u = blockIdx.x; u < units; u += gridDim.x, ++q) {
       const Unit w = unit_of(a, n_mt, u);
       const int buf = q & 1, ring = q % kRing;
-      const bool ok = wait_phase(&acc_full[buf], (q >> 1) & 1, abort_flag, a.status, 256) &&
-                      wait_phase(&rf_full[ring], (q / kRing) & 1, abort_flag, a.status);
-      if (!__all_sync(0xffffffffu, ok)) break;   // warp-uniform: tcgen05.ld is .sync.aligned
+      const bool ok = wait_phase(&acc_full[buf], (q >> 1) & 1, abort_flag, a.status, a.wait_ns, 256) &&
+                      wait_phase(&rf_full[ring], (q / kRing) & 1, abort_flag, a.status, a.wait_ns);
+      // the four warps leave together (tcgen05.ld is .sync.aligned, and down's
+      // combine synchronises all 128 threads)
+      if (!ptx::group_all(1, 128, ok)) break;
       ptx::tc_fence_after();
       const float rowf = rf[ring * kMW + Ln];
       __syncwarp();
@@ -575,7 +590,10 @@ moe_expert_gemm_tmem(const __grid_constant__ CUtensorMap map_w,
           for (int j = 0; j < 16; ++j) {
             const int col = c + j;
             const float colf = col < w.n ? __int_as_float((127 - __ldg(a.rowexp + w.r0 + col)) << 23) : 0.f;
-            z[j] = __uint_as_float(v[j]) * rowf * colf + bias;
+            // the token's factor first: (acc 2^-e_t) is the dot product with
+            // the row's weights scaled to its largest block, whose scale
+            // 2^(r_n - 127) then overflows only if the true value does
+            z[j] = (__uint_as_float(v[j]) * colf) * rowf + bias;
           }
           // gate lanes are even, up lanes odd: the even lane finishes tokens
           // c..c+7, the odd lane tokens c+8..c+15
@@ -622,6 +640,10 @@ moe_expert_gemm_tmem(const __grid_constant__ CUtensorMap map_w,
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&acc_empty[buf]);
+      // K5: the weighted sum of each token whose k rows are now all stored
+      // (after the accumulator is released, so the next unit's MMAs run meanwhile)
+      if constexpr (!kGateUp)
+        combine_tile<2>(a, w.r0, w.n, w.mt, Ln, comb, kNBMax, 2);
     }
   } else if (warp >= kWarpDq0) {
     // --------------------------------------------------------- dequantisers --
@@ -642,22 +664,23 @@ moe_expert_gemm_tmem(const __grid_constant__ CUtensorMap map_w,
       const Unit w = unit_of(a, n_mt, u);
       const bool valid = kGateUp ? (w.mt * (kMW / 2) + (Ln >> 1) < a.W) : (w.mt * kMW + Ln < a.d);
       const int sb = q & 1, ring = q % kRing;
-      ok = __all_sync(0xffffffffu, wait_phase(&sc_full[sb], (q >> 1) & 1, abort_flag, a.status));
+      ok = __all_sync(0xffffffffu, wait_phase(&sc_full[sb], (q >> 1) & 1, abort_flag, a.status, a.wait_ns));
       if (!ok) break;
       const uint8_t* srow = scb + sb * L.scbuf + sr * nsb;
-      int rn = 0;
-      if (F16 && valid)
+      int rn = 0;                                  // the row's largest scale byte
+      if (valid)
         rn = row_max_byte(reinterpret_cast<const uint32_t*>(scb + sb * L.scbuf), uint32_t(sr * nsb), nsb);
       const uint32_t rnb = uint32_t(rn) * 0x0101u;   // r_n in the two low bytes
       if (part == 0) {
-        ok = __all_sync(0xffffffffu, wait_phase(&rf_empty[ring], ((q / kRing) & 1) ^ 1, abort_flag, a.status));
+        ok = __all_sync(0xffffffffu, wait_phase(&rf_empty[ring], ((q / kRing) & 1) ^ 1, abort_flag, a.status, a.wait_ns));
         if (!ok) break;
-        rf[ring * kMW + Ln] = valid ? (F16 ? ldexpf(1.0f, rn - 127) : 1.0f) : 0.f;
+        rf[ring * kMW + Ln] =
+            valid ? (F16 ? ldexpf(1.0f, rn - 127) : ldexpf(1.0f, bf16_row_offset(rn) - 15)) : 0.f;
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&rf_full[ring]);
       }
       for (int cs = 0; cs < nS; ++cs) {
-        ok = __all_sync(0xffffffffu, wait_phase(&code_full[cr.slot], cr.phase, abort_flag, a.status, 32));
+        ok = __all_sync(0xffffffffu, wait_phase(&code_full[cr.slot], cr.phase, abort_flag, a.status, a.wait_ns, 32));
         if (!ok) break;
         const uint8_t* cst = codes + cr.slot * kCodeStageBytes;
         // this thread's 2 scale blocks: one 16-bit read when the row starts at
@@ -672,10 +695,11 @@ moe_expert_gemm_tmem(const __grid_constant__ CUtensorMap map_w,
         }
         uint32_t f0, f1;
         if (F16) {
-          // 2^(s - r_n) as f16x2 for both blocks at once: byte-wise s + 15 - r_n
-          // (s <= r_n; at most 15; 0 below the f16 normal range, where the
+          // 2^(s - r_n) as f16x2 for both blocks at once: byte-wise
+          // 15 - (r_n - s) (s <= r_n, so neither subtraction wraps for any
+          // scale byte; clamped at 0 below the f16 normal range, where the
           // factor becomes 0), moved into both halves' exponent fields
-          const uint32_t e2 = __vsubus4(__vaddus4(s01, 0x0F0Fu), rnb) & 0x1F1Fu;
+          const uint32_t e2 = __vsubus4(0x0F0Fu, __vsubus4(rnb, s01)) & 0x1F1Fu;
           f0 = (__byte_perm(e2, 0, 0x4040) << 10);
           f1 = (__byte_perm(e2, 0, 0x4141) << 10);
           if (!(valid && b0 < nsb)) f0 = 0u;
@@ -700,7 +724,7 @@ moe_expert_gemm_tmem(const __grid_constant__ CUtensorMap map_w,
         Dequant<DQ>::convert(x1.y, f1, &r[20]);
         Dequant<DQ>::convert(x1.z, f1, &r[24]);
         Dequant<DQ>::convert(x1.w, f1, &r[28]);
-        ok = __all_sync(0xffffffffu, wait_phase(&a_empty[ar.slot], ar.phase ^ 1, abort_flag, a.status, 32));
+        ok = __all_sync(0xffffffffu, wait_phase(&a_empty[ar.slot], ar.phase ^ 1, abort_flag, a.status, a.wait_ns, 32));
         if (!ok) break;
         ptx::tmem_st_32x32b_x32(tmem_base + lane_addr + a_col0 + ar.slot * kACols + part * 32, r);
         ptx::tmem_st_wait();
@@ -755,17 +779,6 @@ cudaError_t make_map(CUtensorMap* map, CUtensorMapDataType dt, int esize, const 
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-int num_sms() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 148;
-  }
-  return n;
-}
-
 // Ring depths for one launch.  The weight codes stream from HBM, whose
 // latency under load is several microseconds, so after a modest activation
 // ring (the activations are L2-resident) every remaining byte of shared memory
@@ -804,12 +817,9 @@ cudaError_t launch(const GemmArgs& args, cudaStream_t s) {
   if (a.stages_b < 2 || a.stages_c < 2 || smem > size_t(kMaxSmem) || a.nb < 16 || a.nb > kNBMax ||
       a.nb % 16 || a_stages(a.nb) < 2)
     return cudaErrorInvalidConfiguration;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(moe_expert_gemm_tmem<M, F16>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
+  {
+    cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(moe_expert_gemm_tmem<M, F16>), kMaxSmem);
     if (e != cudaSuccess) return e;
-    configured = true;
   }
   // the three maps, from the cache when this layer's buffers were seen before
   struct Key {
@@ -858,7 +868,7 @@ cudaError_t launch(const GemmArgs& args, cudaStream_t s) {
   const int rows_per_tile = (M == Mode::GateUp) ? kMW / 2 : kMW;
   const long long n_mt = (n_out + rows_per_tile - 1) / rows_per_tile;
   const long long units_bound = (long long)(a.R / a.nb + a.E) * n_mt;
-  const int grid = int(units_bound < num_sms() ? units_bound : num_sms());
+  const int grid = int(units_bound < device_sm_count() ? units_bound : device_sm_count());
   return launch_pdl(moe_expert_gemm_tmem<M, F16>, dim3(grid), dim3(kThreads), smem, s, mw, m0, m1, a);
 }
 

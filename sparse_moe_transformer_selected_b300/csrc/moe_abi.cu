@@ -1,19 +1,28 @@
 // C ABI of libmoe_b300 (declared in include/moe.h): argument checking, the
-// workspace layout and the launch sequence K1 -> K5 on the caller's stream.
+// workspace layout and the launch sequence K1 -> K4 (K5 runs in K4's
+// epilogue) on the caller's stream.
 #include "moe.h"
 #include "common.cuh"
 
+#include <math.h>
 #include <stdarg.h>
 #include <stdio.h>
 #include <stdlib.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 #include <string>
+#include <utility>
+#include <vector>
 
 namespace {
 
 thread_local std::string g_last_error;
+// failure detection: the GEMMs' wait limit and the test hook (per thread)
+constexpr long long kDefaultWaitNs = 2000000000ll;
+thread_local long long g_wait_ns = kDefaultWaitNs;
+thread_local int g_inject = 0;
 constexpr int kTraceEvents = 7;
 thread_local cudaEvent_t g_trace[kTraceEvents];
 thread_local bool g_trace_on = false;
@@ -76,22 +85,10 @@ moe_status check_device() {
 //   Mx    block-scaled MMA on the E2M1 codes (expert_gemm_mx.cu): decode-sized
 //         loads (a few rows per expert) with a clamp that bounds h
 //   Tmem  dequantised weights as the MMA's A operand in tensor memory
-//   Smem  dequantised weights staged in shared memory
-// The first that fits is used; MOE_GEMM=tmem or MOE_GEMM=smem skips the ones
-// before it (a diagnostic and tuning knob; all meet the same tolerances).
-enum class Design { Smem, Tmem, Mx };
-
-moe::GemmArgs gemm_args(int64_t T, int d, int W, int E, int k);
-
-Design gemm_design(int64_t T, int d, int W, int E, int k, float limit) {
-  const moe::GemmArgs a = gemm_args(T, d, W, E, k);
-  const char* s = getenv("MOE_GEMM");
-  const bool no_mx = s && (strcmp(s, "tmem") == 0 || strcmp(s, "smem") == 0);
-  const bool no_tmem = s && strcmp(s, "smem") == 0;
-  if (!no_mx && moe::mx_fits(a, limit)) return Design::Mx;
-  if (!no_tmem && moe::expert_gemm_tmem_fits(a)) return Design::Tmem;
-  return Design::Smem;
-}
+//         (expert_gemm_tmem.cu): everything else
+// MOE_GEMM=tmem skips the first (a diagnostic knob; both meet the same
+// tolerances).  None: no design's shared-memory plan fits the shape.
+enum class Design { None, Tmem, Mx };
 
 moe::GemmArgs gemm_args(int64_t T, int d, int W, int E, int k) {
   moe::GemmArgs a{};
@@ -99,8 +96,18 @@ moe::GemmArgs gemm_args(int64_t T, int d, int W, int E, int k) {
   a.d = d;
   a.W = W;
   a.E = E;
+  a.k = k;
   a.nb = moe::kGemmBM;
   return a;
+}
+
+Design gemm_design(int64_t T, int d, int W, int E, int k, float limit) {
+  const moe::GemmArgs a = gemm_args(T, d, W, E, k);
+  const char* s = getenv("MOE_GEMM");
+  const bool no_mx = s && strcmp(s, "tmem") == 0;
+  if (!no_mx && moe::mx_fits(a, limit)) return Design::Mx;
+  if (moe::expert_gemm_tmem_fits(a)) return Design::Tmem;
+  return Design::None;
 }
 
 template <class T>
@@ -108,30 +115,29 @@ T* at(void* base, size_t off) {
   return reinterpret_cast<T*>(static_cast<char*>(base) + off);
 }
 
-struct RouteOut {
-  float* logit_part;
-  int32_t* topk_idx;
-  float* topk_w;
-  int32_t* rank;
-  int32_t* tile_counts;
-  int32_t* tile_base;
-  int32_t* offsets;
-  int32_t* mtile_off;
-  int32_t* perm;
-  int32_t* inv;
-  int32_t* rowexp;
-  void* x_perm;
-  int32_t* status;
-  // block-scaled design: E4M3 pairs and their block scales
-  uint8_t* xq_hi;
-  uint8_t* xq_lo;
-  uint8_t* sx_hi;
-  uint8_t* sx_lo;
-  int ld_sx;
-};
-
-RouteOut route_tables(void* ws, const moe::Workspace& L, bool gather) {
-  RouteOut r;
+// Routing tables inside the workspace, as K1/K2 arguments.
+// norm_w != null: x is the block's residual stream and the routing stages
+// read its normalised copy, written by K1 at the start of the y region.
+moe::RouteArgs route_args(void* ws, const moe::Workspace& L, const void* x, int64_t T, int d,
+                          const float* rw, const float* rb, const float* norm_w, float eps,
+                          int E, int k, int chunk) {
+  moe::RouteArgs r{};
+  r.router_w = rw;
+  r.router_b = rb;
+  r.norm_w = norm_w;
+  r.eps = eps;
+  if (norm_w) {
+    r.x_pre = static_cast<const __nv_bfloat16*>(x);
+    r.xn = at<__nv_bfloat16>(ws, L.y);
+    r.x = r.xn;
+  } else {
+    r.x = static_cast<const __nv_bfloat16*>(x);
+  }
+  r.T = int(T);
+  r.d = d;
+  r.E = E;
+  r.k = k;
+  r.chunk = chunk;
   r.logit_part = at<float>(ws, L.logit_part);
   r.topk_idx = at<int32_t>(ws, L.topk_idx);
   r.topk_w = at<float>(ws, L.topk_w);
@@ -140,44 +146,150 @@ RouteOut route_tables(void* ws, const moe::Workspace& L, bool gather) {
   r.tile_base = at<int32_t>(ws, L.tile_base);
   r.offsets = at<int32_t>(ws, L.offsets);
   r.mtile_off = at<int32_t>(ws, L.mtile_off);
+  r.status = at<int32_t>(ws, L.status);
+  r.rnorm = at<float>(ws, L.rnorm);
+  r.cnt = at<int32_t>(ws, L.cnt);
+  r.ncnt = T * moe::down_col_tiles(d);
   r.perm = at<int32_t>(ws, L.perm);
   r.inv = at<int32_t>(ws, L.inv);
-  r.rowexp = at<int32_t>(ws, L.rowexp);
-  r.x_perm = gather ? at<void>(ws, L.x_perm) : nullptr;
-  r.status = at<int32_t>(ws, L.status);
-  r.xq_hi = nullptr;
-  r.xq_lo = nullptr;
-  r.sx_hi = nullptr;
-  r.sx_lo = nullptr;
-  r.ld_sx = 0;
   return r;
 }
 
-moe_status run_route(const void* x, int64_t T, int d, const float* rw, const float* rb, int E,
-                     int k, int chunk, const RouteOut& r, cudaStream_t s) {
-  const auto* xb = static_cast<const __nv_bfloat16*>(x);
-  const int ntiles = int((T + moe::kRouterTile - 1) / moe::kRouterTile);
+// K1, K2a, K2b on stream s (trace events 1..3 after each stage).  x_perm:
+// the TMEM design's gathered f16 rows (null for the block-scaled design, whose
+// token tables K1 writes).  The scan and the scatter run as kernels of their
+// own only when K1's last top-k CTA did not run them (more than 8 router
+// tiles, or rows to gather).
+moe_status run_route(const moe::RouteArgs& r, int32_t* rowexp, void* x_perm, cudaStream_t s) {
+  const int ntiles = int((r.T + moe::kRouterTile - 1) / moe::kRouterTile);
   bool scanned = false;
-  cudaError_t e = moe::launch_router_topk(xb, rw, rb, int(T), d, E, k, r.logit_part, r.topk_idx,
-                                          r.topk_w, r.rank, r.tile_counts, r.status, chunk,
-                                          r.tile_base, r.offsets, r.mtile_off, &scanned, s);
+  cudaError_t e = moe::launch_router_topk(r, &scanned, s);
   if (e != cudaSuccess) return cuda_fail(e, "router_topk launch");
   if ((e = trace(1, s)) != cudaSuccess) return cuda_fail(e, "trace event");
   if (!scanned) {
-    e = moe::launch_route_scan(r.tile_counts, ntiles, E, chunk, r.tile_base, r.offsets,
+    e = moe::launch_route_scan(r.tile_counts, ntiles, r.E, r.chunk, r.tile_base, r.offsets,
                                r.mtile_off, s);
     if (e != cudaSuccess) return cuda_fail(e, "route_scan launch");
   }
   if ((e = trace(2, s)) != cudaSuccess) return cuda_fail(e, "trace event");
-  if (r.xq_hi) {
-    e = moe::launch_route_scatter_mx(xb, int(T), d, E, k, r.topk_idx, r.rank, r.tile_base, r.perm,
-                                     r.inv, r.xq_hi, r.xq_lo, r.sx_hi, r.sx_lo, r.ld_sx, r.status, s);
-  } else {
-    e = moe::launch_route_scatter(xb, int(T), d, E, k, r.topk_idx, r.rank, r.tile_base, r.perm,
-                                  r.inv, r.x_perm, r.rowexp, r.status, s);
+  if (x_perm || !scanned || !r.perm) {
+    e = moe::launch_route_scatter(r.x, r.T, r.d, r.E, r.k, r.topk_idx, r.rank, r.tile_base,
+                                  r.perm, r.inv, x_perm, rowexp, r.status, s);
+    if (e != cudaSuccess) return cuda_fail(e, "route_scatter launch");
   }
-  if (e != cudaSuccess) return cuda_fail(e, "route_scatter launch");
   if ((e = trace(3, s)) != cudaSuccess) return cuda_fail(e, "trace event");
+  return MOE_OK;
+}
+
+// Checks shared by moe_forward and moe_block_forward.
+moe_status check_forward_args(const void* x_bf16, int64_t T, int d, int W, const float* router_w,
+                              const float* router_b, const uint8_t* w_gu_fp4,
+                              const uint8_t* w_gu_scale, const void* b_gu_bf16,
+                              const uint8_t* w_dn_fp4, const uint8_t* w_dn_scale,
+                              const void* b_dn_bf16, int E, int k, float limit, float alpha,
+                              const void* out_bf16, const void* workspace) {
+  moe_status st = check_shape(T, d, W, E, k);
+  if (st != MOE_OK) return st;
+  const void* ptrs[] = {x_bf16, router_w, router_b, w_gu_fp4, w_gu_scale, b_gu_bf16,
+                        w_dn_fp4, w_dn_scale, b_dn_bf16, out_bf16, workspace};
+  const char* names[] = {"x", "router_w", "router_b", "w_gu", "w_gu_scale", "b_gu",
+                         "w_dn", "w_dn_scale", "b_dn", "out", "workspace"};
+  for (int i = 0; i < 11; ++i) {
+    if (T > 0 && !ptrs[i]) return fail(MOE_ERR_NULL, "%s is NULL", names[i]);
+    if (misaligned(ptrs[i])) return fail(MOE_ERR_ALIGN, "%s is not 16-byte aligned", names[i]);
+  }
+  if (alpha != alpha || limit != limit) return fail(MOE_ERR_SHAPE, "limit/alpha is NaN");
+  return MOE_OK;
+}
+
+// The whole block (arguments already checked, T > 0).  norm_w == null: x is
+// the MoE input (moe_forward); otherwise x is the residual stream, the MoE
+// reads RMSNorm(x) and out = x + MoE (moe_block_forward).
+moe_status forward_impl(const void* x_bf16, int64_t T, int d, int W, const float* norm_w,
+                        float eps, const float* router_w, const float* router_b,
+                        const uint8_t* w_gu_fp4, const uint8_t* w_gu_scale, const void* b_gu_bf16,
+                        const uint8_t* w_dn_fp4, const uint8_t* w_dn_scale, const void* b_dn_bf16,
+                        int E, int k, float limit, float alpha, void* out_bf16, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+  const moe::Workspace L = moe::workspace_layout(T, d, W, E, k);
+  if (workspace_bytes < L.total)
+    return fail(MOE_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", workspace_bytes, L.total);
+  moe_status st = check_device();
+  if (st != MOE_OK) return st;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  moe::GemmArgs a = gemm_args(T, d, W, E, k);
+  Design design = gemm_design(T, d, W, E, k, limit);
+  // the block-scaled path reads the weights with 4-bit TMA maps, whose base
+  // addresses want 32-byte alignment (the tail map starts inside a row)
+  if (design == Design::Mx &&
+      ((reinterpret_cast<uintptr_t>(w_gu_fp4) | reinterpret_cast<uintptr_t>(w_dn_fp4)) & 31u))
+    design = moe::expert_gemm_tmem_fits(a) ? Design::Tmem : Design::None;
+  if (design == Design::None)
+    return fail(MOE_ERR_UNSUPPORTED, "no grouped-GEMM design fits d = %d, W = %d", d, W);
+  const bool mx = design == Design::Mx;
+  a.nb = mx ? moe::mx_chunk(a.R, E) : moe::expert_gemm_tmem_chunk(a.R, E);
+  moe::RouteArgs r = route_args(workspace, L, x_bf16, T, d, router_w, router_b, norm_w, eps, E,
+                                k, a.nb);
+  int32_t* rowexp = at<int32_t>(workspace, L.rowexp);
+  void* x_perm = nullptr;
+  if (mx) {                                    // token tables of the E4M3 terms
+    r.xq_hi = at<uint8_t>(workspace, L.x_perm);
+    r.xq_lo = at<uint8_t>(workspace, L.x_perm + size_t(T) * d);
+    r.sx_hi = at<uint8_t>(workspace, L.sx_hi);
+    r.sx_lo = at<uint8_t>(workspace, L.sx_lo);
+    r.ld_sx = moe::scale_row_bytes(d);
+  } else {
+    x_perm = at<void>(workspace, L.x_perm);
+  }
+  cudaError_t e = trace(0, s);
+  if (e != cudaSuccess) return cuda_fail(e, "trace event");
+  st = run_route(r, rowexp, x_perm, s);
+  if (st != MOE_OK) return st;
+
+  a.offsets = r.offsets;
+  a.mtile_off = r.mtile_off;
+  a.x_perm = x_perm;
+  a.rowexp = rowexp;
+  a.w_gu = w_gu_fp4;
+  a.w_gu_scale = w_gu_scale;
+  a.b_gu = static_cast<const __nv_bfloat16*>(b_gu_bf16);
+  a.w_dn = w_dn_fp4;
+  a.w_dn_scale = w_dn_scale;
+  a.b_dn = static_cast<const __nv_bfloat16*>(b_dn_bf16);
+  a.limit = limit;
+  a.alpha = alpha;
+  a.h_f16 = !mx && moe::hidden_fits_f16(limit) ? 1 : 0;
+  a.h_hi = at<__nv_bfloat16>(workspace, L.h_hi);
+  a.h_lo = at<__nv_bfloat16>(workspace, L.h_lo);
+  a.y = at<float>(workspace, L.y);
+  a.status = r.status;
+  a.perm = r.perm;
+  a.inv = r.inv;
+  a.topk_w = r.topk_w;
+  a.cnt = r.cnt;
+  a.n_mt_dn = moe::down_col_tiles(d);
+  a.out = static_cast<__nv_bfloat16*>(out_bf16);
+  a.resid = norm_w ? static_cast<const __nv_bfloat16*>(x_bf16) : nullptr;
+  a.wait_ns = g_wait_ns;
+  a.inject = g_inject;
+  if (mx) {
+    a.xq_hi = r.xq_hi;
+    a.xq_lo = r.xq_lo;
+    a.sx_hi = r.sx_hi;
+    a.sx_lo = r.sx_lo;
+    a.ld_sx = r.ld_sx;
+    a.hq = at<uint8_t>(workspace, L.h_hi);
+    a.h_exp = moe::mx_hidden_exp(limit);
+  }
+  e = mx ? moe::launch_gateup_mx(a, s) : moe::launch_gateup_tmem(a, s);
+  if (e != cudaSuccess) return cuda_fail(e, "gate_up launch");
+  if ((e = trace(4, s)) != cudaSuccess) return cuda_fail(e, "trace event");
+  // K4 with K5 in its epilogue
+  e = mx ? moe::launch_down_mx(a, s) : moe::launch_down_tmem(a, s);
+  if (e != cudaSuccess) return cuda_fail(e, "down launch");
+  if ((e = trace(5, s)) != cudaSuccess) return cuda_fail(e, "trace event");
+  if ((e = trace(6, s)) != cudaSuccess) return cuda_fail(e, "trace event");
   return MOE_OK;
 }
 
@@ -186,6 +298,33 @@ moe_status run_route(const void* x, int64_t T, int d, const float* rw, const flo
 namespace moe {
 // Lets other translation units of the library report through moe_last_error().
 void set_last_error(const std::string& msg) { g_last_error = msg; }
+
+cudaError_t set_smem_limit_once(const void* kernel, int bytes) {
+  static std::mutex mu;
+  static std::vector<std::pair<const void*, int>> done;   // (kernel, device)
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  for (const auto& kd : done)
+    if (kd.first == kernel && kd.second == dev) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.emplace_back(kernel, dev);
+  return e;
+}
+
+int device_sm_count() {
+  static std::atomic<int> count[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  int n = count[dev].load(std::memory_order_relaxed);
+  if (n <= 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    count[dev].store(n, std::memory_order_relaxed);
+  }
+  return n;
+}
 }  // namespace moe
 
 extern "C" {
@@ -223,86 +362,33 @@ moe_status moe_forward(const void* x_bf16, int64_t T, int d, int W, const float*
                        const void* b_gu_bf16, const uint8_t* w_dn_fp4, const uint8_t* w_dn_scale,
                        const void* b_dn_bf16, int E, int k, float limit, float alpha,
                        void* out_bf16, void* workspace, size_t workspace_bytes, void* stream) {
-  moe_status st = check_shape(T, d, W, E, k);
+  moe_status st = check_forward_args(x_bf16, T, d, W, router_w, router_b, w_gu_fp4, w_gu_scale,
+                                     b_gu_bf16, w_dn_fp4, w_dn_scale, b_dn_bf16, E, k, limit,
+                                     alpha, out_bf16, workspace);
+  if (st != MOE_OK || T == 0) return st;
+  return forward_impl(x_bf16, T, d, W, nullptr, 0.f, router_w, router_b, w_gu_fp4, w_gu_scale,
+                      b_gu_bf16, w_dn_fp4, w_dn_scale, b_dn_bf16, E, k, limit, alpha, out_bf16,
+                      workspace, workspace_bytes, stream);
+}
+
+moe_status moe_block_forward(const void* x_bf16, int64_t T, int d, int W, const float* norm_w,
+                             float eps, const float* router_w, const float* router_b,
+                             const uint8_t* w_gu_fp4, const uint8_t* w_gu_scale,
+                             const void* b_gu_bf16, const uint8_t* w_dn_fp4,
+                             const uint8_t* w_dn_scale, const void* b_dn_bf16, int E, int k,
+                             float limit, float alpha, void* out_bf16, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  moe_status st = check_forward_args(x_bf16, T, d, W, router_w, router_b, w_gu_fp4, w_gu_scale,
+                                     b_gu_bf16, w_dn_fp4, w_dn_scale, b_dn_bf16, E, k, limit,
+                                     alpha, out_bf16, workspace);
   if (st != MOE_OK) return st;
-  const void* ptrs[] = {x_bf16, router_w, router_b, w_gu_fp4, w_gu_scale, b_gu_bf16,
-                        w_dn_fp4, w_dn_scale, b_dn_bf16, out_bf16, workspace};
-  const char* names[] = {"x", "router_w", "router_b", "w_gu", "w_gu_scale", "b_gu",
-                         "w_dn", "w_dn_scale", "b_dn", "out", "workspace"};
-  for (int i = 0; i < 11; ++i) {
-    if (T > 0 && !ptrs[i]) return fail(MOE_ERR_NULL, "%s is NULL", names[i]);
-    if (misaligned(ptrs[i])) return fail(MOE_ERR_ALIGN, "%s is not 16-byte aligned", names[i]);
-  }
-  if (alpha != alpha || limit != limit) return fail(MOE_ERR_SHAPE, "limit/alpha is NaN");
+  if (T > 0 && !norm_w) return fail(MOE_ERR_NULL, "norm_w is NULL");
+  if (misaligned(norm_w)) return fail(MOE_ERR_ALIGN, "norm_w is not 16-byte aligned");
+  if (!(eps >= 0.f) || !std::isfinite(eps)) return fail(MOE_ERR_SHAPE, "eps must be finite and >= 0");
   if (T == 0) return MOE_OK;
-  const moe::Workspace L = moe::workspace_layout(T, d, W, E, k);
-  if (workspace_bytes < L.total)
-    return fail(MOE_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", workspace_bytes, L.total);
-  st = check_device();
-  if (st != MOE_OK) return st;
-
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  RouteOut r = route_tables(workspace, L, true);
-  moe::GemmArgs a = gemm_args(T, d, W, E, k);
-  Design design = gemm_design(T, d, W, E, k, limit);
-  // the block-scaled path reads the weights with 4-bit TMA maps, whose base
-  // addresses want 32-byte alignment (the tail map starts inside a row)
-  if (design == Design::Mx &&
-      ((reinterpret_cast<uintptr_t>(w_gu_fp4) | reinterpret_cast<uintptr_t>(w_dn_fp4)) & 31u))
-    design = moe::expert_gemm_tmem_fits(a) ? Design::Tmem : Design::Smem;
-  const bool tmem = design == Design::Tmem;
-  const bool mx = design == Design::Mx;
-  if (tmem) a.nb = moe::expert_gemm_tmem_chunk(a.R, E);
-  if (mx) {
-    a.nb = moe::mx_chunk(a.R, E);
-    r.xq_hi = at<uint8_t>(workspace, L.x_perm);
-    r.xq_lo = at<uint8_t>(workspace, L.x_perm + size_t(a.R) * d);
-    r.sx_hi = at<uint8_t>(workspace, L.sx_hi);
-    r.sx_lo = at<uint8_t>(workspace, L.sx_lo);
-    r.ld_sx = moe::scale_row_bytes(d);
-  }
-  cudaError_t e = trace(0, s);
-  if (e != cudaSuccess) return cuda_fail(e, "trace event");
-  st = run_route(x_bf16, T, d, router_w, router_b, E, k, a.nb, r, s);
-  if (st != MOE_OK) return st;
-
-  a.offsets = r.offsets;
-  a.mtile_off = r.mtile_off;
-  a.x_perm = r.x_perm;
-  a.rowexp = r.rowexp;
-  a.w_gu = w_gu_fp4;
-  a.w_gu_scale = w_gu_scale;
-  a.b_gu = static_cast<const __nv_bfloat16*>(b_gu_bf16);
-  a.w_dn = w_dn_fp4;
-  a.w_dn_scale = w_dn_scale;
-  a.b_dn = static_cast<const __nv_bfloat16*>(b_dn_bf16);
-  a.limit = limit;
-  a.alpha = alpha;
-  a.h_f16 = tmem && moe::hidden_fits_f16(limit) ? 1 : 0;
-  a.h_hi = at<__nv_bfloat16>(workspace, L.h_hi);
-  a.h_lo = at<__nv_bfloat16>(workspace, L.h_lo);
-  a.y = at<float>(workspace, L.y);
-  a.status = r.status;
-  if (mx) {
-    a.xq_hi = r.xq_hi;
-    a.xq_lo = r.xq_lo;
-    a.sx_hi = r.sx_hi;
-    a.sx_lo = r.sx_lo;
-    a.ld_sx = r.ld_sx;
-    a.hq = at<uint8_t>(workspace, L.h_hi);
-    a.h_exp = moe::mx_hidden_exp(limit);
-  }
-  e = mx ? moe::launch_gateup_mx(a, s) : tmem ? moe::launch_gateup_tmem(a, s) : moe::launch_gateup(a, s);
-  if (e != cudaSuccess) return cuda_fail(e, "gate_up launch");
-  if ((e = trace(4, s)) != cudaSuccess) return cuda_fail(e, "trace event");
-  e = mx ? moe::launch_down_mx(a, s) : tmem ? moe::launch_down_tmem(a, s) : moe::launch_down(a, s);
-  if (e != cudaSuccess) return cuda_fail(e, "down launch");
-  if ((e = trace(5, s)) != cudaSuccess) return cuda_fail(e, "trace event");
-  e = moe::launch_combine(a.y, r.topk_w, r.inv, int(T), d, k,
-                          static_cast<__nv_bfloat16*>(out_bf16), r.status, s);
-  if (e != cudaSuccess) return cuda_fail(e, "combine launch");
-  if ((e = trace(6, s)) != cudaSuccess) return cuda_fail(e, "trace event");
-  return MOE_OK;
+  return forward_impl(x_bf16, T, d, W, norm_w, eps, router_w, router_b, w_gu_fp4, w_gu_scale,
+                      b_gu_bf16, w_dn_fp4, w_dn_scale, b_dn_bf16, E, k, limit, alpha, out_bf16,
+                      workspace, workspace_bytes, stream);
 }
 
 moe_status moe_route(const void* x_bf16, int64_t T, int d, const float* router_w,
@@ -327,8 +413,10 @@ moe_status moe_route(const void* x_bf16, int64_t T, int d, const float* router_w
   st = check_device();
   if (st != MOE_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const RouteOut r = route_tables(workspace, L, false);
-  st = run_route(x_bf16, T, d, router_w, router_b, E, k, moe::kGemmBM, r, s);
+  moe::RouteArgs r = route_args(workspace, L, x_bf16, T, d, router_w, router_b, nullptr, 0.f, E,
+                                k, moe::kGemmBM);
+  r.ncnt = 0;                                  // no combine follows
+  st = run_route(r, nullptr, nullptr, s);
   if (st != MOE_OK) return st;
   const size_t R = size_t(T) * k;
   struct { void* dst; const void* src; size_t n; } copies[] = {
@@ -363,7 +451,7 @@ moe_status moe_hidden_format(int64_t T, int d, int W, int E, int k, float limit,
   moe_status st = check_shape(T, d, W, E, k);
   if (st != MOE_OK) return st;
   if (!format) return fail(MOE_ERR_NULL, "format is NULL");
-  const Design design = T > 0 ? gemm_design(T, d, W, E, k, limit) : Design::Smem;
+  const Design design = T > 0 ? gemm_design(T, d, W, E, k, limit) : Design::Tmem;
   int f = MOE_HIDDEN_BF16_PAIR, x = 0;
   if (design == Design::Mx) {
     f = MOE_HIDDEN_E4M3_TERMS;
@@ -373,6 +461,23 @@ moe_status moe_hidden_format(int64_t T, int d, int W, int E, int k, float limit,
   }
   *format = f;
   if (exponent) *exponent = x;
+  return MOE_OK;
+}
+
+moe_status moe_set_wait_limit(double seconds) {
+  if (seconds == 0.0) {
+    g_wait_ns = kDefaultWaitNs;
+    return MOE_OK;
+  }
+  if (!(seconds >= 1e-4 && seconds <= 60.0))
+    return fail(MOE_ERR_SHAPE, "wait limit %g s outside [1e-4, 60] (0 restores 2 s)", seconds);
+  g_wait_ns = (long long)(seconds * 1e9);
+  return MOE_OK;
+}
+
+moe_status moe_set_fault_injection(int mode) {
+  if (mode < 0 || mode > 1) return fail(MOE_ERR_SHAPE, "unknown fault-injection mode %d", mode);
+  g_inject = mode;
   return MOE_OK;
 }
 

@@ -46,7 +46,10 @@ DevicePtrs& device_ptrs() {
 }
 
 // Device address of the scratch on the current device, looked up once per
-// device (the first call on a device does this set-up).
+// device (the first call on a device does this set-up).  The cached address
+// belongs to the device's current context: after cudaDeviceReset the module is
+// loaded again and the array may move, so this library must not be used
+// across a reset of a device it has already run on.
 moe_status scratch_address(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -84,7 +87,13 @@ moe_status moe_forward_noalloc(const void* x_bf16, int64_t T, int d, int W,
                                const void* b_gu_bf16, const uint8_t* w_dn_fp4,
                                const uint8_t* w_dn_scale, const void* b_dn_bf16, int E, int k,
                                float limit, float alpha, void* out_bf16, void* stream) {
-  if (T == 0) return MOE_OK;
+  if (T == 0) {
+    // nothing to run, but the arguments get moe_forward's checks (shape,
+    // alignment, NaN clamp); no scratch is needed for them
+    return moe_forward(x_bf16, T, d, W, router_w, router_b, w_gu_fp4, w_gu_scale, b_gu_bf16,
+                       w_dn_fp4, w_dn_scale, b_dn_bf16, E, k, limit, alpha, out_bf16, nullptr, 0,
+                       stream);
+  }
   const size_t need = moe_workspace_bytes(T, d, W, E, k);
   if (need == 0) return MOE_ERR_SHAPE;   // invalid shape; moe_last_error() says which
   if (need > kScratchBytes) {
@@ -101,6 +110,14 @@ moe_status moe_forward_noalloc(const void* x_bf16, int64_t T, int d, int W,
   return moe_forward(x_bf16, T, d, W, router_w, router_b, w_gu_fp4, w_gu_scale, b_gu_bf16,
                      w_dn_fp4, w_dn_scale, b_dn_bf16, E, k, limit, alpha, out_bf16, scratch,
                      kScratchBytes, stream);
+}
+
+moe_status moe_poll_status_noalloc(void* stream) {
+  void* scratch = nullptr;
+  const moe_status st = scratch_address(&scratch);
+  if (st != MOE_OK) return st;
+  // the status word is the first word of the scratch, as of any workspace
+  return moe_poll_status(scratch, stream);
 }
 
 }  // extern "C"

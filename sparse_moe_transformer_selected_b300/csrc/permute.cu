@@ -11,7 +11,6 @@
 #include "route_scan.cuh"
 
 #include <cuda_fp16.h>
-#include <cuda_fp8.h>
 #include <math.h>
 
 namespace moe {
@@ -123,119 +122,7 @@ route_scatter_kernel(const __nv_bfloat16* __restrict__ x, int T, int d, int E, i
   }
 }
 
-// E4M3 (round to nearest even, saturating) of v, and its value.
-__device__ __forceinline__ uint32_t to_e4m3(float v) {
-  return uint32_t(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
-}
-__device__ __forceinline__ float from_e4m3(uint32_t b) {
-  return __half2float(__half(__nv_cvt_fp8_to_halfraw(__nv_fp8_storage_t(b), __NV_E4M3)));
-}
-
-// Block-scaled variant: four warps per routed row (t, j), each over a quarter
-// of the row's 32-element blocks (a decode step has few rows, so a row per
-// warp would leave most of the GPU idle); the first writes perm / inv.  x[t]
-// goes out as two E4M3 tables with one UE8M0 scale per 32-element block
-// (the OCP MX block of 32 elements sharing a power-of-two scale, the format the
-// pages give the weights).  For block b with largest |x| = m_b > 0,
-// e_b = floor(log2 m_b) - 7, so x 2^-e_b has magnitude below 256 (E4M3 holds
-// up to 448); hi = E4M3(x 2^-e_b), lo = E4M3((x 2^-e_b - hi) 16), and
-// x = (hi + lo / 16) 2^e_b up to the rounding of lo: about 8 significant
-// bits, the precision of bf16.  The scale bytes are 127 + e_b (hi) and
-// 123 + e_b (lo).
-__global__ void __launch_bounds__(256)
-route_scatter_mx_kernel(const __nv_bfloat16* __restrict__ x, int T, int d, int E, int k,
-                        const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ rank,
-                        const int32_t* __restrict__ tile_base, int32_t* __restrict__ perm,
-                        int32_t* __restrict__ inv, uint8_t* __restrict__ xq_hi,
-                        uint8_t* __restrict__ xq_lo, uint8_t* __restrict__ sx_hi,
-                        uint8_t* __restrict__ sx_lo, int ld_sx, int32_t* __restrict__ status) {
-  const int64_t R = (int64_t)T * k;
-  const int64_t gw = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  const int64_t q = gw >> 2;             // routed row (t, j)
-  const int part = int(gw & 3);          // quarter of the row's blocks
-  const int lane = threadIdx.x & 31;
-  pdl_wait();
-  if (q >= R) return;
-  const int t = (int)(q / k);
-  const int e = topk_idx[q];
-  if (e < 0 || e >= E) {
-    if (lane == 0 && part == 0) atomicMax(status, kStatusBounds);
-    return;
-  }
-  const int64_t row = (int64_t)tile_base[(size_t)(t / kRouterTile) * E + e] + rank[q];
-  if (row < 0 || row >= R) {
-    if (lane == 0 && part == 0) atomicMax(status, kStatusBounds);
-    return;
-  }
-  if (lane == 0 && part == 0) {
-    perm[row] = (int32_t)q;
-    inv[q] = (int32_t)row;
-  }
-  const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * d);
-  uint2* dhi = reinterpret_cast<uint2*>(xq_hi + (size_t)row * d);
-  uint2* dlo = reinterpret_cast<uint2*>(xq_lo + (size_t)row * d);
-  const int nblk = d / 32;               // 32-element blocks; 4 lanes (8 elements each) make one
-  const int b0 = part * nblk / 4, b1 = (part + 1) * nblk / 4;
-  const int p_end = 4 * b1;              // this warp's 8-element pieces: [4 b0, 4 b1)
-  for (int i0 = 4 * b0; i0 < p_end; i0 += 32 * 4) {
-    uint4 v[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int i = i0 + lane + 32 * j;
-      v[j] = i < p_end ? src[i] : make_uint4(0, 0, 0, 0);
-    }
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int i = i0 + lane + 32 * j;
-      const uint32_t in[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-      float f[8];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        f[2 * c] = __uint_as_float(in[c] << 16);
-        f[2 * c + 1] = __uint_as_float(in[c] & 0xFFFF0000u);
-      }
-      float m = 0.f;
-#pragma unroll
-      for (int c = 0; c < 8; ++c) m = fmaxf(m, fabsf(f[c]));
-      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-      const int eb = (m > 0.f && isfinite(m)) ? max(-120, min(120, ilogbf(m) - 7)) : 0;
-      const float sc = __int_as_float((127 - eb) << 23);        // 2^-e_b
-      uint32_t h0 = 0, h1 = 0, l0 = 0, l1 = 0;
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const float v2 = f[c] * sc;
-        const uint32_t hb = to_e4m3(v2);
-        const uint32_t lb = to_e4m3((v2 - from_e4m3(hb)) * 16.f);
-        if (c < 4) { h0 |= hb << (8 * c); l0 |= lb << (8 * c); }
-        else { h1 |= hb << (8 * (c - 4)); l1 |= lb << (8 * (c - 4)); }
-      }
-      if (i < p_end) {
-        dhi[i] = make_uint2(h0, h1);
-        dlo[i] = make_uint2(l0, l1);
-        if ((lane & 3) == 0) {
-          sx_hi[(size_t)row * ld_sx + i / 4] = uint8_t(127 + eb);
-          sx_lo[(size_t)row * ld_sx + i / 4] = uint8_t(123 + eb);
-        }
-      }
-    }
-  }
-}
-
 }  // namespace
-
-cudaError_t launch_route_scatter_mx(const __nv_bfloat16* x, int T, int d, int E, int k,
-                                    const int32_t* topk_idx, const int32_t* rank,
-                                    const int32_t* tile_base, int32_t* perm, int32_t* inv,
-                                    uint8_t* xq_hi, uint8_t* xq_lo, uint8_t* sx_hi,
-                                    uint8_t* sx_lo, int ld_sx, int32_t* status, cudaStream_t s) {
-  const int64_t R = (int64_t)T * k;
-  const int warps_per_block = 8;
-  const int64_t grid = (4 * R + warps_per_block - 1) / warps_per_block;   // 4 warps per row
-  return launch_pdl(route_scatter_mx_kernel, dim3((unsigned)grid), dim3(warps_per_block * 32), 0,
-                    s, x, T, d, E, k, topk_idx, rank, tile_base, perm, inv, xq_hi, xq_lo, sx_hi,
-                    sx_lo, ld_sx, status);
-}
 
 cudaError_t launch_route_scan(const int32_t* tile_counts, int ntiles, int E, int chunk,
                               int32_t* tile_base, int32_t* offsets, int32_t* mtile_off,

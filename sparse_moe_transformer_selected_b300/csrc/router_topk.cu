@@ -14,7 +14,15 @@
 // tokens in a fixed order, adds the bias, and selects.  The router is 2·T·d·E
 // flops, well under 1% of the block; fp32 keeps the selection faithful to the
 // exact logits except at true near-ties.
+//
+// The pre-norm block ("【LLM】GPT-OSS架构变化详解" 2.7.1: RMSNorm divides by the
+// root mean square, with no mean and no bias) feeds the MoE the bf16 values of
+// x / sqrt(mean(x²) + eps) · g.  At decode sizes the logits kernel computes
+// them on the fly (1/rms in fp64, then rms_scaled_bf16) and its first expert
+// group writes them out for the later stages; larger batches run
+// rms_norm_kernel first and route on its table.
 #include "common.cuh"
+#include "quantize.cuh"
 #include "route_scan.cuh"
 
 #include <math.h>
@@ -28,14 +36,29 @@ constexpr int kTT = kRouterTile;         // tokens per CTA (32)
 constexpr int kMaxE = 256;
 constexpr int kLgStride = kMaxE + 8;     // floats per row of the logits / W tile
 
+// The first kernel of a call clears the status word and the combine counts
+// (grid-stride over all CTAs of the launch).
+__device__ __forceinline__ void clear_call_state(const RouteArgs& r) {
+  const int64_t cta = (int64_t(blockIdx.z) * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
+  const int64_t nthr = int64_t(gridDim.x) * gridDim.y * gridDim.z * blockDim.x;
+  if (cta == 0 && threadIdx.x == 0) {
+    r.status[0] = 0;                             // first kernel of a call
+    r.status[1] = 0;                             // top-k tiles done (fused scan)
+    r.status[4] = 0;                             // which wait of a GEMM timed out, if one did
+  }
+  for (int64_t i = cta * blockDim.x + threadIdx.x; i < r.ncnt; i += nthr) r.cnt[i] = 0;
+}
+
 template <int NPER>   // experts per lane: e = lane + 32*i, i < NPER
 __global__ void __launch_bounds__(kThreads)
-router_logits_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__ rw, int T,
-                     int d, int E, int kc, int eg, float* __restrict__ part,
-                     int32_t* __restrict__ status) {
+router_logits_kernel(const RouteArgs r, int kc, int eg) {
   __shared__ float xs[kTT][kKC + 1];
   __shared__ float wl[kKC * kLgStride];  // W chunk [k][e]
 
+  const __nv_bfloat16* __restrict__ x = r.x;
+  const float* __restrict__ rw = r.router_w;
+  const int T = r.T, d = r.d, E = r.E;
+  float* __restrict__ part = r.logit_part;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int t0 = blockIdx.x * kTT;
   const int ks = blockIdx.y;
@@ -43,11 +66,7 @@ router_logits_kernel(const __nv_bfloat16* __restrict__ x, const float* __restric
   const int e0 = blockIdx.z * eg;                // this CTA's experts: e0 .. e0+eg-1
   const int ne = min(eg, E - e0);
   pdl_wait();
-  if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && tid == 0) {
-    status[0] = 0;                               // first kernel of a call
-    status[1] = 0;                               // top-k tiles done (fused scan)
-    status[4] = 0;                               // which wait of a GEMM timed out, if one did
-  }
+  clear_call_state(r);
 
   float acc[4][NPER];
 #pragma unroll
@@ -161,32 +180,59 @@ router_logits_kernel(const __nv_bfloat16* __restrict__ x, const float* __restric
 constexpr int kRowExp = 4, kRowParts = kThreads / 32, kRowIt = 4;
 
 __global__ void __launch_bounds__(kThreads)
-router_logits_rows_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__ rw,
-                          int T, int d, int E, float* __restrict__ part,
-                          int32_t* __restrict__ status) {
+router_logits_rows_kernel(const RouteArgs r) {
   __shared__ float red[kRowParts][kRowExp];
+  __shared__ double red_ss[kRowParts];
+  const bool norm = r.x_pre != nullptr;
+  const __nv_bfloat16* __restrict__ x = norm ? r.x_pre : r.x;
+  const float* __restrict__ rw = r.router_w;
+  const float* __restrict__ g = r.norm_w;
+  const int d = r.d, E = r.E;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x;
   const int e0 = blockIdx.y * kRowExp;
   pdl_wait();
-  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
-    status[0] = 0;                               // first kernel of a call
-    status[1] = 0;                               // top-k tiles done (fused scan)
-    status[4] = 0;                               // which wait of a GEMM timed out, if one did
-  }
+  clear_call_state(r);
   const int np = d / 4;                          // 4-element pieces of a row
   const int per = (np + kRowParts - 1) / kRowParts;
   const int p0 = warp * per, p1 = min(np, p0 + per);
   const uint2* xr = reinterpret_cast<const uint2*>(x + (size_t)t * d);
+  // the block's RMSNorm: 1/rms(x_t) in fp64 (every square of a bf16 value is
+  // exact in fp32; the sum is kept in fp64 so the bf16 rounding of x·g/rms
+  // below is decided as for the exact value)
+  float r32 = 1.f;
+  double r64 = 1.0;
+  if (norm) {
+    double ss = 0.0;
+    for (int pc = p0 + lane; pc < p1; pc += 32) {
+      const uint2 v = __ldg(xr + pc);
+      const float a0 = __uint_as_float(v.x << 16), a1 = __uint_as_float(v.x & 0xFFFF0000u);
+      const float a2 = __uint_as_float(v.y << 16), a3 = __uint_as_float(v.y & 0xFFFF0000u);
+      ss += double(a0 * a0) + double(a1 * a1) + double(a2 * a2) + double(a3 * a3);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    if (lane == 0) red_ss[warp] = ss;
+    __syncthreads();
+    double tot = 0.0;
+#pragma unroll
+    for (int q = 0; q < kRowParts; ++q) tot += red_ss[q];
+    r64 = 1.0 / sqrt(tot / double(d) + double(r.eps));
+    r32 = float(r64);
+    if (blockIdx.y == 0 && threadIdx.x == 0) r.rnorm[t] = r32;
+  }
   float acc[kRowExp] = {0.f, 0.f, 0.f, 0.f};
   for (int base = p0; base < p1; base += 32 * kRowIt) {
     uint2 xv[kRowIt];
     float4 wv[kRowExp][kRowIt];
+    float4 gv[kRowIt];
 #pragma unroll
     for (int it = 0; it < kRowIt; ++it) {
       const int pc = base + lane + 32 * it;
       const bool in = pc < p1;
       xv[it] = in ? __ldg(xr + pc) : make_uint2(0, 0);
+      gv[it] = (in && norm) ? __ldg(reinterpret_cast<const float4*>(g) + pc)
+                            : make_float4(1.f, 1.f, 1.f, 1.f);
 #pragma unroll
       for (int j = 0; j < kRowExp; ++j)
         wv[j][it] = (in && e0 + j < E)
@@ -195,9 +241,23 @@ router_logits_rows_kernel(const __nv_bfloat16* __restrict__ x, const float* __re
     }
 #pragma unroll
     for (int it = 0; it < kRowIt; ++it) {
+      const int pc = base + lane + 32 * it;
       const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&xv[it].x);
       const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&xv[it].y);
-      const float x0 = __low2float(a), x1 = __high2float(a), x2 = __low2float(b), x3 = __high2float(b);
+      float x0 = __low2float(a), x1 = __high2float(a), x2 = __low2float(b), x3 = __high2float(b);
+      if (norm) {                                // the MoE input: bf16(x·g/rms)
+        x0 = rms_scaled_bf16(x0, gv[it].x, r32, r64);
+        x1 = rms_scaled_bf16(x1, gv[it].y, r32, r64);
+        x2 = rms_scaled_bf16(x2, gv[it].z, r32, r64);
+        x3 = rms_scaled_bf16(x3, gv[it].w, r32, r64);
+        if (blockIdx.y == 0 && pc < p1) {
+          const __nv_bfloat162 lo = __floats2bfloat162_rn(x0, x1), hi = __floats2bfloat162_rn(x2, x3);
+          uint2 o;
+          o.x = *reinterpret_cast<const uint32_t*>(&lo);
+          o.y = *reinterpret_cast<const uint32_t*>(&hi);
+          reinterpret_cast<uint2*>(r.xn + (size_t)t * d)[pc] = o;
+        }
+      }
 #pragma unroll
       for (int j = 0; j < kRowExp; ++j)
         acc[j] = fmaf(x3, wv[j][it].w, fmaf(x2, wv[j][it].z, fmaf(x1, wv[j][it].y, fmaf(x0, wv[j][it].x, acc[j]))));
@@ -216,42 +276,91 @@ router_logits_rows_kernel(const __nv_bfloat16* __restrict__ x, const float* __re
     float v = 0.f;
 #pragma unroll
     for (int q = 0; q < kRowParts; ++q) v += red[q][lane];
-    part[(size_t)t * E + e0 + lane] = v;
+    r.logit_part[(size_t)t * E + e0 + lane] = v;
+  }
+  // the block-scaled design's token tables (the xn row this CTA wrote above is
+  // visible to all its threads after the barrier)
+  if (blockIdx.y == 0 && r.xq_hi)
+    quantize_rows_mx(r.x, t, 1, d, r.xq_hi, r.xq_lo, r.sx_hi, r.sx_lo, r.ld_sx);
+}
+
+// The block's RMSNorm for larger batches, before the split logits kernel: one
+// warp per token writes xn = bf16(x·g/rms) and 1/rms (as the rows kernel does).
+__global__ void __launch_bounds__(kThreads)
+rms_norm_kernel(const RouteArgs r) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (kThreads / 32) + warp;
+  pdl_wait();
+  if (t >= r.T) return;
+  const int np = r.d / 4;
+  const uint2* xr = reinterpret_cast<const uint2*>(r.x_pre + (size_t)t * r.d);
+  double ss = 0.0;
+  for (int pc = lane; pc < np; pc += 32) {
+    const uint2 v = __ldg(xr + pc);
+    const float a0 = __uint_as_float(v.x << 16), a1 = __uint_as_float(v.x & 0xFFFF0000u);
+    const float a2 = __uint_as_float(v.y << 16), a3 = __uint_as_float(v.y & 0xFFFF0000u);
+    ss += double(a0 * a0) + double(a1 * a1) + double(a2 * a2) + double(a3 * a3);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+  const double r64 = 1.0 / sqrt(ss / double(r.d) + double(r.eps));
+  const float r32 = float(r64);
+  if (lane == 0) r.rnorm[t] = r32;
+  uint2* dst = reinterpret_cast<uint2*>(r.xn + (size_t)t * r.d);
+  for (int pc = lane; pc < np; pc += 32) {
+    const uint2 v = __ldg(xr + pc);
+    const float4 gv = __ldg(reinterpret_cast<const float4*>(r.norm_w) + pc);
+    const float x0 = rms_scaled_bf16(__uint_as_float(v.x << 16), gv.x, r32, r64);
+    const float x1 = rms_scaled_bf16(__uint_as_float(v.x & 0xFFFF0000u), gv.y, r32, r64);
+    const float x2 = rms_scaled_bf16(__uint_as_float(v.y << 16), gv.z, r32, r64);
+    const float x3 = rms_scaled_bf16(__uint_as_float(v.y & 0xFFFF0000u), gv.w, r32, r64);
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(x0, x1), hi = __floats2bfloat162_rn(x2, x3);
+    uint2 o;
+    o.x = *reinterpret_cast<const uint32_t*>(&lo);
+    o.y = *reinterpret_cast<const uint32_t*>(&hi);
+    dst[pc] = o;
   }
 }
 
+// quantize: write the block-scaled design's token tables for this tile (when
+// the logits kernel did not).  One warp per token of the tile.
+constexpr int kTopkThreads = 32 * kTT;
+
 template <int NPER>
-__global__ void __launch_bounds__(kThreads)
-router_topk_kernel(const float* __restrict__ part, int nks, const float* __restrict__ rb, int T,
-                   int E, int k, int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
-                   int32_t* __restrict__ rank, int32_t* __restrict__ tile_counts,
-                   int32_t* __restrict__ tiles_done, int chunk, int32_t* __restrict__ tile_base,
-                   int32_t* __restrict__ offsets, int32_t* __restrict__ mtile_off) {
+__global__ void __launch_bounds__(kTopkThreads)
+router_topk_kernel(const RouteArgs r, int nks, bool quantize, int32_t* __restrict__ tiles_done) {
   __shared__ float wl[kTT * kLgStride];  // logits [t][e]
   __shared__ uint32_t mask[kMaxE];       // bit t: token t of this tile picked e
   __shared__ int32_t sel[kTT][8];
-  __shared__ int32_t scan_part[kThreads], scan_total[257], scan_off[257];
+  __shared__ int32_t scan_part[kTopkThreads], scan_total[257], scan_off[257];
   __shared__ int last_cta;
 
+  const float* __restrict__ part = r.logit_part;
+  const float* __restrict__ rb = r.router_b;
+  const int T = r.T, E = r.E, k = r.k;
+  int32_t* __restrict__ topk_idx = r.topk_idx;
+  float* __restrict__ topk_w = r.topk_w;
+  int32_t* __restrict__ rank = r.rank;
+  int32_t* __restrict__ tile_counts = r.tile_counts;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int t0 = blockIdx.x * kTT;
   const int ntok = min(kTT, T - t0);
-  for (int e = tid; e < kMaxE; e += kThreads) mask[e] = 0u;
+  for (int e = tid; e < kMaxE; e += kTopkThreads) mask[e] = 0u;
   pdl_wait();
 
   // logits = the K-range partial sums in a fixed order, then the bias (up to
-  // 16 partials are all loaded before any is added, one round of loads)
-  for (int idx = tid; idx < ntok * E; idx += kThreads) {
+  // 8 partials are all loaded before any is added, one round of loads)
+  for (int idx = tid; idx < ntok * E; idx += kTopkThreads) {
     const int tl = idx / E, e = idx - tl * E;
     const float* p = part + (size_t)(t0 + tl) * E + e;
     const size_t stride = (size_t)T * E;
     float v = 0.f;
-    if (nks <= 16) {
-      float pv[16];
+    if (nks <= 8) {
+      float pv[8];
 #pragma unroll
-      for (int s = 0; s < 16; ++s) pv[s] = s < nks ? p[s * stride] : 0.f;
+      for (int s = 0; s < 8; ++s) pv[s] = s < nks ? p[s * stride] : 0.f;
 #pragma unroll
-      for (int s = 0; s < 16; ++s)
+      for (int s = 0; s < 8; ++s)
         if (s < nks) v += pv[s];
     } else {
       for (int s = 0; s < nks; ++s) v += p[s * stride];
@@ -260,20 +369,20 @@ router_topk_kernel(const float* __restrict__ part, int nks, const float* __restr
   }
   __syncthreads();
 
-  // top-k per token: warp w owns tokens 4w..4w+3
-  for (int i = 0; i < 4; ++i) {
-    const int tl = warp * 4 + i, t = t0 + tl;
-    if (t >= T) break;
+  // top-k of token `warp`: k rounds of a warp-wide (logit desc, index asc)
+  // maximum over the experts not yet taken; lane j keeps slot j
+  if (warp < ntok) {
+    const int tl = warp, t = t0 + tl;
     float v[NPER];
 #pragma unroll
     for (int j = 0; j < NPER; ++j) {
       const int e = lane + 32 * j;
-      float lv = (e < E) ? wl[tl * kLgStride + e] : -INFINITY;
+      const float lv = (e < E) ? wl[tl * kLgStride + e] : -INFINITY;
       v[j] = isnan(lv) ? -INFINITY : lv;
     }
     uint32_t taken = 0;
-    float sv[8];
-    int se[8];
+    int my_e = 0;
+    float my_l = -INFINITY;
     for (int j = 0; j < k; ++j) {
       float bv = -INFINITY;
       int be = 0x7fffffff;
@@ -295,30 +404,28 @@ router_topk_kernel(const float* __restrict__ part, int nks, const float* __restr
         }
       }
       if ((be & 31) == lane) taken |= 1u << (be >> 5);
-      sv[j] = bv;
-      se[j] = be;
-    }
-    if (lane == 0) {
-      const float m = sv[0];
-      float p[8], s = 0.f;
-      for (int j = 0; j < k; ++j) {
-        p[j] = expf(sv[j] - m);
-        s += p[j];
-      }
-      const float inv_s = 1.0f / s;
-      for (int j = 0; j < k; ++j) {
-        topk_idx[(size_t)t * k + j] = se[j];
-        topk_w[(size_t)t * k + j] = p[j] * inv_s;
-        sel[tl][j] = se[j];
+      if (lane == j) {
+        my_e = be;
+        my_l = bv;
       }
     }
-    if (lane < k) atomicOr(&mask[se[lane]], 1u << tl);  // order-free: deterministic
+    // softmax over the k selected logits: exp(l_j - l_0), summed in slot order
+    const float m = __shfl_sync(0xffffffffu, my_l, 0);
+    const float pj = lane < k ? expf(my_l - m) : 0.f;
+    float ssum = 0.f;
+    for (int j = 0; j < k; ++j) ssum += __shfl_sync(0xffffffffu, pj, j);
+    if (lane < k) {
+      topk_idx[(size_t)t * k + lane] = my_e;
+      topk_w[(size_t)t * k + lane] = pj * (1.0f / ssum);
+      sel[tl][lane] = my_e;
+      atomicOr(&mask[my_e], 1u << tl);             // order-free: deterministic
+    }
   }
   __syncthreads();
 
-  for (int e = tid; e < E; e += kThreads)
+  for (int e = tid; e < E; e += kTopkThreads)
     tile_counts[(size_t)blockIdx.x * E + e] = __popc(mask[e]);
-  for (int q = tid; q < ntok * k; q += kThreads) {
+  for (int q = tid; q < ntok * k; q += kTopkThreads) {
     const int tl = q / k, j = q - tl * k;
     const int e = sel[tl][j];
     rank[(size_t)(t0 + tl) * k + j] = __popc(mask[e] & ((1u << tl) - 1u));
@@ -333,20 +440,34 @@ router_topk_kernel(const float* __restrict__ part, int nks, const float* __restr
     __syncthreads();
     if (last_cta) {
       __threadfence();
-      scan_tiles<kThreads>(tile_counts, int(gridDim.x), E, chunk, tile_base, offsets, mtile_off,
-                           scan_part, scan_total, scan_off);
+      scan_tiles<kTopkThreads>(tile_counts, int(gridDim.x), E, r.chunk, r.tile_base, r.offsets,
+                           r.mtile_off, scan_part, scan_total, scan_off);
+      if (r.perm) {
+        // every routed row's place: the (tile, expert) base this CTA just
+        // wrote plus the row's rank in its tile (other CTAs wrote those)
+        __syncthreads();
+        const int R = T * k;
+        for (int q = tid; q < R; q += kTopkThreads) {
+          const int e = __ldcg(topk_idx + q);
+          const int row = __ldcg(r.tile_base + (size_t)(q / k / kTT) * E + e) + __ldcg(rank + q);
+          if (e < 0 || e >= E || row < 0 || row >= R) {
+            atomicMax(r.status, kStatusBounds);
+            continue;
+          }
+          r.perm[row] = q;
+          r.inv[q] = row;
+        }
+      }
     }
   }
+  if (quantize)
+    quantize_rows_mx(r.x, t0, ntok, r.d, r.xq_hi, r.xq_lo, r.sx_hi, r.sx_lo, r.ld_sx);
 }
 
 }  // namespace
 
-cudaError_t launch_router_topk(const __nv_bfloat16* x, const float* router_w,
-                               const float* router_b, int T, int d, int E, int k,
-                               float* logit_part, int32_t* topk_idx, float* topk_w,
-                               int32_t* rank, int32_t* tile_counts, int32_t* status, int chunk,
-                               int32_t* tile_base, int32_t* offsets, int32_t* mtile_off,
-                               bool* scanned, cudaStream_t s) {
+cudaError_t launch_router_topk(const RouteArgs& r, bool* scanned, cudaStream_t s) {
+  const int T = r.T, d = r.d, E = r.E;
   const int ntiles = (T + kTT - 1) / kTT;
   const bool rows = ntiles <= kFuseScanTiles;   // decode-sized: whole dot products
   const int nks = rows ? 1 : router_splits(T, d, E);
@@ -357,13 +478,17 @@ cudaError_t launch_router_topk(const __nv_bfloat16* x, const float* router_w,
   const int nper = (E + 31) / 32;                // ... and in the top-k kernel
   if (nper_g < 1 || nper_g > 8 || nper > 8) return cudaErrorInvalidValue;
   cudaError_t e = cudaSuccess;
-  if (rows)
+  if (rows) {
     e = launch_pdl(router_logits_rows_kernel, dim3(T, (E + kRowExp - 1) / kRowExp), dim3(kThreads), 0,
-                   s, x, router_w, T, d, E, logit_part, status);
+                   s, r);
+  } else if (r.x_pre) {
+    // the block: the normalised table first; the logits kernel reads it
+    e = launch_pdl(rms_norm_kernel, dim3((T + kThreads / 32 - 1) / (kThreads / 32)), dim3(kThreads),
+                   0, s, r);
+  }
 #define MOE_LOGITS_CASE(N)                                                                   \
   case N:                                                                                    \
-    e = launch_pdl(router_logits_kernel<N>, g1, dim3(kThreads), 0, s, x, router_w, T, d, E,   \
-                   kc, eg, logit_part, status);                                              \
+    e = launch_pdl(router_logits_kernel<N>, g1, dim3(kThreads), 0, s, r, kc, eg);             \
     break;
   switch (rows ? 0 : nper_g) {
     MOE_LOGITS_CASE(1)
@@ -378,14 +503,16 @@ cudaError_t launch_router_topk(const __nv_bfloat16* x, const float* router_w,
 #undef MOE_LOGITS_CASE
   if (e != cudaSuccess) return e;
   // few tiles: the last top-k CTA runs the expert scan (no separate launch)
-  const bool fuse = ntiles <= kFuseScanTiles && tile_base != nullptr;
-  int32_t* done = fuse ? status + 1 : nullptr;
+  const bool fuse = ntiles <= kFuseScanTiles && r.tile_base != nullptr;
+  int32_t* done = fuse ? r.status + 1 : nullptr;
   if (scanned) *scanned = fuse;
+  RouteArgs rt = r;
+  if (!fuse) rt.perm = rt.inv = nullptr;          // the scatter kernel writes them
+  const bool quantize = !rows && r.xq_hi != nullptr;
 #define MOE_TOPK_CASE(N)                                                                     \
   case N:                                                                                    \
-    e = launch_pdl(router_topk_kernel<N>, dim3(ntiles), dim3(kThreads), 0, s, logit_part,    \
-                   nks, router_b, T, E, k, topk_idx, topk_w, rank, tile_counts, done, chunk, \
-                   tile_base, offsets, mtile_off);                                           \
+    e = launch_pdl(router_topk_kernel<N>, dim3(ntiles), dim3(kTopkThreads), 0, s, rt, nks,   \
+                   quantize, done);                                                          \
     break;
   switch (nper) {
     MOE_TOPK_CASE(1)

@@ -44,6 +44,8 @@ class DeviceMoE:
     b_dn: torch.Tensor
     out: torch.Tensor
     workspace: torch.Tensor
+    norm_w: torch.Tensor | None = None     # RMSNorm weight of the pre-norm block
+    eps: float = 1e-5
 
     @classmethod
     def upload(cls, inp: MoEInputs, device="cuda") -> "DeviceMoE":
@@ -60,11 +62,21 @@ class DeviceMoE:
             b_dn=_bf16(inp.b_dn, device),
             out=torch.empty((wl.T, wl.d), dtype=torch.bfloat16, device=device),
             workspace=torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=device),
+            norm_w=None if inp.norm_w is None else torch.from_numpy(inp.norm_w).to(device),
+            eps=inp.eps,
         )
 
     def forward(self, x=None, out=None, stream=None) -> torch.Tensor:
+        """moe_forward, or moe_block_forward when the layer carries a norm weight."""
         x = self.x if x is None else x
         out = self.out if out is None else out
+        if self.norm_w is not None:
+            moe.moe_block_forward(x, self.T, self.d, self.W, self.norm_w, self.eps,
+                                  self.router_w, self.router_b, self.w_gu, self.w_gu_scale,
+                                  self.b_gu, self.w_dn, self.w_dn_scale, self.b_dn, self.E,
+                                  self.k, self.limit, self.alpha, out, self.workspace,
+                                  self.workspace.numel(), stream)
+            return out
         moe.moe_forward(x, self.T, self.d, self.W, self.router_w, self.router_b,
                         self.w_gu, self.w_gu_scale, self.b_gu, self.w_dn, self.w_dn_scale,
                         self.b_dn, self.E, self.k, self.limit, self.alpha, out,

@@ -24,9 +24,11 @@ REGIONS = {"topk_idx": 0, "topk_w": 1, "offsets": 2, "perm": 3, "inv": 4,
            "x_perm": 5, "h_hi": 6, "h_lo": 7, "y": 8}
 
 # Every symbol include/moe.h declares.
-EXPORTS = ("moe_workspace_bytes", "moe_forward", "moe_route", "moe_poll_status",
-           "moe_last_error", "moe_workspace_region", "moe_set_trace_events",
-           "moe_forward_noalloc", "moe_hidden_format")
+EXPORTS = ("moe_workspace_bytes", "moe_forward", "moe_block_forward", "moe_route",
+           "moe_poll_status", "moe_last_error", "moe_workspace_region", "moe_set_trace_events",
+           "moe_forward_noalloc", "moe_poll_status_noalloc", "moe_hidden_format",
+           "moe_set_wait_limit", "moe_set_fault_injection", "moe_debug_combine",
+           "moe_mma_peak")
 
 # Scratch built into the library for moe_forward_noalloc (MOE_NOALLOC_SCRATCH_BYTES).
 NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -57,6 +59,9 @@ def load() -> ctypes.CDLL:
     lib.moe_forward.argtypes = [P, I64, I32, I32, P, P, P, P, P, P, P, P, I32, I32, F32, F32,
                                 P, P, SZ, P]
     lib.moe_forward.restype = I32
+    lib.moe_block_forward.argtypes = [P, I64, I32, I32, P, F32, P, P, P, P, P, P, P, P, I32,
+                                      I32, F32, F32, P, P, SZ, P]
+    lib.moe_block_forward.restype = I32
     lib.moe_route.argtypes = [P, I64, I32, P, P, I32, I32, P, P, P, P, P, P, SZ, P]
     lib.moe_route.restype = I32
     lib.moe_poll_status.argtypes = [P, P]
@@ -71,6 +76,16 @@ def load() -> ctypes.CDLL:
     lib.moe_forward_noalloc.argtypes = [P, I64, I32, I32, P, P, P, P, P, P, P, P, I32, I32, F32,
                                         F32, P, P]
     lib.moe_forward_noalloc.restype = I32
+    lib.moe_set_wait_limit.argtypes = [ctypes.c_double]
+    lib.moe_set_wait_limit.restype = I32
+    lib.moe_set_fault_injection.argtypes = [I32]
+    lib.moe_set_fault_injection.restype = I32
+    lib.moe_debug_combine.argtypes = [P, P, P, P, I64, I32, I32, P, P, SZ, P]
+    lib.moe_debug_combine.restype = I32
+    lib.moe_mma_peak.argtypes = [I32, I32, ctypes.POINTER(ctypes.c_double), P, P]
+    lib.moe_mma_peak.restype = I32
+    lib.moe_poll_status_noalloc.argtypes = [P]
+    lib.moe_poll_status_noalloc.restype = I32
     lib.moe_hidden_format.argtypes = [I64, I32, I32, I32, I32, F32, ctypes.POINTER(I32),
                                       ctypes.POINTER(I32)]
     lib.moe_hidden_format.restype = I32
@@ -125,6 +140,17 @@ def moe_forward(x_bf16, T, d, W, router_w, router_b, w_gu_fp4, w_gu_scale, b_gu_
         E, k, limit, alpha, _ptr(out_bf16), _ptr(workspace), workspace_bytes, _stream(stream)))
 
 
+def moe_block_forward(x_bf16, T, d, W, norm_w, eps, router_w, router_b, w_gu_fp4, w_gu_scale,
+                      b_gu_bf16, w_dn_fp4, w_dn_scale, b_dn_bf16, E, k, limit, alpha, out_bf16,
+                      workspace, workspace_bytes, stream=None) -> int:
+    """out = x + MoE(RMSNorm(x)); see include/moe.h."""
+    return _check(load().moe_block_forward(
+        _ptr(x_bf16), T, d, W, _ptr(norm_w), eps, _ptr(router_w), _ptr(router_b),
+        _ptr(w_gu_fp4), _ptr(w_gu_scale), _ptr(b_gu_bf16), _ptr(w_dn_fp4), _ptr(w_dn_scale),
+        _ptr(b_dn_bf16), E, k, limit, alpha, _ptr(out_bf16), _ptr(workspace), workspace_bytes,
+        _stream(stream)))
+
+
 def moe_route(x_bf16, T, d, router_w, router_b, E, k, topk_idx, topk_w, offsets, perm, inv,
               workspace, workspace_bytes, stream=None) -> int:
     return _check(load().moe_route(
@@ -170,3 +196,37 @@ def moe_forward_noalloc(x_bf16, T, d, W, router_w, router_b, w_gu_fp4, w_gu_scal
         _ptr(x_bf16), T, d, W, _ptr(router_w), _ptr(router_b), _ptr(w_gu_fp4),
         _ptr(w_gu_scale), _ptr(b_gu_bf16), _ptr(w_dn_fp4), _ptr(w_dn_scale), _ptr(b_dn_bf16),
         E, k, limit, alpha, _ptr(out_bf16), _stream(stream)))
+
+
+def moe_poll_status_noalloc(stream=None) -> int:
+    """moe_poll_status for the built-in scratch of moe_forward_noalloc."""
+    return _check(load().moe_poll_status_noalloc(_stream(stream)))
+
+
+def moe_set_wait_limit(seconds: float) -> int:
+    """Wait limit of the GEMMs' bounded waits for later calls (0: default 2 s)."""
+    return _check(load().moe_set_wait_limit(seconds))
+
+
+def moe_set_fault_injection(mode: int) -> int:
+    """Test hook (include/moe.h): 1 makes gate_up's weight producer issue nothing."""
+    return _check(load().moe_set_fault_injection(mode))
+
+
+def moe_debug_combine(y, perm, inv, topk_w, T, d, k, out_bf16, workspace, workspace_bytes,
+                      stream=None) -> int:
+    """Test hook: the fused combine on caller tables (include/moe.h)."""
+    return _check(load().moe_debug_combine(
+        _ptr(y), _ptr(perm), _ptr(inv), _ptr(topk_w), T, d, k, _ptr(out_bf16), _ptr(workspace),
+        workspace_bytes, _stream(stream)))
+
+
+MMA_KINDS = {"f16": 0, "mxf8f6f4": 1}
+
+
+def moe_mma_peak(kind, iters, workspace, stream=None) -> float:
+    """Dense TFLOP/s of an MMA kind ("f16" or "mxf8f6f4"); include/moe.h."""
+    kind = MMA_KINDS[kind] if isinstance(kind, str) else kind
+    out = ctypes.c_double(0.0)
+    _check(load().moe_mma_peak(kind, iters, ctypes.byref(out), _ptr(workspace), _stream(stream)))
+    return out.value
