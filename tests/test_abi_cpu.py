@@ -148,5 +148,54 @@ def test_gemm_design_override(lib, monkeypatch):
     decode = (32, 2880, 2880, 32, 4)
     monkeypatch.setenv("MOE_GEMM", "tmem")
     assert moe.moe_hidden_format(*decode, 7.0)[0] == moe.HIDDEN_F16_PAIR
-    monkeypatch.setenv("MOE_GEMM", "smem")
-    assert moe.moe_hidden_format(*decode, 7.0)[0] == moe.HIDDEN_BF16_PAIR
+    monkeypatch.setenv("MOE_GEMM", "anything-else")                 # ignored
+    assert moe.moe_hidden_format(*decode, 7.0)[0] == moe.HIDDEN_E4M3_TERMS
+
+
+def _block(lib, T=64, d=256, W=256, E=8, k=4, eps=1e-5, ws_bytes=None, **ptrs):
+    good = dict(x=16, g=16, rw=16, rb=16, wgu=16, wgus=16, bgu=16, wdn=16, wdns=16, bdn=16,
+                out=16, ws=16)
+    good.update(ptrs)
+    if ws_bytes is None:
+        ws_bytes = max(1, moe.moe_workspace_bytes(T, d, W, E, k))
+    p = {k_: ctypes.c_void_p(v) for k_, v in good.items()}
+    return lib.moe_block_forward(p["x"], T, d, W, p["g"], eps, p["rw"], p["rb"], p["wgu"],
+                                 p["wgus"], p["bgu"], p["wdn"], p["wdns"], p["bdn"], E, k, 7.0,
+                                 1.702, p["out"], p["ws"], ws_bytes, None)
+
+
+def test_block_argument_errors_return_before_any_launch(lib):
+    # every case below is rejected on the host; the fake addresses are never used
+    assert _block(lib, g=0) == 1                                  # MOE_ERR_NULL
+    assert "norm_w" in moe.moe_last_error()
+    assert _block(lib, g=24) == 3                                 # MOE_ERR_ALIGN
+    assert _block(lib, eps=float("nan")) == 2                     # MOE_ERR_SHAPE
+    assert _block(lib, eps=-1.0) == 2
+    assert _block(lib, eps=float("inf")) == 2
+    assert _block(lib, d=100) == 2
+    assert _block(lib, x=0) == 1
+    assert _block(lib, ws_bytes=1024) == 4                        # MOE_ERR_WORKSPACE
+    assert _block(lib, T=0, g=0) == 0                             # nothing to do
+    assert _block(lib, T=0, g=24) == 3                            # still checked at T = 0
+
+
+def test_failure_hooks_check_their_arguments(lib):
+    with pytest.raises(moe.MoEError):
+        moe.moe_set_wait_limit(1e-6)
+    with pytest.raises(moe.MoEError):
+        moe.moe_set_wait_limit(120.0)
+    with pytest.raises(moe.MoEError):
+        moe.moe_set_fault_injection(2)
+    assert moe.moe_set_wait_limit(0.5) == 0
+    assert moe.moe_set_wait_limit(0) == 0
+    assert moe.moe_set_fault_injection(0) == 0
+    # the combine launcher rejects shapes on the host (fake addresses unused)
+    assert lib.moe_debug_combine(16, 16, 16, 16, 4, 100, 4, 16, 16, 1 << 20, None) == 2
+    assert lib.moe_debug_combine(16, 16, 16, 16, 4, 128, 4, 16, 16, 8, None) == 4
+
+
+def test_mma_peak_checks_its_arguments(lib):
+    out = ctypes.c_double(0.0)
+    assert lib.moe_mma_peak(2, 10, ctypes.byref(out), 16, None) == 2
+    assert lib.moe_mma_peak(0, 0, ctypes.byref(out), 16, None) == 2
+    assert lib.moe_mma_peak(1, 10, None, 16, None) == 1

@@ -1,9 +1,11 @@
 """CUDA path vs the CPU oracle, through the C ABI, on one GPU.
 
-Small layers are compared element by element; the full gpt-oss layer shapes
-are run at full size in the same launch configuration the benchmark times,
-and compared on a seeded sample of tokens the oracle computes one by one.
+Every layer is compared element by element, the full gpt-oss layer shapes
+included: they run at full size in the launch configuration the benchmark
+times, and the oracle computes every token (its experts on all host cores).
 """
+import os
+
 import numpy as np
 import pytest
 
@@ -112,18 +114,18 @@ def test_forward_decode_20b_all_tokens():
 
 @pytest.mark.parametrize("name", ["gptoss20b_prefill", "gptoss120b_prefill",
                                   "gptoss120b_skew16k", "gptoss120b_skew64"])
-def test_forward_full_size_sampled(name):
+def test_forward_full_size_every_token(name):
+    """The full gpt-oss layers in the launch configuration the benchmark times,
+    every output element of every token against the oracle (its experts on all
+    host cores): every work unit of both GEMMs, every chunk boundary and every
+    expert segment's last partial chunk is compared."""
     wl = gen.WORKLOADS[name]
     inp = gen.make_inputs(wl)
-    rng = np.random.Generator(np.random.PCG64(1234))
-    tokens = np.unique(np.concatenate([[0, wl.T - 1], rng.choice(wl.T, size=10, replace=False)]))
-    dev, out, ref = _run(inp, tokens=tokens)
-    idx = dev.region("topk_idx").cpu().numpy()
-    excused = parity.check_routing(ref, idx, dev.region("topk_w").cpu().numpy(), wl.k)
-    keep = np.array([i for i, t in enumerate(tokens) if int(t) not in excused])
-    parity.check_output(out[tokens[keep]], ref["out"][keep])
-    # properties of the whole output: finite and written everywhere
-    assert np.all(np.isfinite(out))
+    dev = DeviceMoE.upload(inp)
+    out = bf16_to_f64(dev.forward())
+    moe.moe_poll_status(dev.workspace)
+    ref = O.moe_forward_inputs(inp, workers=os.cpu_count() or 1)
+    rel, worst = _check_full(dev, out, ref, wl.k)
     # deterministic: a second run is bitwise identical
     first = dev.out.clone()
     dev.forward()
@@ -204,29 +206,63 @@ def test_zero_tokens_is_a_no_op():
     assert torch.all(sentinel == 3.0)
 
 
-# ------------------------------------------- the other grouped-GEMM design --
+# ---------------------------------------- the TMEM design on small shapes --
 
-@pytest.mark.parametrize("name", ["T1", "ragged77", "d96_w160", "E256", "k8"])
-def test_edge_shapes_smem_staged_gemm(name, monkeypatch):
-    """MOE_GEMM=smem runs K3/K4 with the dequantised weights staged in shared
-    memory (tokens as the MMA M side) instead of tensor memory; it must meet
-    the same bar."""
-    monkeypatch.setenv("MOE_GEMM", "smem")
+@pytest.mark.parametrize("name", ["T1", "T33", "d32", "k8"])
+def test_edge_shapes_forced_tmem_design(name, monkeypatch):
+    """MOE_GEMM=tmem runs K3/K4 with the dequantised weights in tensor memory
+    on shapes the block-scaled design would otherwise take (or on its fallback
+    shapes); it must meet the same bar."""
+    monkeypatch.setenv("MOE_GEMM", "tmem")
     inp = gen.make_inputs(EDGE[name])
     dev, out, ref = _run(inp)
+    assert dev.hidden_format()[0] != moe.HIDDEN_E4M3_TERMS
     _check_full(dev, out, ref, EDGE[name].k)
 
 
-def test_both_gemm_designs_agree_on_decode(monkeypatch):
-    """The default (block-scaled) and the shared-memory-staged designs agree on
-    the 20b decode layer to well inside the oracle tolerance."""
-    inp = gen.make_inputs(gen.WORKLOADS["gptoss20b_decode"])
+# ----------------------------------- the pre-norm block: RMSNorm + residual --
+
+def _run_block(inp, tokens=None):
     dev = DeviceMoE.upload(inp)
-    a = bf16_to_f64(dev.forward().clone())
-    monkeypatch.setenv("MOE_GEMM", "smem")
-    b = bf16_to_f64(dev.forward().clone())
+    out = dev.forward()
     moe.moe_poll_status(dev.workspace)
-    parity.check_output(a, b, what="tmem vs smem design")
+    ref = O.moe_block_forward_inputs(inp, tokens=tokens, workers=os.cpu_count() or 1)
+    return dev, bf16_to_f64(out), ref
+
+
+@pytest.mark.parametrize("name,want", [("tiny", moe.HIDDEN_F16_PAIR),
+                                       ("gptoss20b_decode", moe.HIDDEN_E4M3_TERMS),
+                                       ("ragged77", moe.HIDDEN_F16_PAIR),
+                                       ("E256", moe.HIDDEN_F16_PAIR)])
+def test_block_forward_parity(name, want):
+    """out = x + MoE(RMSNorm(x)) against the oracle's block, on both GEMM
+    designs: routing (from the normalised x) bit-exact up to flagged near-ties,
+    every output element within the tolerances."""
+    wl = gen.WORKLOADS.get(name) or EDGE[name]
+    inp = gen.make_block_inputs(wl)
+    dev, out, ref = _run_block(inp)
+    assert dev.hidden_format()[0] == want
+    _check_full(dev, out, ref, wl.k)
+
+
+def test_block_forward_prefill_every_token():
+    """The 20b prefill shape through the block entry point (its RMSNorm runs as
+    a pass of its own for more than 256 tokens), every token compared."""
+    wl = gen.WORKLOADS["gptoss20b_prefill"]
+    inp = gen.make_block_inputs(wl)
+    dev, out, ref = _run_block(inp)
+    _check_full(dev, out, ref, wl.k)
+
+
+def test_block_forward_in_place():
+    """out may be the input buffer itself (an in-place residual update)."""
+    inp = gen.make_block_inputs(gen.WORKLOADS["gptoss20b_decode"])
+    dev = DeviceMoE.upload(inp)
+    want = dev.forward().clone()
+    x = dev.x.clone()
+    dev.forward(x=x, out=x)
+    moe.moe_poll_status(dev.workspace)
+    assert torch.equal(x.view(torch.int16), want.view(torch.int16))
 
 
 def test_cuda_graph_replay_matches_eager_call():
@@ -307,24 +343,16 @@ def test_block_scaled_design_falls_back(case):
 def test_stress_shape_d2048_w768_e128_top8(name):
     """Another model's MoE layer shape (d 2048, expert width 768, 128 experts,
     top-8) through the same kernels: the decode size takes the block-scaled
-    design, the prefill size the TMEM design; all tokens at decode, a seeded
-    sample at prefill."""
+    design, the prefill size the TMEM design; every token compared."""
     wl = gen.STRESS_WORKLOADS[name]
     inp = gen.make_inputs(wl)
-    tokens = None
-    if wl.T > 64:
-        rng = np.random.Generator(np.random.PCG64(4321))
-        tokens = np.unique(np.concatenate([[0, wl.T - 1], rng.choice(wl.T, size=10, replace=False)]))
-    dev, out, ref = _run(inp, tokens=tokens)
+    dev = DeviceMoE.upload(inp)
+    out = bf16_to_f64(dev.forward())
+    moe.moe_poll_status(dev.workspace)
+    ref = O.moe_forward_inputs(inp, workers=os.cpu_count() or 1)
     fmt = dev.hidden_format()[0]
     assert (fmt == moe.HIDDEN_E4M3_TERMS) == (wl.T <= 64)
-    idx = dev.region("topk_idx").cpu().numpy()
-    if tokens is None:
-        _check_full(dev, out, ref, wl.k)
-    else:
-        excused = parity.check_routing(ref, idx, dev.region("topk_w").cpu().numpy(), wl.k)
-        keep = np.array([i for i, t in enumerate(tokens) if int(t) not in excused])
-        parity.check_output(out[tokens[keep]], ref["out"][keep])
+    _check_full(dev, out, ref, wl.k)
 
 
 def test_block_scaled_design_with_16_byte_aligned_weights():
@@ -353,3 +381,38 @@ def test_block_scaled_design_with_16_byte_aligned_weights():
     _check_full(dev, bf16_to_f64(out), ref, 4)
     # the aligned call (block-scaled design) agrees with it
     parity.check_output(bf16_to_f64(dev.forward()), bf16_to_f64(out), what="aligned vs 16-byte-aligned weights")
+
+
+# ------------------------------------ the TMEM design at extreme weight scales --
+
+def _scale_extreme_inputs(limit):
+    """A layer the TMEM design takes (128 rows per expert) whose E8M0 weight
+    scales reach past the old limits of its number formats (f16: bytes above
+    240; bf16: above 142) and span far more than 2^14 within a row."""
+    wl = gen.Workload("scale_extremes", T=256, d=256, W=256, E=4, k=2, router_bias="normal",
+                      seed=51)
+    inp = gen.make_inputs(wl, limit=limit)
+    W, nsb = wl.W, wl.d // 32
+    gus, dns = inp.w_gu_scale, inp.w_dn_scale
+    if np.isfinite(limit):                     # (the clamp bounds h whatever z is)
+        gus[0, 0:16, 0] = 244                  # gate rows: one block near the top of E8M0
+    gus[0, 16:48, 1::2] = gus[0, 16:48, 0::2] - 20   # blocks 2^20 below their neighbours
+    gus[1, W:W + 32, 2] = 1                    # up rows: a block at the bottom of E8M0
+    dns[1, 0:64, 3] = dns[1, 0:64, 0] - 18      # down rows spanning 2^18
+    if not np.isfinite(limit):
+        dns[2, 0:32, 0] = 150                  # bf16 form: above 2^(142 - 127)
+    return inp
+
+
+@pytest.mark.parametrize("limit", [7.0, float("inf")])
+def test_tmem_design_extreme_weight_scales(limit):
+    """The dequantiser's per-row power-of-two factors stay exact for scale bytes
+    up to 254 (the f16 form for the clamped layer, the bf16 form for the
+    unclamped one); blocks more than 2^14 below their row's largest are left
+    out in the f16 form, an error far inside the tolerance."""
+    inp = _scale_extreme_inputs(limit)
+    dev, out, ref = _run(inp)
+    fmt = dev.hidden_format()[0]
+    assert fmt == (moe.HIDDEN_F16_PAIR if np.isfinite(limit) else moe.HIDDEN_BF16_PAIR)
+    assert np.all(np.isfinite(ref["out"]))
+    _check_full(dev, out, ref, 2)

@@ -50,3 +50,45 @@ def test_single_rank_needs_no_process_group():
     import bench
     assert bench.max_over_ranks([3.0, 4.0], 1) == [3.0, 4.0]
     assert bench.whole_job_tokens_per_s(32, 1, 0.25) == pytest.approx(128000.0)
+
+
+_RANK_SCRIPT = """
+import json, os, sys
+sys.path.insert(0, {root!r})
+import torch.distributed as dist
+import bench
+rank, local_rank, world = bench.env_rank()
+dist.init_process_group("gloo")
+ms = bench.max_over_ranks([1.0 + rank], world)[0]
+if rank == 0:
+    print(json.dumps({{"world": world, "ms": ms,
+                      "value": bench.whole_job_tokens_per_s(32, world, ms)}}), flush=True)
+dist.destroy_process_group()
+"""
+
+
+def test_launcher_starts_ranks_under_torchrun(tmp_path):
+    """bench.py --gpus N without torchrun's environment re-runs itself under
+    torch.distributed.run with N ranks on 127.0.0.1; the same command, pointed
+    at a small rank script, brings up two gloo ranks that see WORLD_SIZE = 2."""
+    import json
+    import subprocess
+    import sys
+
+    import bench
+    port = _free_port()
+    cmd = bench.launcher_command(["--gpus", "2", "--steps", "3"], 2, port)
+    assert cmd[1:3] == ["-m", "torch.distributed.run"]
+    assert "--nproc-per-node=2" in cmd and ["--master-addr", "127.0.0.1"] == cmd[5:7]
+    assert cmd[-4:] == ["--gpus", "2", "--steps", "3"]
+    assert cmd[-5].endswith("bench.py")
+    script = tmp_path / "rank.py"
+    script.write_text(_RANK_SCRIPT.format(root=os.path.dirname(os.path.abspath(bench.__file__))))
+    cmd = cmd[:-5] + [str(script)]
+    env = dict(os.environ, OMP_NUM_THREADS="1")
+    env.pop("WORLD_SIZE", None)
+    res = subprocess.run(cmd, capture_output=True, text=True, timeout=180, env=env)
+    assert res.returncode == 0, res.stderr[-2000:]
+    line = json.loads([ln for ln in res.stdout.splitlines() if ln.startswith("{")][-1])
+    assert line["world"] == 2 and line["ms"] == 2.0
+    assert line["value"] == pytest.approx(2 * 32 / 2e-3)

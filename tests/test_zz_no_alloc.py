@@ -37,6 +37,20 @@ def test_oversize_shape_is_rejected_before_any_gpu_work():
                                    v[7], v[8], 32, 4, 7.0, 1.702, v[9], None) == 2
 
 
+def test_zero_tokens_gets_the_same_argument_checks():
+    """With T = 0 the call enqueues nothing but still rejects what moe_forward
+    rejects (the fake addresses are never used)."""
+    lib = moe.load()
+    v = [16] * 11
+    args = lambda x, lim: (x, 0, 2880, 2880, v[1], v[2], v[3], v[4], v[5], v[6], v[7], v[8],
+                           32, 4, lim, 1.702, v[9], None)
+    assert lib.moe_forward_noalloc(*args(v[0], 7.0)) == 0
+    assert lib.moe_forward_noalloc(*args(24, 7.0)) == 3            # misaligned x
+    assert lib.moe_forward_noalloc(*args(v[0], float("nan"))) == 2
+    assert lib.moe_forward_noalloc(24, 0, 100, 2880, *([16] * 8), 32, 4, 7.0, 1.702, 16,
+                                   None) == 2                        # d % 32
+
+
 @pytest.mark.gpu
 @pytest.mark.parametrize("name", ["tiny", "gptoss20b_decode"])
 def test_noalloc_matches_moe_forward_on_two_calls(name):
@@ -57,6 +71,7 @@ def test_noalloc_matches_moe_forward_on_two_calls(name):
         out = torch.full_like(dev.out, float("nan"))
         _call_noalloc(dev, x, out)
         torch.cuda.synchronize()
+        assert moe.moe_poll_status_noalloc() == 0       # its own status word: no failure
         got = bf16_to_f64(out)
         parity.check_output(got, ref, what=f"{name} no-alloc vs workspace")
         # same kernels, same order of arithmetic: the results agree bit for bit
