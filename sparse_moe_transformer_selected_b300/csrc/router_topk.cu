@@ -431,9 +431,48 @@ router_topk_kernel(const RouteArgs r, int nks, bool quantize, int32_t* __restric
     rank[(size_t)(t0 + tl) * k + j] = __popc(mask[e] & ((1u << tl) - 1u));
   }
 
-  // With few tiles the CTA that finishes last also runs the expert scan (the
-  // counter was zeroed by the logits kernel of this call).
-  if (tiles_done != nullptr) {
+  if (tiles_done != nullptr && gridDim.x == 1) {
+    // One router tile (T <= 32): the expert scan and the permutation from this
+    // CTA's shared tables; no other CTA to count or wait for.
+    __syncthreads();
+    const int lane_e = tid & 31, wid = tid >> 5;
+    const int32_t v = tid < E ? __popc(mask[tid]) : 0;
+    const int32_t c = tid < E ? (v + r.chunk - 1) / r.chunk : 0;
+    int32_t iv = v, ic = c;                      // inclusive scans inside each warp
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t pv = __shfl_up_sync(0xffffffffu, iv, o);
+      const int32_t pc = __shfl_up_sync(0xffffffffu, ic, o);
+      if (lane_e >= o) { iv += pv; ic += pc; }
+    }
+    if (lane_e == 31 && wid < 8) { scan_part[wid] = iv; scan_part[8 + wid] = ic; }
+    __syncthreads();
+    if (tid < E) {
+      int32_t bv = 0, bc = 0;                    // the earlier warps' totals, in order
+      for (int w2 = 0; w2 < wid; ++w2) { bv += scan_part[w2]; bc += scan_part[8 + w2]; }
+      const int32_t ev = bv + iv - v, ec = bc + ic - c;
+      scan_off[tid] = ev;
+      r.offsets[tid] = ev;
+      r.tile_base[tid] = ev;
+      r.mtile_off[tid] = ec;
+      if (tid == E - 1) {
+        r.offsets[E] = ev + v;
+        r.mtile_off[E] = ec + c;
+      }
+    }
+    __syncthreads();
+    if (r.perm) {                                // row = expert base + rank among its tokens
+      for (int q = tid; q < ntok * k; q += kTopkThreads) {
+        const int tl = q / k, j = q - tl * k;
+        const int e = sel[tl][j];
+        const int row = scan_off[e] + __popc(mask[e] & ((1u << tl) - 1u));
+        r.perm[row] = q;
+        r.inv[q] = row;
+      }
+    }
+  } else if (tiles_done != nullptr) {
+    // With few tiles the CTA that finishes last also runs the expert scan (the
+    // counter was zeroed by the logits kernel of this call).
     __threadfence();
     __syncthreads();
     if (tid == 0) last_cta = atomicAdd(tiles_done, 1) == int(gridDim.x) - 1;
