@@ -52,22 +52,25 @@ SUSTAINED_AFTER_MS = 1000.0
 
 
 def kernels_per_step(T: int, block_scaled: bool) -> int:
-    """Kernels one moe_forward launches: router logits, router top-k, gate_up,
-    and down with the combine; plus the scan and the scatter when T has more
-    than 8 router tiles (else the last top-k CTA runs them), and the scatter
-    whenever the TMEM design needs its gathered f16 rows."""
+    """Kernels one moe_forward launches: router logits, router top-k, then
+    gate_up and down with the combine (the block-scaled design runs the three
+    in one kernel); plus the scan and the scatter when T has more than 8
+    router tiles (else the last top-k CTA runs them), and the scatter whenever
+    the TMEM design needs its gathered f16 rows."""
     tiles = (T + 31) // 32
+    experts = 1 if block_scaled else 2
     if tiles > FUSE_SCAN_TILES:
-        return 6
-    return 4 if block_scaled else 5
+        return 4 + experts
+    return 2 + experts + (0 if block_scaled else 1)
 
 
 KERNEL_SOURCES = {
     "router_topk": "router_topk.cu", "route_scan": "permute.cu", "route_scatter": "permute.cu",
     "gate_up": "expert_gemm_tmem.cu", "down_combine": "expert_gemm_tmem.cu",
 }
-# the grouped GEMMs of the block-scaled design (E4M3-term activations)
-MX_SOURCES = {"gate_up": "expert_gemm_mx.cu", "down_combine": "expert_gemm_mx.cu"}
+# the block-scaled design (E4M3-term activations) runs gate_up, down and the
+# combine as one kernel, timed as the stage "experts"
+MX_SOURCES = {"experts": "expert_gemm_mx.cu"}
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 
 
@@ -159,7 +162,7 @@ def stage_work(wl: gen.Workload, counts: np.ndarray):
     active = int((counts > 0).sum())
     gu_bytes_expert = 2 * W * d // 2 + 2 * W * d // 32 + 2 * W * 2          # codes, scales, bias
     dn_bytes_expert = d * W // 2 + d * W // 32 + d * 2
-    return {
+    out = {
         "router_topk": {"flops": 2 * T * d * E, "bytes": T * d * 2 + E * d * 4 + E * 4 + R * 12},
         "route_scan": {"flops": 0, "bytes": 8 * E * ((T + 31) // 32) + 8 * (E + 1)},
         "route_scatter": {"flops": 0, "bytes": R * d * 2 + T * d * 2 + R * 20},
@@ -172,6 +175,12 @@ def stage_work(wl: gen.Workload, counts: np.ndarray):
                          "unit": f"{active} active experts x {dn_bytes_expert} B + h + y + out"},
         "_active": active,
     }
+    out["experts"] = {
+        "flops": out["gate_up"]["flops"] + out["down_combine"]["flops"],
+        "bytes": active * (gu_bytes_expert + dn_bytes_expert) + T * d * 2 + T * d * 2,
+        "unit": f"{active} active experts x {gu_bytes_expert + dn_bytes_expert} B + x terms + out "
+                "(h and y are produced and consumed inside the kernel)"}
+    return out
 
 
 def kernel_traffic(kernel: str, workload: str, mx: bool = False):
@@ -196,7 +205,7 @@ def roofline(wl, counts, stage_ms, step_ms, mx, peaks, peak_src):
     under the ridge point, else tensor flops against the dense peak of the MMA
     kind it issues (kind::f16: bf16's; burst for steps under a second)."""
     work = stage_work(wl, counts)
-    top = max((s for s in STAGES if s in work), key=lambda s_: stage_ms[s_])
+    top = max((s for s in stage_ms if s in work), key=lambda s_: stage_ms[s_])
     wk = work[top]
     intensity = wk["flops"] / max(1, wk["bytes"])
     ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
@@ -380,6 +389,9 @@ def measure(wl, steps, warmup, world, flush_l2, with_e2e):
     stage_ms = {name: statistics.fmean(r[i].elapsed_time(r[i + 1]) for r in tev)
                 for i, name in enumerate(STAGES)}
     fmt, _ = dev.hidden_format()
+    if fmt == moe.HIDDEN_E4M3_TERMS:
+        # one expert kernel between trace events 3 and 4
+        stage_ms["experts"] = stage_ms.pop("gate_up") + stage_ms.pop("down_combine")
     res = {"ms": ms, "stage_ms": stage_ms, "counts": counts,
            "mx": fmt == moe.HIDDEN_E4M3_TERMS, "dev": dev}
     if with_e2e:

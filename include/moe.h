@@ -222,6 +222,8 @@ moe_status moe_hidden_format(int64_t T, int d, int W, int E, int k, float limit,
  *   [0] before the router   [1] after router/top-k   [2] after the scan
  *   [3] after the permute   [4] after gate_up        [5] after down and the
  *   combine (which runs in the down kernel's epilogue)   [6] = [5]
+ * The block-scaled design (MOE_HIDDEN_E4M3_TERMS) runs gate_up, down and the
+ * combine in one kernel: [4] = [5] = [6] follow it.
  * n = 0 (or events = NULL) turns tracing off.  The handles are used by every
  * later moe_forward on this thread until replaced; the caller keeps them alive.
  * Returns MOE_ERR_SHAPE for any other n.

@@ -101,7 +101,9 @@ struct Workspace {
   size_t y;            // float[R, d]
   size_t sx_hi;        // uint8[T, ld_sx]  UE8M0 block scales of x hi (block-scaled design)
   size_t sx_lo;        // uint8[T, ld_sx]  ... of x lo
-  size_t cnt;          // int32[T, ceil(d/128)]  combine counts per (token, output column tile)
+  size_t cnt;          // int32[T, ceil(d/128)]  combine counts per (token, output column tile),
+                      // then int32[T k / 8 + E + 1]: per token chunk of 8 rows, the gate_up
+                      // tiles whose h is stored (block-scaled design)
   size_t rnorm;        // float[T]  1/rms of each token (the block's RMSNorm)
   // The block's MoE input bf16(RMSNorm(x)) [T, d] lives at the start of the y
   // region: it is read only by the routing stages, before K4 writes y.
@@ -145,7 +147,7 @@ inline Workspace workspace_layout(int64_t T, int d, int W, int E, int k) {
   ws.y = take(size_t(R) * d * 4);
   ws.sx_hi = take(size_t(T) * scale_row_bytes(d));
   ws.sx_lo = take(size_t(T) * scale_row_bytes(d));
-  ws.cnt = take(size_t(T) * down_col_tiles(d) * 4);
+  ws.cnt = take((size_t(T) * down_col_tiles(d) + size_t(R) / 8 + E + 1) * 4);
   ws.rnorm = take(size_t(T) * 4);
   ws.total = off;
   return ws;
@@ -266,6 +268,9 @@ struct GemmArgs {
   const float* topk_w;        // [T k]
   int32_t* cnt;               // [T, n_mt_dn], zero when K4 starts
   int n_mt_dn;
+  // block-scaled design: per token chunk, the gate_up tiles whose h rows are
+  // stored (zero when the expert kernel starts); a down unit waits for all
+  int32_t* ready;
   __nv_bfloat16* out;         // [T, d]
   const __nv_bfloat16* resid; // [T, d] or null
   // failure detection: a bounded wait gives up after wait_ns nanoseconds
@@ -307,8 +312,11 @@ int mx_chunk(int64_t R, int E);
 // Exponent of the fixed power-of-two scale of h: |h| <= limit * (limit + 1)
 // maps inside the E4M3 range.
 int mx_hidden_exp(float limit);
-cudaError_t launch_gateup_mx(const GemmArgs& a, cudaStream_t s);
-cudaError_t launch_down_mx(const GemmArgs& a, cudaStream_t s);
+// Chunks the block-scaled design can have for R rows over E experts (the
+// length of GemmArgs::ready).
+int mx_chunk_bound(int64_t R, int E);
+// K3, K4 and K5 of the block-scaled design in one persistent kernel.
+cudaError_t launch_experts_mx(const GemmArgs& a, cudaStream_t s);
 
 
 }  // namespace moe

@@ -39,7 +39,7 @@
 // (a row's 4 scale bytes of 4 consecutive K blocks share a 32-bit column; the
 // MMA picks the byte with the descriptor's scale-factor ID).
 //
-// Persistent kernel, one CTA per SM, 12 warps:
+// One persistent kernel runs both GEMMs, one CTA per SM, 12 warps:
 //   warp 0      producer: per unit the weight scale rows (1-D bulk copies),
 //               per stage A and B (TMA); one ring of stages of 256 K
 //   warp 1      MMA issuer (one elected thread)
@@ -48,7 +48,16 @@
 //   warps 4-7   epilogue, TMEM lane quarter = warp % 4
 //   warps 8-11  scale writers, TMEM lane quarter = warp % 4 (gate_up's
 //               activation scales read from L2, one token row per lane)
-// Work unit = (token chunk of one expert, weight tile of 128 rows), chunk-major.
+// Work units: first every gate_up unit, then every down unit, each list
+// chunk-major (token chunk of one expert x weight tile); CTA c takes units
+// c, c + grid, ...  A down unit needs the whole h of its chunk: the gate_up
+// epilogue of each (chunk, tile) releases a per-chunk count once its h rows
+// are stored, and the producer acquires the full count before it loads the
+// chunk's h.  Every CTA finishes its gate_up units before it reaches a down
+// unit, so the waits form no cycle; the launch is cooperative (all CTAs
+// resident), and each wait is bounded.  CTAs that finish their gate_up share
+// early start on the first chunks' down units while the others finish, so
+// the two GEMMs share one ramp and one tail.
 #include "combine.cuh"
 #include "common.cuh"
 #include "map_cache.cuh"
@@ -82,8 +91,6 @@ constexpr int kMaxSmem = 232448;
 // stage ring (full + empty), scales (2 + 2), scale columns (2 + 2),
 // accumulators (2 + 2), final drain
 constexpr int kNumBars = 2 * kMaxStages + 4 + 4 + 4 + 1;
-
-enum class Mode { GateUp, Down };
 
 // Bounded wait: true when the phase completed; false after limit_ns
 // nanoseconds (code in status[0], the waiting role's tag in status[4]) or when
@@ -139,56 +146,72 @@ __device__ __forceinline__ float from_e4m3(uint32_t b) {
   return __half2float(__half(__nv_cvt_fp8_to_halfraw(__nv_fp8_storage_t(b), __NV_E4M3)));
 }
 
-// Per-launch geometry, the same on host and device.
-struct Geo {
+// Geometry of one GEMM (gate_up or down), the same on host and device.
+struct ModeGeo {
   int K, nsb, groups;        // reduction length, scale bytes per weight row, SF groups
   int nbox_main, tail;       // 128-K boxes from the main map; K % 128 (0: no tail box)
   int nbox, nstage;          // boxes per unit (main + tail), stages of 2 boxes
-  int NT, rpt, N;            // B terms, B rows per term, MMA N = NT rpt
-  int box_rows;              // A rows per TMA box: 64 (gate and up halves) or 128
-  int a_stage, b_stage;      // bytes per stage
-  int sc_a, sc_b, sc_buf;    // scale bytes per unit: A rows, one B table, buffer stride
-  int stages;                // ring depth
-  int off_b, off_sc, off_xch, off_bars, total;
+  int NT, rpt;               // B terms, B rows per term (N = NT rpt = kBRows)
+  int n_out, rows_per_tile;  // output columns; weight rows of one tile's output
+  int n_mt;                  // weight tiles per chunk
+  int rpe;                   // weight rows per expert
+  int sc_a;                  // scale bytes of a unit's weight rows (16-byte multiple)
 };
 
-template <Mode M>
-__host__ __device__ inline Geo geometry(int d, int W, int nb, int ld_sx, int stages) {
-  Geo g{};
-  g.K = (M == Mode::GateUp) ? d : W;
+__host__ __device__ inline ModeGeo mode_geo(bool gate_up, int d, int W) {
+  ModeGeo g{};
+  g.K = gate_up ? d : W;
   g.nsb = g.K / 32;
   g.groups = (g.nsb + 3) / 4;
   g.nbox_main = g.K / kBoxK;
   g.tail = g.K % kBoxK;
   g.nbox = g.nbox_main + (g.tail ? 1 : 0);
   g.nstage = (g.nbox + 1) / 2;
-  g.NT = (M == Mode::GateUp) ? kXTerms : kHTerms;
+  g.NT = gate_up ? kXTerms : kHTerms;
   g.rpt = kBRows / g.NT;                   // gate_up: two atoms of 4 tokens; down: 8 rows
-  g.N = kBRows;
-  g.box_rows = (M == Mode::GateUp) ? kMW / 2 : kMW;
-  g.a_stage = 2 * kBoxBytesA;
-  g.b_stage = 2 * g.N * kBoxK;
+  g.n_out = gate_up ? W : d;
+  g.rows_per_tile = gate_up ? kMW / 2 : kMW;
+  g.n_mt = (g.n_out + g.rows_per_tile - 1) / g.rows_per_tile;
+  g.rpe = gate_up ? 2 * W : d;
   g.sc_a = (kMW * g.nsb + 15) / 16 * 16;
-  g.sc_b = 0;                               // (activation scales are read from L2)
-  g.sc_buf = g.sc_a + 2 * g.sc_b;
+  return g;
+}
+
+// Shared-memory plan of the launch (both GEMMs share the ring).
+struct Geo {
+  int groups;                // SF groups of the larger K (TMEM scale columns)
+  int a_stage, b_stage;      // bytes per stage
+  int stages;                // ring depth
+  int off_b, off_sc, off_xch, off_bars, off_comb, total;
+};
+
+__host__ __device__ inline Geo geometry(int d, int W, int stages) {
+  const ModeGeo gu = mode_geo(true, d, W), dn = mode_geo(false, d, W);
+  Geo g{};
+  g.groups = gu.groups > dn.groups ? gu.groups : dn.groups;
+  g.a_stage = 2 * kBoxBytesA;
+  g.b_stage = 2 * kBRows * kBoxK;
   g.stages = stages;
   int off = stages * g.a_stage;
   g.off_b = off;
   off += stages * g.b_stage;
   g.off_sc = off;
-  off += g.sc_buf;
+  off += gu.sc_a > dn.sc_a ? gu.sc_a : dn.sc_a;
   g.off_xch = off;
-  off += (M == Mode::GateUp) ? (kMW / 2) * kNB * 4 : 0;
+  off += (kMW / 2) * kNB * 4;
   off = (off + 7) & ~7;
   g.off_bars = off;
   off += kNumBars * 8 + 16;           // barriers, TMEM base, abort flag
-  off += (M == Mode::Down) ? combine_smem_bytes(kNB) : 0;
+  g.off_comb = off;
+  off += combine_smem_bytes(kNB);
   g.total = off;
   return g;
 }
 
 struct Unit {
   int e, r0, n, mt;   // expert, first permuted row of the chunk, tokens in it, weight tile
+  int g;              // chunk index (over all experts)
+  bool gu;            // a gate_up unit (else down)
 };
 
 __device__ __forceinline__ int expert_of_chunk(const int32_t* mtile_off, int E, int g) {
@@ -200,12 +223,17 @@ __device__ __forceinline__ int expert_of_chunk(const int32_t* mtile_off, int E, 
   return lo;
 }
 
-__device__ __forceinline__ Unit unit_of(const GemmArgs& a, int n_mt, int u) {
-  const int g = u / n_mt;
+// Unit u of the launch: gate_up units [0, u_gu), then down units.
+__device__ __forceinline__ Unit unit_of(const GemmArgs& a, const ModeGeo& MG, const ModeGeo& MD,
+                                        int u_gu, int u) {
   Unit w;
-  w.mt = u - g * n_mt;
-  w.e = expert_of_chunk(a.mtile_off, a.E, g);
-  w.r0 = __ldg(a.offsets + w.e) + (g - __ldg(a.mtile_off + w.e)) * a.nb;
+  w.gu = u < u_gu;
+  const int n_mt = w.gu ? MG.n_mt : MD.n_mt;
+  const int ul = w.gu ? u : u - u_gu;
+  w.g = ul / n_mt;
+  w.mt = ul - w.g * n_mt;
+  w.e = expert_of_chunk(a.mtile_off, a.E, w.g);
+  w.r0 = __ldg(a.offsets + w.e) + (w.g - __ldg(a.mtile_off + w.e)) * a.nb;
   w.n = min(a.nb, __ldg(a.offsets + w.e + 1) - w.r0);
   return w;
 }
@@ -219,23 +247,44 @@ __device__ __forceinline__ uint32_t scale_word(const uint8_t* row, int g, int ns
   return w;
 }
 
+// Bounded wait until *count >= target (acquire): false after limit_ns
+// (status word MOE_ERR_TIMEOUT, the waiting role's tag in status[4]) or when
+// another thread of the CTA gave up.
+__device__ __forceinline__ bool wait_count(const int32_t* count, int target, volatile int* abort_flag,
+                                           int32_t* status, long long limit_ns, int tag) {
+  if (ptx::ld_acquire_gpu(count) >= target) return true;
+  const unsigned long long t0 = global_ns();
+  for (uint32_t n = 1;; ++n) {
+    __nanosleep(128);
+    if (ptx::ld_acquire_gpu(count) >= target) return true;
+    if ((n & 31) == 0) {
+      if (*abort_flag) return false;
+      if ((long long)(global_ns() - t0) > limit_ns) {
+        *abort_flag = 1;
+        atomicMax(status, kStatusTimeout);
+        atomicExch(status + 4, tag);
+        return false;
+      }
+    }
+  }
+}
+
 // ------------------------------------------------------------- kernel --
 
-template <Mode M>
 __global__ void __launch_bounds__(kThreads, 1)
-moe_expert_gemm_mx(const __grid_constant__ CUtensorMap map_w,     // main codes
-                   const __grid_constant__ CUtensorMap map_wt,    // tail codes
-                   const __grid_constant__ CUtensorMap map_b0,    // activation terms
-                   const __grid_constant__ CUtensorMap map_b1,
-                   const __grid_constant__ CUtensorMap map_b2,
-                   const __grid_constant__ CUtensorMap map_b3,
-                   const GemmArgs a, const int stages) {
-  constexpr bool kGateUp = (M == Mode::GateUp);
-  const Geo G = geometry<M>(a.d, a.W, a.nb, a.ld_sx, stages);
-  const int rpe = kGateUp ? 2 * a.W : a.d;           // weight rows per expert
-  const int n_out = kGateUp ? a.W : a.d;
-  const int rows_per_tile = kGateUp ? kMW / 2 : kMW;
-  const int n_mt = (n_out + rows_per_tile - 1) / rows_per_tile;
+moe_expert_mx(const __grid_constant__ CUtensorMap map_wg,     // gate_up codes, main and tail
+              const __grid_constant__ CUtensorMap map_wgt,
+              const __grid_constant__ CUtensorMap map_wd,     // down codes, main and tail
+              const __grid_constant__ CUtensorMap map_wdt,
+              const __grid_constant__ CUtensorMap map_x0,     // x term token tables
+              const __grid_constant__ CUtensorMap map_x1,
+              const __grid_constant__ CUtensorMap map_h0,     // h term tables
+              const __grid_constant__ CUtensorMap map_h1,
+              const __grid_constant__ CUtensorMap map_h2,
+              const __grid_constant__ CUtensorMap map_h3,
+              const GemmArgs a, const int stages) {
+  const ModeGeo MG = mode_geo(true, a.d, a.W), MD = mode_geo(false, a.d, a.W);
+  const Geo G = geometry(a.d, a.W, stages);
   const int S = G.stages;
 
   extern __shared__ uint8_t smem_raw[];
@@ -256,7 +305,7 @@ moe_expert_gemm_mx(const __grid_constant__ CUtensorMap map_w,     // main codes
   uint64_t* mma_done = acc_empty + 2;
   uint32_t* tmem_base_p = reinterpret_cast<uint32_t*>(smem + G.off_bars + kNumBars * 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + G.off_bars + kNumBars * 8 + 4);
-  uint8_t* comb = smem + G.off_bars + kNumBars * 8 + 16;         // combine lists (down)
+  uint8_t* comb = smem + G.off_comb;             // combine lists (down units)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -289,30 +338,29 @@ moe_expert_gemm_mx(const __grid_constant__ CUtensorMap map_w,     // main codes
   const uint32_t sfa_col0 = 2 * kAccCols;
   const uint32_t sfb_col0 = 2 * kAccCols + 2 * 4 * G.groups;
   pdl_wait();
-  if (kGateUp) pdl_trigger();
-  const int units = __ldg(a.mtile_off + a.E) * n_mt;
+  const int chunks = __ldg(a.mtile_off + a.E);
+  const int u_gu = chunks * MG.n_mt;
+  const int units = u_gu + chunks * MD.n_mt;
 
   if (warp == kWarpProd) {
     // ------------------------------------------------------------ producer --
-    if (ptx::elect_one() && !(kGateUp && a.inject == 1)) {
-      ptx::tma_prefetch_desc(&map_w);
-      if (G.tail) ptx::tma_prefetch_desc(&map_wt);
-      const CUtensorMap* mb[4] = {&map_b0, &map_b1, &map_b2, &map_b3};
-      for (int t = 0; t < G.NT; ++t) ptx::tma_prefetch_desc(mb[t]);
-      const uint8_t* wscale = kGateUp ? a.w_gu_scale : a.w_dn_scale;
+    if (ptx::elect_one() && a.inject != 1) {
+      ptx::tma_prefetch_desc(&map_wg);
+      ptx::tma_prefetch_desc(&map_x0);
+      ptx::tma_prefetch_desc(&map_x1);
       Ring st;
       Inflight in_st, in_sc;
       // weight rows of a unit: gate and up halves (gate_up) or one block (down)
       auto rows_of = [&](const Unit& w, int& ra, int& rb, int& nrows) {
-        if constexpr (kGateUp) {
+        if (w.gu) {
           const int n0 = w.mt * (kMW / 2);
           nrows = min(kMW / 2, a.W - n0);
-          ra = w.e * rpe + n0;
-          rb = w.e * rpe + a.W + n0;
+          ra = w.e * MG.rpe + n0;
+          rb = w.e * MG.rpe + a.W + n0;
         } else {
           const int m0 = w.mt * kMW;
           nrows = min(kMW, a.d - m0);
-          ra = w.e * rpe + m0;
+          ra = w.e * MD.rpe + m0;
           rb = ra;
         }
       };
@@ -321,67 +369,83 @@ moe_expert_gemm_mx(const __grid_constant__ CUtensorMap map_w,     // main codes
       // scale writers have emptied (they copy a unit's scales into TMEM during
       // the unit before it), so the MMA finds them in TMEM.
       auto load_scales = [&](int uu, int qq) -> bool {
-        const Unit w = unit_of(a, n_mt, uu);
+        const Unit w = unit_of(a, MG, MD, u_gu, uu);
         if (!wait_phase(&sc_empty[0], (qq & 1) ^ 1, abort_flag, a.status, a.wait_ns, 64, 5)) return false;
-        uint8_t* dst = scb;
         int ra, rb, nrows;
         rows_of(w, ra, rb, nrows);
-        const uint32_t bytes = uint32_t(nrows * G.nsb);
-        if constexpr (kGateUp) {
+        const int nsb = w.gu ? MG.nsb : MD.nsb;
+        const uint8_t* wscale = w.gu ? a.w_gu_scale : a.w_dn_scale;
+        const uint32_t bytes = uint32_t(nrows * nsb);
+        if (w.gu) {
           // the weight scale rows (the activations' are read by the writers)
           ptx::mbar_arrive_expect_tx(&sc_full[0], 2 * bytes);
-          ptx::bulk_load(dst, wscale + size_t(ra) * G.nsb, bytes, &sc_full[0]);
-          ptx::bulk_load(dst + (kMW / 2) * G.nsb, wscale + size_t(rb) * G.nsb, bytes, &sc_full[0]);
+          ptx::bulk_load(scb, wscale + size_t(ra) * nsb, bytes, &sc_full[0]);
+          ptx::bulk_load(scb + (kMW / 2) * nsb, wscale + size_t(rb) * nsb, bytes, &sc_full[0]);
         } else {
           ptx::mbar_arrive_expect_tx(&sc_full[0], bytes);
-          ptx::bulk_load(dst, wscale + size_t(ra) * G.nsb, bytes, &sc_full[0]);
+          ptx::bulk_load(scb, wscale + size_t(ra) * nsb, bytes, &sc_full[0]);
         }
         in_sc.mark(0, qq & 1);
         return true;
       };
+      const CUtensorMap* mh[4] = {&map_h0, &map_h1, &map_h2, &map_h3};
       bool ok = blockIdx.x >= units || load_scales(blockIdx.x, 0);
+      bool down_maps = false;
       int q = 0;
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++q) {
-        const Unit w = unit_of(a, n_mt, u);
+        const Unit w = unit_of(a, MG, MD, u_gu, u);
+        const ModeGeo& M = w.gu ? MG : MD;
         int row_a, row_b, nrows;
         rows_of(w, row_a, row_b, nrows);
         // gate_up: the chunk's tokens (rows past the chunk repeat its first)
         int tok[kNB];
-        if constexpr (kGateUp) {
+        if (w.gu) {
 #pragma unroll
           for (int j = 0; j < kNB; ++j) tok[j] = __ldg(a.perm + w.r0 + (j < w.n ? j : 0)) / a.k;
+        } else {
+          if (!down_maps) {
+            ptx::tma_prefetch_desc(&map_wd);
+            for (int t = 0; t < kHTerms; ++t) ptx::tma_prefetch_desc(mh[t]);
+            down_maps = true;
+          }
+          // every gate_up tile of this chunk has stored its h rows
+          if (!wait_count(a.ready + w.g, MG.n_mt, abort_flag, a.status, a.wait_ns, 9)) { ok = false; break; }
+          ptx::fence_proxy_async_global();
         }
-        for (int s = 0; s < G.nstage; ++s) {
+        const CUtensorMap* mw = w.gu ? &map_wg : &map_wd;
+        const CUtensorMap* mwt = w.gu ? &map_wgt : &map_wdt;
+        for (int s = 0; s < M.nstage; ++s) {
           // the next unit's scales, once this unit's first stages are out
-          if (s == min(1, G.nstage - 1) && u + int(gridDim.x) < units &&
+          if (s == min(1, M.nstage - 1) && u + int(gridDim.x) < units &&
               !load_scales(u + int(gridDim.x), q + 1)) { ok = false; break; }
           if (!wait_phase(&empty[st.slot], st.phase ^ 1, abort_flag, a.status, a.wait_ns, 64, 4)) { ok = false; break; }
-          const int i0 = 2 * s, i1 = min(2 * s + 2, G.nbox);
+          const int i0 = 2 * s, i1 = min(2 * s + 2, M.nbox);
           // the 4-bit TMA counts the packed bytes it reads (half of what it
           // writes); gate_up's B is two gathers of 4 rows per term
-          const uint32_t b_box = kGateUp ? uint32_t(G.NT * 2 * 4 * kBoxK) : uint32_t(G.N * kBoxK);
+          const uint32_t b_box = w.gu ? uint32_t(MG.NT * 2 * 4 * kBoxK) : uint32_t(kBRows * kBoxK);
           ptx::mbar_arrive_expect_tx(&full[st.slot], uint32_t(i1 - i0) * (kBoxBytesA / 2 + b_box));
           uint8_t* da = sa + st.slot * G.a_stage;
           uint8_t* db = sb + st.slot * G.b_stage;
           for (int i = i0; i < i1; ++i) {
             uint8_t* dai = da + (i - i0) * kBoxBytesA;
-            uint8_t* dbi = db + (i - i0) * G.N * kBoxK;
-            const bool main_box = i < G.nbox_main;
-            const CUtensorMap* mw = main_box ? &map_w : &map_wt;
+            uint8_t* dbi = db + (i - i0) * kBRows * kBoxK;
+            const bool main_box = i < M.nbox_main;
+            const CUtensorMap* mwi = main_box ? mw : mwt;
             const int xa = main_box ? i * kBoxK : 0;
-            ptx::tma_load_2d(dai, mw, &full[st.slot], xa, row_a);
             const int xb = i * kBoxK;
-            if constexpr (kGateUp) {
-              ptx::tma_load_2d(dai + (kMW / 2) * kBoxK, mw, &full[st.slot], xa, row_b);
-              for (int t = 0; t < G.NT; ++t) {
-                ptx::tma_gather4(dbi + t * G.rpt * kBoxK, mb[t], &full[st.slot], xb, tok[0], tok[1],
+            ptx::tma_load_2d(dai, mwi, &full[st.slot], xa, row_a);
+            if (w.gu) {
+              ptx::tma_load_2d(dai + (kMW / 2) * kBoxK, mwi, &full[st.slot], xa, row_b);
+              for (int t = 0; t < MG.NT; ++t) {
+                const CUtensorMap* mb = t ? &map_x1 : &map_x0;
+                ptx::tma_gather4(dbi + t * MG.rpt * kBoxK, mb, &full[st.slot], xb, tok[0], tok[1],
                                  tok[2], tok[3]);
-                ptx::tma_gather4(dbi + t * G.rpt * kBoxK + 1024, mb[t], &full[st.slot], xb, tok[4],
+                ptx::tma_gather4(dbi + t * MG.rpt * kBoxK + 1024, mb, &full[st.slot], xb, tok[4],
                                  tok[5], tok[6], tok[7]);
               }
             } else {
-              for (int t = 0; t < G.NT; ++t)
-                ptx::tma_load_2d(dbi + t * G.rpt * kBoxK, mb[t], &full[st.slot], xb, w.r0);
+              for (int t = 0; t < MD.NT; ++t)
+                ptx::tma_load_2d(dbi + t * MD.rpt * kBoxK, mh[t], &full[st.slot], xb, w.r0);
             }
           }
           in_st.mark(st.slot, st.phase);
@@ -393,17 +457,19 @@ moe_expert_gemm_mx(const __grid_constant__ CUtensorMap map_w,     // main codes
         in_sc.drain(sc_full, 1);
       }
     }
+    __syncwarp();                 // the warp reaches the final barrier converged
   } else if (warp == kWarpMMA) {
     // ------------------------------------------------------------ MMA issuer --
     if (ptx::elect_one()) {
       uint32_t idesc[4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) idesc[j] = ptx::idesc_mx(kMW, G.N, j, j);
-      const int tail_off = kBoxK - G.tail;          // first tail code inside the tail box
+      for (int j = 0; j < 4; ++j) idesc[j] = ptx::idesc_mx(kMW, kBRows, j, j);
       Ring st;
       bool ok = true;
       int q = 0;
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++q) {
+        const ModeGeo& M = u < u_gu ? MG : MD;
+        const int tail_off = kBoxK - M.tail;          // first tail code inside the tail box
         const int buf = q & 1;
         if (!wait_phase(&acc_empty[buf], ((q >> 1) & 1) ^ 1, abort_flag, a.status, a.wait_ns, 0, 2)) { ok = false; break; }
         if (!wait_phase(&sf_full[buf], (q >> 1) & 1, abort_flag, a.status, a.wait_ns, 0, 3)) { ok = false; break; }
@@ -412,24 +478,24 @@ moe_expert_gemm_mx(const __grid_constant__ CUtensorMap map_w,     // main codes
         const uint32_t sfa = tmem_base + sfa_col0 + buf * 4 * G.groups;
         const uint32_t sfb = tmem_base + sfb_col0 + buf * 4 * G.groups;
         uint32_t acc = 0;
-        for (int s = 0; s < G.nstage; ++s) {
+        for (int s = 0; s < M.nstage; ++s) {
           if (!wait_phase(&full[st.slot], st.phase, abort_flag, a.status, a.wait_ns, 0, 1)) { ok = false; break; }
           ptx::tc_fence_after();
           const uint32_t a_addr = ptx::smem_u32(sa + st.slot * G.a_stage);
           const uint32_t b_addr = ptx::smem_u32(sb + st.slot * G.b_stage);
-          const int i0 = 2 * s, i1 = min(2 * s + 2, G.nbox);
+          const int i0 = 2 * s, i1 = min(2 * s + 2, M.nbox);
           for (int i = i0; i < i1; ++i) {
             const uint64_t adesc = ptx::desc_kmajor_sw128(a_addr + uint32_t((i - i0) * kBoxBytesA));
-            const uint64_t bdesc = ptx::desc_kmajor_sw128(b_addr + uint32_t((i - i0) * G.N * kBoxK));
+            const uint64_t bdesc = ptx::desc_kmajor_sw128(b_addr + uint32_t((i - i0) * kBRows * kBoxK));
             const uint32_t sf_off = uint32_t(4 * i);     // SF group i: K blocks 4i..4i+3
-            if (i < G.nbox_main) {
+            if (i < M.nbox_main) {
 #pragma unroll
               for (int j = 0; j < 4; ++j) {
                 ptx::mma_mx(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc[j], sfa + sf_off, sfb + sf_off, acc);
                 acc = 1;
               }
             } else {
-              for (int j = 0; j < G.tail / 32; ++j) {
+              for (int j = 0; j < M.tail / 32; ++j) {
                 ptx::mma_mx(d_tmem, adesc + uint64_t((tail_off + 32 * j) >> 4), bdesc + 2 * j, idesc[j],
                             sfa + sf_off, sfb + sf_off, acc);
                 acc = 1;
@@ -448,6 +514,7 @@ moe_expert_gemm_mx(const __grid_constant__ CUtensorMap map_w,     // main codes
       while (!ptx::mbar_try_wait(mma_done, 0) && clock64() - t0 < kSpinLimit) {
       }
     }
+    __syncwarp();
   } else if (warp >= kWarpSf0 && warp < kWarpSf0 + 4) {
     // ------------------------------------------------------ scale writers --
     const int quarter = warp & 3;
@@ -455,18 +522,19 @@ moe_expert_gemm_mx(const __grid_constant__ CUtensorMap map_w,     // main codes
     const int m = quarter * 32 + lane;             // weight row of the tile = TMEM lane
     int q = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x, ++q) {
+      const bool gu = u < u_gu;
+      const ModeGeo& M = gu ? MG : MD;
       const int sbuf = q & 1;                      // TMEM scale set
       const bool ok = wait_phase(&sc_full[0], q & 1, abort_flag, a.status, a.wait_ns, 64, 6) &&
                       wait_phase(&sf_empty[sbuf], ((q >> 1) & 1) ^ 1, abort_flag, a.status, a.wait_ns, 64, 7);
       if (!__all_sync(0xffffffffu, ok)) break;
-      const uint8_t* buf = scb;
       const uint32_t ta = tmem_base + lane_addr + sfa_col0 + sbuf * 4 * G.groups;
       const uint32_t tb = tmem_base + lane_addr + sfb_col0 + sbuf * 4 * G.groups;
       // A: row m's word of group g in all four columns 4g..4g+3 (the MMA reads
       // column 4g + m / 32)
-      const uint8_t* ra = buf + m * G.nsb;
-      for (int g = 0; g < G.groups; ++g) {
-        const uint32_t wa = scale_word(ra, g, G.nsb);
+      const uint8_t* ra = scb + m * M.nsb;
+      for (int g = 0; g < M.groups; ++g) {
+        const uint32_t wa = scale_word(ra, g, M.nsb);
         ptx::tmem_st_32x32b_x4(ta + 4 * g, wa, wa, wa, wa);
       }
       // B: row n = lane of B at lane n of every lane quarter, column 4g
@@ -474,9 +542,9 @@ moe_expert_gemm_mx(const __grid_constant__ CUtensorMap map_w,     // main codes
       // n % 4 of the chunk (rows with n % 8 >= 4 are unused), whose scale row
       // of that term's table this lane reads from L2; h terms: row n is term
       // n / 8, scale 2^(h_exp - 4t) for every block.
-      const int t0 = lane / G.rpt;
-      if constexpr (kGateUp) {
-        const Unit w = unit_of(a, n_mt, u);
+      const int t0 = lane / M.rpt;
+      if (gu) {
+        const Unit w = unit_of(a, MG, MD, u_gu, u);
         const int jx = 4 * ((lane % 16) / 8) + (lane % 4);
         const int tk = __ldg(a.perm + w.r0 + (jx < w.n ? jx : 0)) / a.k;
         const uint32_t* srow =
@@ -485,13 +553,13 @@ moe_expert_gemm_mx(const __grid_constant__ CUtensorMap map_w,     // main codes
         uint32_t sw[kMaxGroups];
 #pragma unroll
         for (int g = 0; g < kMaxGroups; ++g)
-          if (g < G.groups) sw[g] = __ldg(srow + g);
+          if (g < MG.groups) sw[g] = __ldg(srow + g);
 #pragma unroll
         for (int g = 0; g < kMaxGroups; ++g)
-          if (g < G.groups) ptx::tmem_st_32x32b_x1(tb + 4 * g, sw[g]);
+          if (g < MG.groups) ptx::tmem_st_32x32b_x1(tb + 4 * g, sw[g]);
       } else {
         const uint32_t c0 = uint32_t(127 + a.h_exp - 4 * t0) * 0x01010101u;
-        for (int g = 0; g < G.groups; ++g) ptx::tmem_st_32x32b_x1(tb + 4 * g, c0);
+        for (int g = 0; g < MD.groups; ++g) ptx::tmem_st_32x32b_x1(tb + 4 * g, c0);
       }
       ptx::tmem_st_wait();
       ptx::tc_fence_before();
@@ -508,7 +576,7 @@ moe_expert_gemm_mx(const __grid_constant__ CUtensorMap map_w,     // main codes
     const float hscale = __int_as_float((127 - a.h_exp) << 23);   // 2^-h_exp
     int q = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x, ++q) {
-      const Unit w = unit_of(a, n_mt, u);
+      const Unit w = unit_of(a, MG, MD, u_gu, u);
       const int buf = q & 1;
       const bool ok0 = wait_phase(&acc_full[buf], (q >> 1) & 1, abort_flag, a.status, a.wait_ns, 256, 8);
       if (!ptx::group_all(1, 128, ok0)) break;
@@ -524,7 +592,7 @@ moe_expert_gemm_mx(const __grid_constant__ CUtensorMap map_w,     // main codes
         ptx::tmem_ld_wait();
 #pragma unroll
         for (int j = 0; j < kNB; ++j) {
-          if constexpr (kGateUp) {
+          if (w.gu) {
             const int c = 8 * (j / 4) + j % 4;
             z[j] = __uint_as_float(v[0][c]) + __uint_as_float(v[1][c]);
           } else {
@@ -536,7 +604,7 @@ moe_expert_gemm_mx(const __grid_constant__ CUtensorMap map_w,     // main codes
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&acc_empty[buf]);
-      if constexpr (kGateUp) {
+      if (w.gu) {
         const bool is_up = m >= kMW / 2;
         const int n = w.mt * (kMW / 2) + (m & (kMW / 2 - 1));
         const bool nvalid = n < a.W;
@@ -564,8 +632,11 @@ moe_expert_gemm_mx(const __grid_constant__ CUtensorMap map_w,     // main codes
               }
             }
           }
+          // the down units read these rows with TMA (the async proxy)
+          ptx::fence_proxy_async_global();
         }
-        ptx::named_barrier(3, 128);              // xch is reused by the next unit
+        ptx::named_barrier(3, 128);              // h stored; xch is reused by the next unit
+        if (m == 0) ptx::red_release_gpu_add(a.ready + w.g, 1);
       } else {
         const int n = w.mt * kMW + m;
         const bool nvalid = n < a.d;
@@ -621,18 +692,15 @@ cudaError_t make_map(CUtensorMap* map, CUtensorMapDataType dt, const void* base,
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <Mode M>
 int plan_stages(const GemmArgs& a) {
-  const Geo g0 = geometry<M>(a.d, a.W, a.nb, a.ld_sx, 0);
+  const Geo g0 = geometry(a.d, a.W, 0);
   const int per = g0.a_stage + g0.b_stage;
   int s = (kMaxSmem - 1024 - g0.total) / per;
   return s < kMaxStages ? s : kMaxStages;
 }
 
-// The four tensor maps of one launch.
-template <Mode M>
-cudaError_t make_maps(const GemmArgs& a, CUtensorMap* mw, CUtensorMap* mwt, CUtensorMap* mb) {
-  const bool gu = (M == Mode::GateUp);
+// The weight maps of one GEMM: the main map and the tail map.
+cudaError_t make_weight_maps(bool gu, const GemmArgs& a, CUtensorMap* mw, CUtensorMap* mwt) {
   const int K = gu ? a.d : a.W;
   const uint8_t* w = gu ? a.w_gu : a.w_dn;
   const long long rows = gu ? (long long)a.E * 2 * a.W : (long long)a.E * a.d;
@@ -640,29 +708,31 @@ cudaError_t make_maps(const GemmArgs& a, CUtensorMap* mw, CUtensorMap* mwt, CUte
   const int kmain = K / kBoxK * kBoxK;
   cudaError_t e = make_map(mw, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w, rows, kmain, K / 2, kBoxK,
                            box_rows);
-  if (e == cudaSuccess) {
-    if (K % kBoxK) {
-      // the last 128 codes of each row: base at code K - 128 of row 0
-      e = make_map(mwt, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w + (K - kBoxK) / 2, rows, kBoxK,
-                   K / 2, kBoxK, box_rows);
-    } else {
-      *mwt = *mw;
-    }
-  }
-  // B: gate_up's token tables [T, d] (a one-row box per gather4 coordinate),
-  // down's h term tables [R, W] (boxes of a chunk's 8 rows)
+  if (e != cudaSuccess) return e;
+  if (K % kBoxK)       // the last 128 codes of each row: base at code K - 128 of row 0
+    return make_map(mwt, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w + (K - kBoxK) / 2, rows, kBoxK,
+                    K / 2, kBoxK, box_rows);
+  *mwt = *mw;
+  return cudaSuccess;
+}
+
+// The ten tensor maps of one launch: gate_up and down weights (main, tail),
+// gate_up's token tables [T, d] (a one-row box per gather4 coordinate), down's
+// h term tables [R, W] (boxes of a chunk's 8 rows).
+cudaError_t make_maps(const GemmArgs& a, CUtensorMap* maps) {
+  cudaError_t e = make_weight_maps(true, a, &maps[0], &maps[1]);
+  if (e == cudaSuccess) e = make_weight_maps(false, a, &maps[2], &maps[3]);
   const long long T = a.R / a.k;
-  for (int t = 0; t < 4 && e == cudaSuccess; ++t) {
-    const uint8_t* base = gu ? ((t & 1) ? a.xq_lo : a.xq_hi) : a.hq + size_t(t) * a.R * a.W;
-    e = make_map(&mb[t], CU_TENSOR_MAP_DATA_TYPE_UINT8, base, gu ? T : a.R, K, K, kBoxK,
-                 gu ? 1 : a.nb);
-  }
+  for (int t = 0; t < 2 && e == cudaSuccess; ++t)
+    e = make_map(&maps[4 + t], CU_TENSOR_MAP_DATA_TYPE_UINT8, t ? a.xq_lo : a.xq_hi, T, a.d, a.d,
+                 kBoxK, 1);
+  for (int t = 0; t < kHTerms && e == cudaSuccess; ++t)
+    e = make_map(&maps[6 + t], CU_TENSOR_MAP_DATA_TYPE_UINT8, a.hq + size_t(t) * a.R * a.W, a.R,
+                 a.W, a.W, kBoxK, a.nb);
   return e;
 }
 
-template <Mode M>
-bool fits_mode(const GemmArgs& a) {
-  const bool gu = (M == Mode::GateUp);
+bool fits_mode(bool gu, const GemmArgs& a) {
   const int K = gu ? a.d : a.W;
   const int nsb = K / 32;
   if (K < kBoxK || K % 32 || (K / 2) % 16) return false;
@@ -676,53 +746,13 @@ bool fits_mode(const GemmArgs& a) {
   } else {
     if ((128 * nsb) % 16 || ((a.d % 128) * nsb) % 16) return false;
   }
-  return plan_stages<M>(a) >= 2;
+  return true;
 }
 
-template <Mode M>
-cudaError_t launch(const GemmArgs& a, cudaStream_t s) {
-  if (a.nb != kNB || !fits_mode<M>(a)) return cudaErrorInvalidConfiguration;
-  const int stages = plan_stages<M>(a);
-  const Geo g = geometry<M>(a.d, a.W, a.nb, a.ld_sx, stages);
-  const size_t smem = size_t(g.total) + 1024;
-  if (smem > size_t(kMaxSmem)) return cudaErrorInvalidConfiguration;
-  {
-    cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(moe_expert_gemm_mx<M>), kMaxSmem);
-    if (e != cudaSuccess) return e;
-  }
-  // the six maps, from the cache when this layer's buffers were seen before
-  struct Key {
-    const void* p[7];
-    int R, d, W, E, nb, k;
-  } key;
-  memset(&key, 0, sizeof(key));
-  key.p[0] = (M == Mode::GateUp) ? a.w_gu : a.w_dn;
-  key.p[1] = a.xq_hi;
-  key.p[2] = a.xq_lo;
-  key.p[3] = a.hq;
-  key.R = a.R;
-  key.d = a.d;
-  key.W = a.W;
-  key.E = a.E;
-  key.nb = a.nb;
-  key.k = a.k;
-  static MapCache<Key, 6> cache;
-  CUtensorMap maps[6];
-  if (!cache.find(key, maps)) {
-    cudaError_t e = make_maps<M>(a, &maps[0], &maps[1], &maps[2]);
-    if (e != cudaSuccess) return e;
-    cache.put(key, maps);
-  }
-  const CUtensorMap &mw = maps[0], &mwt = maps[1];
-  const CUtensorMap* mb = &maps[2];
-  const int n_out = (M == Mode::GateUp) ? a.W : a.d;
-  const int rows_per_tile = (M == Mode::GateUp) ? kMW / 2 : kMW;
-  const long long n_mt = (n_out + rows_per_tile - 1) / rows_per_tile;
-  const long long units_bound = (long long)(a.R / a.nb + a.E) * n_mt;
-  const int grid = int(units_bound < device_sm_count() ? units_bound : device_sm_count());
-  return launch_pdl(moe_expert_gemm_mx<M>, dim3(grid), dim3(kThreads), smem, s, mw, mwt, mb[0], mb[1],
-                    mb[2], mb[3], a, stages);
-}
+struct MapKey {
+  const void* p[5];
+  int R, d, W, E, nb, k;
+};
 
 }  // namespace
 
@@ -737,6 +767,8 @@ int mx_hidden_exp(float limit) {
   return e;
 }
 
+int mx_chunk_bound(int64_t R, int E) { return int(R / kNB + E + 1); }
+
 bool mx_fits(const GemmArgs& args, float limit) {
   // h is carried with a fixed scale, so the clamp must bound it, and tightly
   // enough that typical values stay far above the E4M3 subnormals
@@ -745,10 +777,68 @@ bool mx_fits(const GemmArgs& args, float limit) {
   a.nb = mx_chunk(a.R, a.E);
   if (a.R / (a.E > 0 ? a.E : 1) > 8) return false;              // a decode-sized load
   a.ld_sx = scale_row_bytes(a.d);
-  return fits_mode<Mode::GateUp>(a) && fits_mode<Mode::Down>(a);
+  return fits_mode(true, a) && fits_mode(false, a) && plan_stages(a) >= 2;
 }
 
-cudaError_t launch_gateup_mx(const GemmArgs& a, cudaStream_t s) { return launch<Mode::GateUp>(a, s); }
-cudaError_t launch_down_mx(const GemmArgs& a, cudaStream_t s) { return launch<Mode::Down>(a, s); }
+cudaError_t launch_experts_mx(const GemmArgs& a, cudaStream_t s) {
+  if (a.nb != kNB || !fits_mode(true, a) || !fits_mode(false, a) || !a.ready)
+    return cudaErrorInvalidConfiguration;
+  const int stages = plan_stages(a);
+  if (stages < 2) return cudaErrorInvalidConfiguration;
+  const Geo g = geometry(a.d, a.W, stages);
+  const size_t smem = size_t(g.total) + 1024;
+  if (smem > size_t(kMaxSmem)) return cudaErrorInvalidConfiguration;
+  {
+    cudaError_t e = set_smem_limit_once(reinterpret_cast<const void*>(moe_expert_mx), kMaxSmem);
+    if (e != cudaSuccess) return e;
+  }
+  // the ten maps, from the cache when this layer's buffers were seen before
+  MapKey key;
+  memset(&key, 0, sizeof(key));
+  key.p[0] = a.w_gu;
+  key.p[1] = a.w_dn;
+  key.p[2] = a.xq_hi;
+  key.p[3] = a.xq_lo;
+  key.p[4] = a.hq;
+  key.R = a.R;
+  key.d = a.d;
+  key.W = a.W;
+  key.E = a.E;
+  key.nb = a.nb;
+  key.k = a.k;
+  static MapCache<MapKey, 10> cache;
+  CUtensorMap m[10];
+  if (!cache.find(key, m)) {
+    cudaError_t e = make_maps(a, m);
+    if (e != cudaSuccess) return e;
+    cache.put(key, m);
+  }
+  const ModeGeo MG = mode_geo(true, a.d, a.W), MD = mode_geo(false, a.d, a.W);
+  const long long units_bound = (long long)(a.R / a.nb + a.E) * (MG.n_mt + MD.n_mt);
+  const int grid = int(units_bound < device_sm_count() ? units_bound : device_sm_count());
+  // CTAs wait on each other's gate_up units: all must be resident at once
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, moe_expert_mx, m[0], m[1], m[2], m[3], m[4], m[5], m[6],
+                                     m[7], m[8], m[9], a, stages);
+  if (e == cudaErrorInvalidValue || e == cudaErrorNotSupported) {
+    // a driver that does not combine the two attributes: cooperative alone
+    (void)cudaGetLastError();
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, moe_expert_mx, m[0], m[1], m[2], m[3], m[4], m[5], m[6], m[7],
+                           m[8], m[9], a, stages);
+  }
+  return e;
+}
 
 }  // namespace moe

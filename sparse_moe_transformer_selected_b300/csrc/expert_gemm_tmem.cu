@@ -465,6 +465,7 @@ moe_expert_gemm_tmem(const __grid_constant__ CUtensorMap map_w,
         s_in.drain(sc_full, 2);
       }
     }
+    __syncwarp();                 // the warp reaches the final barrier converged
   } else if (warp == kWarpProdB) {
     // --------------------------------------------- producer: activations --
     if (ptx::elect_one()) {
@@ -498,6 +499,7 @@ moe_expert_gemm_tmem(const __grid_constant__ CUtensorMap map_w,
       }
       if (!ok) b_in.drain(b_full, NBS);
     }
+    __syncwarp();
   } else if (warp == kWarpMMA) {
     // ------------------------------------------------------------ MMA issuer --
     // One thread's instruction stream sets the pace for short MMAs, so the
@@ -557,6 +559,7 @@ moe_expert_gemm_tmem(const __grid_constant__ CUtensorMap map_w,
       while (!ptx::mbar_try_wait(mma_done, 0) && clock64() - t0 < kSpinLimit) {
       }
     }
+    __syncwarp();
   } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + 4) {
     // ------------------------------------------------------------- epilogue --
     const int quarter = warp & 3;

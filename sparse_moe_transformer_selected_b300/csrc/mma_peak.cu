@@ -78,6 +78,7 @@ __global__ void __launch_bounds__(128, 1) mma_peak_kernel(int iters, int32_t* st
     }
     if (!ok) atomicMax(status, kStatusTimeout);
   }
+  __syncwarp();                   // warp 0 reaches the barrier converged
   ptx::tc_fence_before();
   __syncthreads();
   if (warp == 0) {

@@ -231,6 +231,9 @@ moe_status forward_impl(const void* x_bf16, int64_t T, int d, int W, const float
   a.nb = mx ? moe::mx_chunk(a.R, E) : moe::expert_gemm_tmem_chunk(a.R, E);
   moe::RouteArgs r = route_args(workspace, L, x_bf16, T, d, router_w, router_b, norm_w, eps, E,
                                 k, a.nb);
+  // the block-scaled design's per-chunk counts follow the combine counts and
+  // are zeroed with them
+  if (mx) r.ncnt += moe::mx_chunk_bound(a.R, E);
   int32_t* rowexp = at<int32_t>(workspace, L.rowexp);
   void* x_perm = nullptr;
   if (mx) {                                    // token tables of the E4M3 terms
@@ -269,6 +272,7 @@ moe_status forward_impl(const void* x_bf16, int64_t T, int d, int W, const float
   a.topk_w = r.topk_w;
   a.cnt = r.cnt;
   a.n_mt_dn = moe::down_col_tiles(d);
+  a.ready = mx ? r.cnt + T * a.n_mt_dn : nullptr;
   a.out = static_cast<__nv_bfloat16*>(out_bf16);
   a.resid = norm_w ? static_cast<const __nv_bfloat16*>(x_bf16) : nullptr;
   a.wait_ns = g_wait_ns;
@@ -282,12 +286,19 @@ moe_status forward_impl(const void* x_bf16, int64_t T, int d, int W, const float
     a.hq = at<uint8_t>(workspace, L.h_hi);
     a.h_exp = moe::mx_hidden_exp(limit);
   }
-  e = mx ? moe::launch_gateup_mx(a, s) : moe::launch_gateup_tmem(a, s);
-  if (e != cudaSuccess) return cuda_fail(e, "gate_up launch");
-  if ((e = trace(4, s)) != cudaSuccess) return cuda_fail(e, "trace event");
-  // K4 with K5 in its epilogue
-  e = mx ? moe::launch_down_mx(a, s) : moe::launch_down_tmem(a, s);
-  if (e != cudaSuccess) return cuda_fail(e, "down launch");
+  if (mx) {
+    // K3, K4 and K5 in one kernel: trace events 4 and 5 both follow it
+    e = moe::launch_experts_mx(a, s);
+    if (e != cudaSuccess) return cuda_fail(e, "expert kernel launch");
+    if ((e = trace(4, s)) != cudaSuccess) return cuda_fail(e, "trace event");
+  } else {
+    e = moe::launch_gateup_tmem(a, s);
+    if (e != cudaSuccess) return cuda_fail(e, "gate_up launch");
+    if ((e = trace(4, s)) != cudaSuccess) return cuda_fail(e, "trace event");
+    // K4 with K5 in its epilogue
+    e = moe::launch_down_tmem(a, s);
+    if (e != cudaSuccess) return cuda_fail(e, "down launch");
+  }
   if ((e = trace(5, s)) != cudaSuccess) return cuda_fail(e, "trace event");
   if ((e = trace(6, s)) != cudaSuccess) return cuda_fail(e, "trace event");
   return MOE_OK;
