@@ -11,9 +11,10 @@ namespace moe {
 // the programmatic-serialization attribute, so its launch and prologue overlap
 // the previous kernel's tail; each kernel calls pdl_wait() before its first
 // global-memory access (it returns once the previous kernel has completed and
-// its writes are visible).  Only kernels whose CTAs are all resident at once
-// (the persistent GEMMs) call pdl_trigger(), and only after their own
-// pdl_wait(); the others let the dependent launch when they exit.
+// its writes are visible).  A kernel that calls pdl_trigger() lets the next
+// one launch once every one of its CTAs has triggered or exited: the TMEM
+// design's gate_up does, after its own wait; the others let the next kernel
+// launch when they exit.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");

@@ -82,6 +82,7 @@ constexpr int kHTerms = 4;                    // E4M3 terms of h
 constexpr int kXTerms = 2;                    // E4M3 terms of x
 constexpr int kAccCols = 64;                  // TMEM columns per accumulator
 constexpr int kMaxStages = 8;
+constexpr int kMaxExperts = 256;
 constexpr int kThreads = 384;
 constexpr int kWarpProd = 0, kWarpMMA = 1, kWarpTmem = 2, kWarpEpi0 = 4, kWarpSf0 = 8;
 constexpr int kTmemCols = 512;
@@ -182,7 +183,7 @@ struct Geo {
   int groups;                // SF groups of the larger K (TMEM scale columns)
   int a_stage, b_stage;      // bytes per stage
   int stages;                // ring depth
-  int off_b, off_sc, off_xch, off_bars, off_comb, total;
+  int off_b, off_sc, off_xch, off_bars, off_comb, off_tab, total;
 };
 
 __host__ __device__ inline Geo geometry(int d, int W, int stages) {
@@ -204,6 +205,9 @@ __host__ __device__ inline Geo geometry(int d, int W, int stages) {
   off += kNumBars * 8 + 16;           // barriers, TMEM base, abort flag
   g.off_comb = off;
   off += combine_smem_bytes(kNB);
+  off = (off + 15) & ~15;
+  g.off_tab = off;
+  off += 2 * (kMaxExperts + 1) * 4;   // expert offsets and chunk prefix
   g.total = off;
   return g;
 }
@@ -214,27 +218,33 @@ struct Unit {
   bool gu;            // a gate_up unit (else down)
 };
 
-__device__ __forceinline__ int expert_of_chunk(const int32_t* mtile_off, int E, int g) {
+// The routing tables of the launch, copied into shared memory once.
+struct Tables {
+  const int32_t* off;   // [E + 1] first permuted row of each expert
+  const int32_t* mto;   // [E + 1] first chunk of each expert
+};
+
+__device__ __forceinline__ int expert_of_chunk(const int32_t* mto, int E, int g) {
   int lo = 0, hi = E;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (__ldg(mtile_off + mid) <= g) lo = mid; else hi = mid - 1;
+    if (mto[mid] <= g) lo = mid; else hi = mid - 1;
   }
   return lo;
 }
 
 // Unit u of the launch: gate_up units [0, u_gu), then down units.
-__device__ __forceinline__ Unit unit_of(const GemmArgs& a, const ModeGeo& MG, const ModeGeo& MD,
-                                        int u_gu, int u) {
+__device__ __forceinline__ Unit unit_of(const GemmArgs& a, const Tables& tb, const ModeGeo& MG,
+                                        const ModeGeo& MD, int u_gu, int u) {
   Unit w;
   w.gu = u < u_gu;
   const int n_mt = w.gu ? MG.n_mt : MD.n_mt;
   const int ul = w.gu ? u : u - u_gu;
   w.g = ul / n_mt;
   w.mt = ul - w.g * n_mt;
-  w.e = expert_of_chunk(a.mtile_off, a.E, w.g);
-  w.r0 = __ldg(a.offsets + w.e) + (w.g - __ldg(a.mtile_off + w.e)) * a.nb;
-  w.n = min(a.nb, __ldg(a.offsets + w.e + 1) - w.r0);
+  w.e = expert_of_chunk(tb.mto, a.E, w.g);
+  w.r0 = tb.off[w.e] + (w.g - tb.mto[w.e]) * a.nb;
+  w.n = min(a.nb, tb.off[w.e + 1] - w.r0);
   return w;
 }
 
@@ -338,7 +348,16 @@ moe_expert_mx(const __grid_constant__ CUtensorMap map_wg,     // gate_up codes, 
   const uint32_t sfa_col0 = 2 * kAccCols;
   const uint32_t sfb_col0 = 2 * kAccCols + 2 * 4 * G.groups;
   pdl_wait();
-  const int chunks = __ldg(a.mtile_off + a.E);
+  // the routing tables, once, for every role's unit lookups
+  int32_t* s_off = reinterpret_cast<int32_t*>(smem + G.off_tab);
+  int32_t* s_mto = s_off + kMaxExperts + 1;
+  for (int i = threadIdx.x; i <= a.E; i += kThreads) {
+    s_off[i] = __ldg(a.offsets + i);
+    s_mto[i] = __ldg(a.mtile_off + i);
+  }
+  __syncthreads();
+  const Tables tabs{s_off, s_mto};
+  const int chunks = s_mto[a.E];
   const int u_gu = chunks * MG.n_mt;
   const int units = u_gu + chunks * MD.n_mt;
 
@@ -369,7 +388,7 @@ moe_expert_mx(const __grid_constant__ CUtensorMap map_wg,     // gate_up codes, 
       // scale writers have emptied (they copy a unit's scales into TMEM during
       // the unit before it), so the MMA finds them in TMEM.
       auto load_scales = [&](int uu, int qq) -> bool {
-        const Unit w = unit_of(a, MG, MD, u_gu, uu);
+        const Unit w = unit_of(a, tabs, MG, MD, u_gu, uu);
         if (!wait_phase(&sc_empty[0], (qq & 1) ^ 1, abort_flag, a.status, a.wait_ns, 64, 5)) return false;
         int ra, rb, nrows;
         rows_of(w, ra, rb, nrows);
@@ -393,7 +412,7 @@ moe_expert_mx(const __grid_constant__ CUtensorMap map_wg,     // gate_up codes, 
       bool down_maps = false;
       int q = 0;
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++q) {
-        const Unit w = unit_of(a, MG, MD, u_gu, u);
+        const Unit w = unit_of(a, tabs, MG, MD, u_gu, u);
         const ModeGeo& M = w.gu ? MG : MD;
         int row_a, row_b, nrows;
         rows_of(w, row_a, row_b, nrows);
@@ -525,6 +544,24 @@ moe_expert_mx(const __grid_constant__ CUtensorMap map_wg,     // gate_up codes, 
       const bool gu = u < u_gu;
       const ModeGeo& M = gu ? MG : MD;
       const int sbuf = q & 1;                      // TMEM scale set
+      // B: row n = lane of B at lane n of every lane quarter, column 4g
+      // (N = 32).  x terms: row n is term n / 16, token 4 ((n % 16) / 8) +
+      // n % 4 of the chunk (rows with n % 8 >= 4 are unused), whose scale row
+      // of that term's table this lane reads from L2 (before the waits below,
+      // so these loads overlap the weight scales' copy); h terms: row n is
+      // term n / 8, scale 2^(h_exp - 4t) for every block.
+      const int t0 = lane / M.rpt;
+      uint32_t sw[kMaxGroups];
+      if (gu) {
+        const Unit w = unit_of(a, tabs, MG, MD, u_gu, u);
+        const int jx = 4 * ((lane % 16) / 8) + (lane % 4);
+        const int tk = __ldg(a.perm + w.r0 + (jx < w.n ? jx : 0)) / a.k;
+        const uint32_t* srow =
+            reinterpret_cast<const uint32_t*>((t0 ? a.sx_lo : a.sx_hi) + size_t(tk) * a.ld_sx);
+#pragma unroll
+        for (int g = 0; g < kMaxGroups; ++g)
+          if (g < MG.groups) sw[g] = __ldg(srow + g);
+      }
       const bool ok = wait_phase(&sc_full[0], q & 1, abort_flag, a.status, a.wait_ns, 64, 6) &&
                       wait_phase(&sf_empty[sbuf], ((q >> 1) & 1) ^ 1, abort_flag, a.status, a.wait_ns, 64, 7);
       if (!__all_sync(0xffffffffu, ok)) break;
@@ -537,23 +574,7 @@ moe_expert_mx(const __grid_constant__ CUtensorMap map_wg,     // gate_up codes, 
         const uint32_t wa = scale_word(ra, g, M.nsb);
         ptx::tmem_st_32x32b_x4(ta + 4 * g, wa, wa, wa, wa);
       }
-      // B: row n = lane of B at lane n of every lane quarter, column 4g
-      // (N = 32).  x terms: row n is term n / 16, token 4 ((n % 16) / 8) +
-      // n % 4 of the chunk (rows with n % 8 >= 4 are unused), whose scale row
-      // of that term's table this lane reads from L2; h terms: row n is term
-      // n / 8, scale 2^(h_exp - 4t) for every block.
-      const int t0 = lane / M.rpt;
       if (gu) {
-        const Unit w = unit_of(a, MG, MD, u_gu, u);
-        const int jx = 4 * ((lane % 16) / 8) + (lane % 4);
-        const int tk = __ldg(a.perm + w.r0 + (jx < w.n ? jx : 0)) / a.k;
-        const uint32_t* srow =
-            reinterpret_cast<const uint32_t*>((t0 ? a.sx_lo : a.sx_hi) + size_t(tk) * a.ld_sx);
-        // the row's scale words, all loads in flight before the first store
-        uint32_t sw[kMaxGroups];
-#pragma unroll
-        for (int g = 0; g < kMaxGroups; ++g)
-          if (g < MG.groups) sw[g] = __ldg(srow + g);
 #pragma unroll
         for (int g = 0; g < kMaxGroups; ++g)
           if (g < MG.groups) ptx::tmem_st_32x32b_x1(tb + 4 * g, sw[g]);
@@ -576,7 +597,7 @@ moe_expert_mx(const __grid_constant__ CUtensorMap map_wg,     // gate_up codes, 
     const float hscale = __int_as_float((127 - a.h_exp) << 23);   // 2^-h_exp
     int q = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x, ++q) {
-      const Unit w = unit_of(a, MG, MD, u_gu, u);
+      const Unit w = unit_of(a, tabs, MG, MD, u_gu, u);
       const int buf = q & 1;
       const bool ok0 = wait_phase(&acc_full[buf], (q >> 1) & 1, abort_flag, a.status, a.wait_ns, 256, 8);
       if (!ptx::group_all(1, 128, ok0)) break;
@@ -776,12 +797,13 @@ bool mx_fits(const GemmArgs& args, float limit) {
   GemmArgs a = args;
   a.nb = mx_chunk(a.R, a.E);
   if (a.R / (a.E > 0 ? a.E : 1) > 8) return false;              // a decode-sized load
+  if (a.E > kMaxExperts) return false;
   a.ld_sx = scale_row_bytes(a.d);
   return fits_mode(true, a) && fits_mode(false, a) && plan_stages(a) >= 2;
 }
 
 cudaError_t launch_experts_mx(const GemmArgs& a, cudaStream_t s) {
-  if (a.nb != kNB || !fits_mode(true, a) || !fits_mode(false, a) || !a.ready)
+  if (a.nb != kNB || a.E > kMaxExperts || !fits_mode(true, a) || !fits_mode(false, a) || !a.ready)
     return cudaErrorInvalidConfiguration;
   const int stages = plan_stages(a);
   if (stages < 2) return cudaErrorInvalidConfiguration;

@@ -370,43 +370,38 @@ router_topk_kernel(const RouteArgs r, int nks, bool quantize, int32_t* __restric
   __syncthreads();
 
   // top-k of token `warp`: k rounds of a warp-wide (logit desc, index asc)
-  // maximum over the experts not yet taken; lane j keeps slot j
+  // maximum over the experts not yet taken; lane j keeps slot j.  A logit is
+  // compared through an order-preserving unsigned key (NaN as -inf, -0 as +0,
+  // taken experts as key 0, below every logit), so a round is one warp max of
+  // the keys and one warp min of the indices holding that key.
   if (warp < ntok) {
     const int tl = warp, t = t0 + tl;
-    float v[NPER];
+    uint32_t key[NPER];
 #pragma unroll
     for (int j = 0; j < NPER; ++j) {
       const int e = lane + 32 * j;
-      const float lv = (e < E) ? wl[tl * kLgStride + e] : -INFINITY;
-      v[j] = isnan(lv) ? -INFINITY : lv;
+      float lv = (e < E) ? wl[tl * kLgStride + e] : -INFINITY;
+      lv = isnan(lv) ? -INFINITY : lv + 0.0f;
+      const uint32_t u = __float_as_uint(lv);
+      key[j] = (e < E) ? ((u & 0x80000000u) ? ~u : (u | 0x80000000u)) : 0u;
     }
-    uint32_t taken = 0;
     int my_e = 0;
     float my_l = -INFINITY;
     for (int j = 0; j < k; ++j) {
-      float bv = -INFINITY;
-      int be = 0x7fffffff;
+      uint32_t bk = 0u, be = 0xFFFFFFFFu;        // this lane's best (lowest expert on ties)
 #pragma unroll
-      for (int q = 0; q < NPER; ++q) {
-        const int e = lane + 32 * q;
-        if (e < E && !((taken >> q) & 1u) && (v[q] > bv || (v[q] == bv && e < be))) {
-          bv = v[q];
-          be = e;
-        }
-      }
+      for (int q = 0; q < NPER; ++q)
+        if (key[q] > bk) { bk = key[q]; be = uint32_t(lane + 32 * q); }
+      const uint32_t kmax = __reduce_max_sync(0xffffffffu, bk);
+      const uint32_t emin = __reduce_min_sync(0xffffffffu, bk == kmax ? be : 0xFFFFFFFFu);
+      if ((emin & 31u) == uint32_t(lane)) {
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-        if (ov > bv || (ov == bv && oe < be)) {
-          bv = ov;
-          be = oe;
-        }
+        for (int q = 0; q < NPER; ++q)
+          if (q == int(emin >> 5)) key[q] = 0u;
       }
-      if ((be & 31) == lane) taken |= 1u << (be >> 5);
       if (lane == j) {
-        my_e = be;
-        my_l = bv;
+        my_e = int(emin);
+        my_l = __uint_as_float((kmax & 0x80000000u) ? (kmax & 0x7FFFFFFFu) : ~kmax);
       }
     }
     // softmax over the k selected logits: exp(l_j - l_0), summed in slot order
