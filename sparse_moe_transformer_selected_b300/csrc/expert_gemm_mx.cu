@@ -40,11 +40,16 @@
 // MMA picks the byte with the descriptor's scale-factor ID).
 //
 // One persistent kernel runs both GEMMs, one CTA per SM, 12 warps:
-//   warp 0      producer: per unit the weight scale rows (1-D bulk copies),
-//               per stage A and B (TMA); one ring of stages of 256 K
+//   warp 0      producer: per stage A and B (TMA); one ring of stages of 256 K
 //   warp 1      MMA issuer (one elected thread)
 //   warp 2      TMEM allocator: 512 columns (2 accumulators of 64, then two
 //               sets of A and B scale columns)
+//   warp 3      unit scheduler (one elected thread): decodes this CTA's next
+//               unit (routing tables, the chunk's token indices; for a down
+//               unit, the wait for its chunk's h), hands it to the producer
+//               through a two-entry queue in shared memory, and copies its
+//               weight scale rows; so the producer issues stages only, never
+//               stalled on a global load
 //   warps 4-7   epilogue, TMEM lane quarter = warp % 4
 //   warps 8-11  scale writers, TMEM lane quarter = warp % 4 (gate_up's
 //               activation scales read from L2, one token row per lane)
@@ -84,14 +89,14 @@ constexpr int kAccCols = 64;                  // TMEM columns per accumulator
 constexpr int kMaxStages = 8;
 constexpr int kMaxExperts = 256;
 constexpr int kThreads = 384;
-constexpr int kWarpProd = 0, kWarpMMA = 1, kWarpTmem = 2, kWarpEpi0 = 4, kWarpSf0 = 8;
+constexpr int kWarpProd = 0, kWarpMMA = 1, kWarpTmem = 2, kWarpSched = 3, kWarpEpi0 = 4, kWarpSf0 = 8;
 constexpr int kTmemCols = 512;
 constexpr int kMaxGroups = (kTmemCols - 2 * kAccCols) / 16;   // SF groups (4 K blocks each)
 constexpr long long kSpinLimit = 4000000000ll;   // clock cycles: the final drains
 constexpr int kMaxSmem = 232448;
 // stage ring (full + empty), scales (2 + 2), scale columns (2 + 2),
-// accumulators (2 + 2), final drain
-constexpr int kNumBars = 2 * kMaxStages + 4 + 4 + 4 + 1;
+// accumulators (2 + 2), final drain, unit queue (2 + 2)
+constexpr int kNumBars = 2 * kMaxStages + 4 + 4 + 4 + 1 + 4;
 
 // Bounded wait: true when the phase completed; false after limit_ns
 // nanoseconds (code in status[0], the waiting role's tag in status[4]) or when
@@ -178,12 +183,20 @@ __host__ __device__ inline ModeGeo mode_geo(bool gate_up, int d, int W) {
   return g;
 }
 
+// A unit as the scheduler warp hands it to the producer.
+struct UnitInfo {
+  int gu;                    // gate_up (else down)
+  int row_a, row_b;          // first weight rows of the two A boxes (gate, up) or of the one
+  int r0;                    // first permuted row of the chunk
+  int tok[kNB];              // gate_up: the chunk's tokens (rows past it repeat its first)
+};
+
 // Shared-memory plan of the launch (both GEMMs share the ring).
 struct Geo {
   int groups;                // SF groups of the larger K (TMEM scale columns)
   int a_stage, b_stage;      // bytes per stage
   int stages;                // ring depth
-  int off_b, off_sc, off_xch, off_bars, off_comb, off_tab, total;
+  int off_b, off_sc, off_xch, off_bars, off_comb, off_info, off_tab, total;
 };
 
 __host__ __device__ inline Geo geometry(int d, int W, int stages) {
@@ -205,6 +218,9 @@ __host__ __device__ inline Geo geometry(int d, int W, int stages) {
   off += kNumBars * 8 + 16;           // barriers, TMEM base, abort flag
   g.off_comb = off;
   off += combine_smem_bytes(kNB);
+  off = (off + 15) & ~15;
+  g.off_info = off;
+  off += 2 * int(sizeof(UnitInfo));
   off = (off + 15) & ~15;
   g.off_tab = off;
   off += 2 * (kMaxExperts + 1) * 4;   // expert offsets and chunk prefix
@@ -313,6 +329,9 @@ moe_expert_mx(const __grid_constant__ CUtensorMap map_wg,     // gate_up codes, 
   uint64_t* acc_full = sf_empty + 2;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* mma_done = acc_empty + 2;
+  uint64_t* info_full = mma_done + 1;
+  uint64_t* info_empty = info_full + 2;
+  UnitInfo* info = reinterpret_cast<UnitInfo*>(smem + G.off_info);
   uint32_t* tmem_base_p = reinterpret_cast<uint32_t*>(smem + G.off_bars + kNumBars * 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + G.off_bars + kNumBars * 8 + 4);
   uint8_t* comb = smem + G.off_comb;             // combine lists (down units)
@@ -331,6 +350,8 @@ moe_expert_mx(const __grid_constant__ CUtensorMap map_wg,     // gate_up codes, 
       ptx::mbar_init(&sf_empty[s], 1);
       ptx::mbar_init(&acc_full[s], 1);
       ptx::mbar_init(&acc_empty[s], 4);
+      ptx::mbar_init(&info_full[s], 1);
+      ptx::mbar_init(&info_empty[s], 1);
     }
     ptx::mbar_init(mma_done, 1);
     *abort_flag = 0;
@@ -361,42 +382,54 @@ moe_expert_mx(const __grid_constant__ CUtensorMap map_wg,     // gate_up codes, 
   const int u_gu = chunks * MG.n_mt;
   const int units = u_gu + chunks * MD.n_mt;
 
-  if (warp == kWarpProd) {
-    // ------------------------------------------------------------ producer --
+  // weight rows of a unit: gate and up halves (gate_up) or one block (down)
+  auto rows_of = [&](const Unit& w, int& ra, int& rb, int& nrows) {
+    if (w.gu) {
+      const int n0 = w.mt * (kMW / 2);
+      nrows = min(kMW / 2, a.W - n0);
+      ra = w.e * MG.rpe + n0;
+      rb = w.e * MG.rpe + a.W + n0;
+    } else {
+      const int m0 = w.mt * kMW;
+      nrows = min(kMW, a.d - m0);
+      ra = w.e * MD.rpe + m0;
+      rb = ra;
+    }
+  };
+
+  if (warp == kWarpSched) {
+    // ------------------------------------------------------- unit scheduler --
     if (ptx::elect_one() && a.inject != 1) {
-      ptx::tma_prefetch_desc(&map_wg);
-      ptx::tma_prefetch_desc(&map_x0);
-      ptx::tma_prefetch_desc(&map_x1);
-      Ring st;
-      Inflight in_st, in_sc;
-      // weight rows of a unit: gate and up halves (gate_up) or one block (down)
-      auto rows_of = [&](const Unit& w, int& ra, int& rb, int& nrows) {
-        if (w.gu) {
-          const int n0 = w.mt * (kMW / 2);
-          nrows = min(kMW / 2, a.W - n0);
-          ra = w.e * MG.rpe + n0;
-          rb = w.e * MG.rpe + a.W + n0;
-        } else {
-          const int m0 = w.mt * kMW;
-          nrows = min(kMW, a.d - m0);
-          ra = w.e * MD.rpe + m0;
-          rb = ra;
-        }
-      };
-      // The scale rows of unit number qq (its index in this CTA's sequence)
-      // are loaded while unit qq - 1 streams, into the one staging buffer the
-      // scale writers have emptied (they copy a unit's scales into TMEM during
-      // the unit before it), so the MMA finds them in TMEM.
-      auto load_scales = [&](int uu, int qq) -> bool {
-        const Unit w = unit_of(a, tabs, MG, MD, u_gu, uu);
-        if (!wait_phase(&sc_empty[0], (qq & 1) ^ 1, abort_flag, a.status, a.wait_ns, 64, 5)) return false;
+      Inflight in_sc;
+      bool ok = true;
+      int q = 0;
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++q) {
+        const Unit w = unit_of(a, tabs, MG, MD, u_gu, u);
         int ra, rb, nrows;
         rows_of(w, ra, rb, nrows);
+        UnitInfo& inf = info[q & 1];
+        if (!wait_phase(&info_empty[q & 1], ((q >> 1) & 1) ^ 1, abort_flag, a.status, a.wait_ns, 64, 10)) { ok = false; break; }
+        inf.gu = w.gu;
+        inf.row_a = ra;
+        inf.row_b = rb;
+        inf.r0 = w.r0;
+        if (w.gu) {
+#pragma unroll
+          for (int j = 0; j < kNB; ++j) inf.tok[j] = __ldg(a.perm + w.r0 + (j < w.n ? j : 0)) / a.k;
+        } else {
+          // every gate_up tile of this chunk has stored its h rows
+          if (!wait_count(a.ready + w.g, MG.n_mt, abort_flag, a.status, a.wait_ns, 9)) { ok = false; break; }
+          ptx::fence_proxy_async_global();
+        }
+        ptx::mbar_arrive(&info_full[q & 1]);
+        // the unit's weight scale rows, into the staging buffer once the
+        // scale writers have copied the previous unit's into TMEM (the
+        // activations' scales are read by the writers)
+        if (!wait_phase(&sc_empty[0], (q & 1) ^ 1, abort_flag, a.status, a.wait_ns, 64, 5)) { ok = false; break; }
         const int nsb = w.gu ? MG.nsb : MD.nsb;
         const uint8_t* wscale = w.gu ? a.w_gu_scale : a.w_dn_scale;
         const uint32_t bytes = uint32_t(nrows * nsb);
         if (w.gu) {
-          // the weight scale rows (the activations' are read by the writers)
           ptx::mbar_arrive_expect_tx(&sc_full[0], 2 * bytes);
           ptx::bulk_load(scb, wscale + size_t(ra) * nsb, bytes, &sc_full[0]);
           ptx::bulk_load(scb + (kMW / 2) * nsb, wscale + size_t(rb) * nsb, bytes, &sc_full[0]);
@@ -404,44 +437,49 @@ moe_expert_mx(const __grid_constant__ CUtensorMap map_wg,     // gate_up codes, 
           ptx::mbar_arrive_expect_tx(&sc_full[0], bytes);
           ptx::bulk_load(scb, wscale + size_t(ra) * nsb, bytes, &sc_full[0]);
         }
-        in_sc.mark(0, qq & 1);
-        return true;
-      };
+        in_sc.mark(0, q & 1);
+      }
+      if (!ok) in_sc.drain(sc_full, 1);
+    }
+    __syncwarp();                 // the warp reaches the final barrier converged
+  } else if (warp == kWarpProd) {
+    // ------------------------------------------------------------ producer --
+    if (ptx::elect_one() && a.inject != 1) {
+      ptx::tma_prefetch_desc(&map_wg);
+      ptx::tma_prefetch_desc(&map_x0);
+      ptx::tma_prefetch_desc(&map_x1);
+      Ring st;
+      Inflight in_st;
       const CUtensorMap* mh[4] = {&map_h0, &map_h1, &map_h2, &map_h3};
-      bool ok = blockIdx.x >= units || load_scales(blockIdx.x, 0);
+      bool ok = true;
       bool down_maps = false;
       int q = 0;
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++q) {
-        const Unit w = unit_of(a, tabs, MG, MD, u_gu, u);
-        const ModeGeo& M = w.gu ? MG : MD;
-        int row_a, row_b, nrows;
-        rows_of(w, row_a, row_b, nrows);
-        // gate_up: the chunk's tokens (rows past the chunk repeat its first)
+        if (!wait_phase(&info_full[q & 1], (q >> 1) & 1, abort_flag, a.status, a.wait_ns, 0, 11)) { ok = false; break; }
+        const UnitInfo& inf = info[q & 1];
+        const bool gu = inf.gu != 0;
+        const int row_a = inf.row_a, row_b = inf.row_b, r0 = inf.r0;
         int tok[kNB];
-        if (w.gu) {
 #pragma unroll
-          for (int j = 0; j < kNB; ++j) tok[j] = __ldg(a.perm + w.r0 + (j < w.n ? j : 0)) / a.k;
-        } else {
+        for (int j = 0; j < kNB; ++j) tok[j] = inf.tok[j];
+        ptx::mbar_arrive(&info_empty[q & 1]);
+        const ModeGeo& M = gu ? MG : MD;
+        if (!gu) {
           if (!down_maps) {
             ptx::tma_prefetch_desc(&map_wd);
             for (int t = 0; t < kHTerms; ++t) ptx::tma_prefetch_desc(mh[t]);
             down_maps = true;
           }
-          // every gate_up tile of this chunk has stored its h rows
-          if (!wait_count(a.ready + w.g, MG.n_mt, abort_flag, a.status, a.wait_ns, 9)) { ok = false; break; }
-          ptx::fence_proxy_async_global();
+          ptx::fence_proxy_async_global();     // h rows of other CTAs, read by TMA
         }
-        const CUtensorMap* mw = w.gu ? &map_wg : &map_wd;
-        const CUtensorMap* mwt = w.gu ? &map_wgt : &map_wdt;
+        const CUtensorMap* mw = gu ? &map_wg : &map_wd;
+        const CUtensorMap* mwt = gu ? &map_wgt : &map_wdt;
         for (int s = 0; s < M.nstage; ++s) {
-          // the next unit's scales, once this unit's first stages are out
-          if (s == min(1, M.nstage - 1) && u + int(gridDim.x) < units &&
-              !load_scales(u + int(gridDim.x), q + 1)) { ok = false; break; }
           if (!wait_phase(&empty[st.slot], st.phase ^ 1, abort_flag, a.status, a.wait_ns, 64, 4)) { ok = false; break; }
           const int i0 = 2 * s, i1 = min(2 * s + 2, M.nbox);
           // the 4-bit TMA counts the packed bytes it reads (half of what it
           // writes); gate_up's B is two gathers of 4 rows per term
-          const uint32_t b_box = w.gu ? uint32_t(MG.NT * 2 * 4 * kBoxK) : uint32_t(kBRows * kBoxK);
+          const uint32_t b_box = gu ? uint32_t(MG.NT * 2 * 4 * kBoxK) : uint32_t(kBRows * kBoxK);
           ptx::mbar_arrive_expect_tx(&full[st.slot], uint32_t(i1 - i0) * (kBoxBytesA / 2 + b_box));
           uint8_t* da = sa + st.slot * G.a_stage;
           uint8_t* db = sb + st.slot * G.b_stage;
@@ -453,7 +491,7 @@ moe_expert_mx(const __grid_constant__ CUtensorMap map_wg,     // gate_up codes, 
             const int xa = main_box ? i * kBoxK : 0;
             const int xb = i * kBoxK;
             ptx::tma_load_2d(dai, mwi, &full[st.slot], xa, row_a);
-            if (w.gu) {
+            if (gu) {
               ptx::tma_load_2d(dai + (kMW / 2) * kBoxK, mwi, &full[st.slot], xa, row_b);
               for (int t = 0; t < MG.NT; ++t) {
                 const CUtensorMap* mb = t ? &map_x1 : &map_x0;
@@ -464,17 +502,14 @@ moe_expert_mx(const __grid_constant__ CUtensorMap map_wg,     // gate_up codes, 
               }
             } else {
               for (int t = 0; t < MD.NT; ++t)
-                ptx::tma_load_2d(dbi + t * MD.rpt * kBoxK, mh[t], &full[st.slot], xb, w.r0);
+                ptx::tma_load_2d(dbi + t * MD.rpt * kBoxK, mh[t], &full[st.slot], xb, r0);
             }
           }
           in_st.mark(st.slot, st.phase);
           st.next(S);
         }
       }
-      if (!ok) {
-        in_st.drain(full, S);
-        in_sc.drain(sc_full, 1);
-      }
+      if (!ok) in_st.drain(full, S);
     }
     __syncwarp();                 // the warp reaches the final barrier converged
   } else if (warp == kWarpMMA) {
