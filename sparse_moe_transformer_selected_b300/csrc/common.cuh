@@ -71,9 +71,15 @@ inline int router_split_len(int64_t T, int d, int E) {
   if (len < 256) len = 256;
   return int(len < d ? len : (d + 31) / 32 * 32);
 }
+// The tensor-core logits kernel (router_tc.cu): more than 8 router tiles,
+// d a multiple of 64.  It cuts d into at most kRouterTcMaxSplits ranges.
+constexpr int kRouterTcMaxSplits = 8;
+bool router_tc_fits(int64_t T, int d, int E);
+int router_tc_e_pad(int E);
 inline int router_splits(int64_t T, int d, int E) {
   // at most 8 router tiles: whole dot products, one slab (router_topk.cu)
   if ((T + kRouterTile - 1) / kRouterTile <= 8) return 1;
+  if (router_tc_fits(T, d, E)) return kRouterTcMaxSplits;   // slabs reserved; the launch uses <=
   const int len = router_split_len(T, d, E);
   return (d + len - 1) / len;
 }
@@ -106,6 +112,7 @@ struct Workspace {
                       // then int32[T k / 8 + E + 1]: per token chunk of 8 rows, the gate_up
                       // tiles whose h is stored (block-scaled design)
   size_t rnorm;        // float[T]  1/rms of each token (the block's RMSNorm)
+  size_t rw_terms;     // bf16[3, E_pad, d] the router weights as hi, mid, lo (tensor-core router)
   // The block's MoE input bf16(RMSNorm(x)) [T, d] lives at the start of the y
   // region: it is read only by the routing stages, before K4 writes y.
   size_t total;
@@ -150,6 +157,7 @@ inline Workspace workspace_layout(int64_t T, int d, int W, int E, int k) {
   ws.sx_lo = take(size_t(T) * scale_row_bytes(d));
   ws.cnt = take((size_t(T) * down_col_tiles(d) + size_t(R) / 8 + E + 1) * 4);
   ws.rnorm = take(size_t(T) * 4);
+  ws.rw_terms = take(router_tc_fits(T, d, E) ? size_t(3) * router_tc_e_pad(E) * d * 2 : 0);
   ws.total = off;
   return ws;
 }
@@ -194,6 +202,7 @@ struct RouteArgs {
   // (null: left to the scatter kernel)
   int32_t* perm;
   int32_t* inv;
+  __nv_bfloat16* rw_terms;     // [3, E_pad, d] workspace of the tensor-core router
 };
 
 // bf16 (nearest, ties to even) of x·g·r for a bf16 value x, an fp32 g and
@@ -222,6 +231,10 @@ __device__ __forceinline__ float rms_scaled_bf16(float x, float g, float r32, do
 // Otherwise the caller launches the scan and the scatter.  With r.xq_hi the
 // token tables of the block-scaled design are written too.
 cudaError_t launch_router_topk(const RouteArgs& r, bool* scanned, cudaStream_t s);
+// K1's logits on the tensor cores (router_tc.cu), when router_tc_fits: the
+// weight split, then the partial-logit slabs; *nks = the slabs written.
+int router_tc_splits(int64_t T, int d, int E, int* k_len);
+cudaError_t launch_router_logits_tc(const RouteArgs& r, int* nks, cudaStream_t s);
 
 // K2a: expert offsets, per-(tile, expert) bases, prefix of chunks of `chunk` rows.
 cudaError_t launch_route_scan(const int32_t* tile_counts, int ntiles, int E, int chunk,

@@ -152,6 +152,7 @@ moe::RouteArgs route_args(void* ws, const moe::Workspace& L, const void* x, int6
   r.ncnt = T * moe::down_col_tiles(d);
   r.perm = at<int32_t>(ws, L.perm);
   r.inv = at<int32_t>(ws, L.inv);
+  r.rw_terms = moe::router_tc_fits(T, d, E) ? at<__nv_bfloat16>(ws, L.rw_terms) : nullptr;
   return r;
 }
 

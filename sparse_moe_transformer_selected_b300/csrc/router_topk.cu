@@ -504,7 +504,8 @@ cudaError_t launch_router_topk(const RouteArgs& r, bool* scanned, cudaStream_t s
   const int T = r.T, d = r.d, E = r.E;
   const int ntiles = (T + kTT - 1) / kTT;
   const bool rows = ntiles <= kFuseScanTiles;   // decode-sized: whole dot products
-  const int nks = rows ? 1 : router_splits(T, d, E);
+  const bool tc = !rows && router_tc_fits(T, d, E) && r.rw_terms != nullptr;
+  int nks = rows ? 1 : router_splits(T, d, E);
   const int kc = router_split_len(T, d, E);
   const int eg = router_expert_group(T, E);
   const dim3 g1(ntiles, nks, (E + eg - 1) / eg);
@@ -524,7 +525,8 @@ cudaError_t launch_router_topk(const RouteArgs& r, bool* scanned, cudaStream_t s
   case N:                                                                                    \
     e = launch_pdl(router_logits_kernel<N>, g1, dim3(kThreads), 0, s, r, kc, eg);             \
     break;
-  switch (rows ? 0 : nper_g) {
+  if (tc) e = launch_router_logits_tc(r, &nks, s);
+  switch (rows || tc ? 0 : nper_g) {
     MOE_LOGITS_CASE(1)
     MOE_LOGITS_CASE(2)
     MOE_LOGITS_CASE(3)
