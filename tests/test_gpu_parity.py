@@ -146,6 +146,9 @@ EDGE = {
     "E256": gen.Workload("E256", T=300, d=64, W=64, E=256, router_bias="normal", seed=10),
     "rows_over_tile": gen.Workload("rows_over_tile", T=600, d=256, W=256, E=4, k=2,
                                    router_bias="normal", seed=11),
+    # more than 8 router tiles with d not a multiple of 64: the CUDA-core
+    # split-K logits kernel instead of the tensor-core one
+    "split_d96": gen.Workload("split_d96", T=300, d=96, W=64, E=8, router_bias="normal", seed=13),
 }
 
 
