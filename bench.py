@@ -200,7 +200,7 @@ def kernel_traffic(kernel: str, workload: str, mx: bool = False):
     return None
 
 
-def roofline(wl, counts, stage_ms, step_ms, mx, peaks, peak_src):
+def roofline(wl, counts, stage_ms, step_ms, mx, peaks, peak_src, mma_peaks=None):
     """The dominant kernel against its roofline: HBM bytes when its flop/byte is
     under the ridge point, else tensor flops against the dense peak of the MMA
     kind it issues (kind::f16: bf16's; burst for steps under a second)."""
@@ -221,6 +221,13 @@ def roofline(wl, counts, stage_ms, step_ms, mx, peaks, peak_src):
                 "unit": "TFLOP/s"}
         note = (f"dense bf16 / kind::f16 {'sustained' if sustained else 'burst'} ({peak_src})")
     roof["frac"] = roof["achieved"] / roof["peak"]
+    if roof["bound"] == "tensor" and not mx and mma_peaks and mma_peaks.get("f16_tmem_a_n128"):
+        # the rate of the instruction form the TMEM design issues (kind::f16,
+        # A in tensor memory, N = 128) on this GPU: down issues two MMAs (h hi,
+        # h lo) per K step, gate_up one
+        issued = roof["achieved"] * (2.0 if top == "down_combine" else 1.0)
+        roof["form_peak_tflops"] = mma_peaks["f16_tmem_a_n128"]
+        roof["frac_of_form_peak"] = issued / mma_peaks["f16_tmem_a_n128"]
     roof["traffic"] = kernel_traffic(top, wl.name, mx)
     roof["kernel_source"] = kernel_source(top, mx)
     roof["kernel"] = top
@@ -452,7 +459,7 @@ def run_ours(args, wl):
     # forms (moe_mma_peak): the denominators a block-scaled kernel is held to
     status_ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
     mma_peaks = {kind: round(moe.moe_mma_peak(kind, 20000, status_ws), 1)
-                 for kind in ("f16", "mxf8f6f4")}
+                 for kind in ("f16", "mxf8f6f4", "f16_tmem_a_n128", "f16_tmem_a_n256")}
     moe.moe_poll_status(status_ws)
 
     with ClockSampler(local_rank) as clk:
@@ -460,7 +467,8 @@ def run_ours(args, wl):
     ms, e2e, e2e_graph = max_over_ranks([main["ms"], main["e2e_ms"], main["e2e_graph_ms"]], world,
                                         device="cuda")
     peaks, peak_src = load_peaks()
-    roof, active = roofline(wl, main["counts"], main["stage_ms"], ms, main["mx"], peaks, peak_src)
+    roof, active = roofline(wl, main["counts"], main["stage_ms"], ms, main["mx"], peaks, peak_src,
+                            mma_peaks)
     inp_main = None if args.no_cpu_baseline or world > 1 else gen.make_inputs(wl)
     del main["dev"]
 
@@ -473,12 +481,15 @@ def run_ours(args, wl):
             r = measure(owl, args.other_steps, 3, world, flush_l2, with_e2e=False)
             del r["dev"]
             oms = max_over_ranks([r["ms"]], world, device="cuda")[0]
-            oroof, oact = roofline(owl, r["counts"], r["stage_ms"], oms, r["mx"], peaks, peak_src)
+            oroof, oact = roofline(owl, r["counts"], r["stage_ms"], oms, r["mx"], peaks, peak_src,
+                                   mma_peaks)
             others[name] = {
                 "tokens_per_s": whole_job_tokens_per_s(owl.T, world, oms), "ms_per_step": oms,
                 "steps": args.other_steps, "design": "block-scaled" if r["mx"] else "tmem f16",
                 "roofline": {k_: oroof[k_] for k_ in ("bound", "kernel", "achieved", "unit",
-                                                      "peak", "frac", "peak_source")},
+                                                      "peak", "frac", "peak_source",
+                                                      "form_peak_tflops", "frac_of_form_peak")
+                             if k_ in oroof},
                 "stages_ms": {k_: round(v, 5) for k_, v in r["stage_ms"].items() if k_ != "_end"},
                 "active_experts": oact}
             torch.cuda.empty_cache()
@@ -507,7 +518,9 @@ def run_ours(args, wl):
         "roofline": roof,
         "stages_ms": {k_: round(v, 5) for k_, v in main["stage_ms"].items() if k_ != "_end"},
         "active_experts": active,
-        "mma_peaks_tflops": {**mma_peaks, "how": "moe_mma_peak: 128x256 MMAs from shared memory, "
+        "mma_peaks_tflops": {**mma_peaks, "how": "moe_mma_peak: back-to-back K-steps of each "
+                                                 "instruction form (f16 and mxf8f6f4: 128x256 from "
+                                                 "shared memory; f16_tmem_a: A in tensor memory), "
                                                  "one CTA per SM, CUDA events (this run)"},
     }
     if others:

@@ -264,12 +264,15 @@ moe_status moe_debug_combine(const float* y, const int32_t* perm, const int32_t*
                              void* workspace, size_t workspace_bytes, void* stream);
 
 /*
- * Measurement aid: the dense rate, in TFLOP/s, of the tensor-core MMA kind the
- * grouped GEMMs issue, with their instruction forms and tile shape (M = 128,
- * N = 256, operands in shared memory, fp32 accumulators in tensor memory):
- *   kind 0   tcgen05.mma kind::f16 on bf16 operands (the TMEM design)
+ * Measurement aid: the dense rate, in TFLOP/s, of the tensor-core MMA forms
+ * the grouped GEMMs issue (M = 128, fp32 accumulators in tensor memory):
+ *   kind 0   tcgen05.mma kind::f16 on bf16 operands in shared memory, N = 256
  *   kind 1   tcgen05.mma kind::mxf8f6f4.block_scale, E2M1 x E4M3 with UE8M0
- *            scales (the block-scaled design)
+ *            scales, operands in shared memory, N = 256 (the block-scaled
+ *            design's kind)
+ *   kind 2   kind::f16 with A read from tensor memory, N = 128 (the TMEM
+ *            design's form at 128-token chunks)
+ *   kind 3   kind::f16 with A read from tensor memory, N = 256
  * One CTA per SM issues iters x 4 MMAs back to back; the launch is timed with
  * CUDA events on `stream` (synchronises it).  workspace: 4 bytes of device
  * memory for a status word.  Returns MOE_ERR_SHAPE for another kind or iters

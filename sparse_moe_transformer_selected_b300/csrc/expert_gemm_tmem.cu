@@ -87,9 +87,13 @@ constexpr long long kSpinLimit = 4000000000ll;   // clock cycles: the final drai
 constexpr int kMaxSmem = 232448;                 // 227 KB opt-in per CTA
 
 // K of one activation stage: 256 for small chunks (a stage is a few KB and
-// one wait covers a whole A stage), 64 for large ones (a stage of 128 tokens x
-// 256 K would not leave room for a ring).
-__host__ __device__ inline int act_stage_k(int nb) { return nb <= 32 ? 256 : 64; }
+// one wait covers a whole A stage); for large ones 128 with one operand
+// (gate_up: each stage wait and release then covers 8 MMAs; measured faster
+// than 64) and 64 with two (down: a 128-K stage of h hi and lo would leave
+// only two stages in the ring; measured slower).
+__host__ __device__ inline int act_stage_k(int nb, int nops) {
+  return nb <= 32 ? 256 : (nops == 1 ? 128 : 64);
+}
 // A stages that fit in TMEM next to two accumulators of nb columns.
 __host__ __device__ inline int a_stages(int nb) {
   const int n = (kTmemCols - 2 * nb) / kACols;
@@ -121,7 +125,7 @@ __host__ __device__ inline Lay layout(int nsb, int nb, int nc, int nbs) {
   int off = 0;
   l.codes = off;
   off += nc * kCodeStageBytes;
-  l.bstage = Cfg<M>::NOPS * (act_stage_k(nb) / 64) * nb * 128;
+  l.bstage = Cfg<M>::NOPS * (act_stage_k(nb, Cfg<M>::NOPS) / 64) * nb * 128;
   l.bt = off;
   off += nbs * l.bstage;
   l.scbuf = (kMW * nsb + 15) / 16 * 16;
@@ -336,7 +340,7 @@ moe_expert_gemm_tmem(const __grid_constant__ CUtensorMap map_w,
   const int K = kGateUp ? a.d : a.W;                 // reduction length
   const int nsb = K / 32;                            // scale bytes per weight row
   const int nS = (K + kSK - 1) / kSK;                // stages (code = A) per unit
-  const int bk = act_stage_k(a.nb);                  // K per activation stage
+  const int bk = act_stage_k(a.nb, NOPS);            // K per activation stage
   const int nKB = (K + bk - 1) / bk;                 // activation stages per unit
   const int rpe = kGateUp ? 2 * a.W : a.d;           // weight rows per expert
   const int n_out = kGateUp ? a.W : a.d;
@@ -533,10 +537,19 @@ moe_expert_gemm_tmem(const __grid_constant__ CUtensorMap map_w,
               const uint32_t sub = bsm + uint32_t((kk0 / 4) * NOPS * a.nb * 128);
               const uint64_t bdesc0 = ptx::desc_kmajor_sw128(sub);
               const uint64_t bdesc1 = ptx::desc_kmajor_sw128(sub + uint32_t(a.nb * 128));
-              const int n4 = min(4, nk - kk0);           // 2 or 4 (K % 32 == 0)
+              // a full 64-K sub-tile (4 K16 steps) or a 32-K tail (K % 32 == 0),
+              // each a straight run of MMAs: a branch between the MMAs of a
+              // run slows their issue far below the tensor pipe's rate
+              if (nk - kk0 >= 4) {
 #pragma unroll
-              for (int kk = 0; kk < 4; ++kk) {
-                if (kk < n4) {
+                for (int kk = 0; kk < 4; ++kk) {
+                  ptx::mma_f16_tmem_a(d_tmem, a_cols + (kk0 + kk) * 8, bdesc0 + 2 * kk, idesc, accumulate);
+                  if (NOPS > 1) ptx::mma_f16_tmem_a(d_tmem, a_cols + (kk0 + kk) * 8, bdesc1 + 2 * kk, idesc, 1u);
+                  accumulate = 1u;
+                }
+              } else {
+#pragma unroll
+                for (int kk = 0; kk < 2; ++kk) {
                   ptx::mma_f16_tmem_a(d_tmem, a_cols + (kk0 + kk) * 8, bdesc0 + 2 * kk, idesc, accumulate);
                   if (NOPS > 1) ptx::mma_f16_tmem_a(d_tmem, a_cols + (kk0 + kk) * 8, bdesc1 + 2 * kk, idesc, 1u);
                   accumulate = 1u;

@@ -1,13 +1,14 @@
-// Peak dense rate of the two tensor-core MMA kinds the grouped GEMMs issue,
-// measured with the GEMMs' own instruction forms: kind::f16 (bf16 x bf16, the
-// TMEM design) and kind::mxf8f6f4 with block scales (E2M1 x E4M3, the
-// block-scaled design).  One CTA per SM; one thread issues `iters` rounds of
-// four back-to-back 128 x 256 MMAs over operand tiles resident in shared
-// memory (K = 64 per round for kind::f16, 128 for kind::mxf8f6f4), into one
-// TMEM accumulator; the host times the launch with CUDA events.  The operand
-// values (zeros, scales 2^0) do not matter to the rate.  This is a
-// measurement aid of the library: the roofline of a block-scaled GEMM is
-// reported against the peak of its own kind.
+// Peak dense rate of the tensor-core MMA forms the grouped GEMMs issue,
+// measured with the GEMMs' own instructions: kind::f16 (bf16 x bf16) with both
+// operands in shared memory at 128 x 256, kind::mxf8f6f4 with block scales
+// (E2M1 x E4M3, the block-scaled design) at 128 x 256, and kind::f16 with A
+// read from tensor memory (the TMEM design's form) at 128 x 128 and
+// 128 x 256.  One CTA per SM; one thread issues `iters` rounds of four
+// back-to-back MMAs (K = 64 per round for kind::f16, 128 for kind::mxf8f6f4)
+// into one TMEM accumulator; the host times the launch with CUDA events.  The
+// operand values (zeros, scales 2^0) do not matter to the rate.  This is a
+// measurement aid of the library: a GEMM's roofline can be read against the
+// rate of the very instruction form it issues.
 #include "common.cuh"
 #include "moe.h"
 #include "tc_ptx.cuh"
@@ -19,8 +20,11 @@ constexpr int kM = 128, kN = 256;
 constexpr int kTileA = kM * 128, kTileB = kN * 128;   // one 128-byte swizzle row per operand row
 constexpr long long kWaitCycles = 4000000000ll;
 
-template <bool MX>
+// KIND: 0 kind::f16 A, B in shared memory, N = 256; 1 kind::mxf8f6f4, N = 256;
+// 2 kind::f16, A in TMEM, N = 128; 3 kind::f16, A in TMEM, N = 256.
+template <int KIND>
 __global__ void __launch_bounds__(128, 1) mma_peak_kernel(int iters, int32_t* status) {
+  constexpr bool MX = KIND == 1;
   extern __shared__ uint8_t raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sa = sm;
@@ -43,6 +47,14 @@ __global__ void __launch_bounds__(128, 1) mma_peak_kernel(int iters, int32_t* st
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tbase;
+  if (KIND >= 2) {
+    // A in TMEM: columns 256..287, zeros
+    uint32_t z[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) z[i] = 0u;
+    ptx::tmem_st_32x32b_x32(tmem + (uint32_t(warp * 32) << 16) + 256, z);
+    ptx::tmem_st_wait();
+  }
   if (MX) {
     // UE8M0 scale columns 256..271 (A: 256..259, B: 264..271) hold 2^0
     const uint32_t lane_addr = uint32_t(warp * 32) << 16;
@@ -64,6 +76,12 @@ __global__ void __launch_bounds__(128, 1) mma_peak_kernel(int iters, int32_t* st
 #pragma unroll
         for (int j = 0; j < 4; ++j)               // K = 32 each: 32 bytes of the row
           ptx::mma_mx(tmem, ad + 2 * j, bd + 2 * j, idesc[j], tmem + 256, tmem + 264, it | j);
+    } else if (KIND >= 2) {
+      const uint32_t idesc = ptx::idesc_f16(kM, KIND == 2 ? 128 : kN, true);
+      for (int it = 0; it < iters; ++it)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)               // K = 16 each: 8 TMEM columns of A
+          ptx::mma_f16_tmem_a(tmem, tmem + 256 + 8 * j, bd + 2 * j, idesc, it | j);
     } else {
       const uint32_t idesc = ptx::idesc_f16(kM, kN, true);
       for (int it = 0; it < iters; ++it)
@@ -92,13 +110,16 @@ __global__ void __launch_bounds__(128, 1) mma_peak_kernel(int iters, int32_t* st
 
 extern "C" moe_status moe_mma_peak(int kind, int iters, double* tflops, void* workspace,
                                    void* stream) {
-  if ((kind != 0 && kind != 1) || iters < 1 || iters > (1 << 24)) return MOE_ERR_SHAPE;
+  if (kind < 0 || kind > 3 || iters < 1 || iters > (1 << 24)) return MOE_ERR_SHAPE;
   if (!tflops || !workspace) return MOE_ERR_NULL;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // more shared memory than two CTAs could share, so each SM runs exactly one
   const int smem = 120 * 1024;
-  const void* fn = kind ? reinterpret_cast<const void*>(moe::mma_peak_kernel<true>)
-                        : reinterpret_cast<const void*>(moe::mma_peak_kernel<false>);
+  const void* fns[4] = {reinterpret_cast<const void*>(moe::mma_peak_kernel<0>),
+                        reinterpret_cast<const void*>(moe::mma_peak_kernel<1>),
+                        reinterpret_cast<const void*>(moe::mma_peak_kernel<2>),
+                        reinterpret_cast<const void*>(moe::mma_peak_kernel<3>)};
+  const void* fn = fns[kind];
   if (moe::set_smem_limit_once(fn, smem) != cudaSuccess) return MOE_ERR_CUDA;
   int32_t* status = static_cast<int32_t*>(workspace);
   if (cudaMemsetAsync(status, 0, 4, s) != cudaSuccess) return MOE_ERR_CUDA;
@@ -114,8 +135,12 @@ extern "C" moe_status moe_mma_peak(int kind, int iters, double* tflops, void* wo
   float ms = 0.f;
   for (int rep = 0; rep < 2 && st == MOE_OK; ++rep) {
     if (rep == 1 && cudaEventRecord(a, s) != cudaSuccess) st = MOE_ERR_CUDA;
-    if (kind) moe::mma_peak_kernel<true><<<grid, 128, smem, s>>>(iters, status);
-    else moe::mma_peak_kernel<false><<<grid, 128, smem, s>>>(iters, status);
+    switch (kind) {
+      case 0: moe::mma_peak_kernel<0><<<grid, 128, smem, s>>>(iters, status); break;
+      case 1: moe::mma_peak_kernel<1><<<grid, 128, smem, s>>>(iters, status); break;
+      case 2: moe::mma_peak_kernel<2><<<grid, 128, smem, s>>>(iters, status); break;
+      default: moe::mma_peak_kernel<3><<<grid, 128, smem, s>>>(iters, status); break;
+    }
     if (cudaGetLastError() != cudaSuccess) st = MOE_ERR_CUDA;
   }
   if (st == MOE_OK && cudaEventRecord(b, s) != cudaSuccess) st = MOE_ERR_CUDA;
@@ -124,8 +149,9 @@ extern "C" moe_status moe_mma_peak(int kind, int iters, double* tflops, void* wo
   cudaEventDestroy(a);
   cudaEventDestroy(b);
   if (st != MOE_OK) return st;
-  const double k_per_round = kind ? 128.0 : 64.0;
-  const double flops = 2.0 * moe::kM * moe::kN * k_per_round * double(iters) * grid;
+  const double k_per_round = kind == 1 ? 128.0 : 64.0;
+  const double n = kind == 2 ? 128.0 : double(moe::kN);
+  const double flops = 2.0 * moe::kM * n * k_per_round * double(iters) * grid;
   *tflops = flops / (double(ms) * 1e-3) / 1e12;
   return MOE_OK;
 }

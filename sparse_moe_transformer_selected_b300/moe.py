@@ -221,11 +221,11 @@ def moe_debug_combine(y, perm, inv, topk_w, T, d, k, out_bf16, workspace, worksp
         workspace_bytes, _stream(stream)))
 
 
-MMA_KINDS = {"f16": 0, "mxf8f6f4": 1}
+MMA_KINDS = {"f16": 0, "mxf8f6f4": 1, "f16_tmem_a_n128": 2, "f16_tmem_a_n256": 3}
 
 
 def moe_mma_peak(kind, iters, workspace, stream=None) -> float:
-    """Dense TFLOP/s of an MMA kind ("f16" or "mxf8f6f4"); include/moe.h."""
+    """Dense TFLOP/s of an MMA form (a key of MMA_KINDS); include/moe.h."""
     kind = MMA_KINDS[kind] if isinstance(kind, str) else kind
     out = ctypes.c_double(0.0)
     _check(load().moe_mma_peak(kind, iters, ctypes.byref(out), _ptr(workspace), _stream(stream)))

@@ -196,6 +196,7 @@ def test_failure_hooks_check_their_arguments(lib):
 
 def test_mma_peak_checks_its_arguments(lib):
     out = ctypes.c_double(0.0)
-    assert lib.moe_mma_peak(2, 10, ctypes.byref(out), 16, None) == 2
+    assert lib.moe_mma_peak(4, 10, ctypes.byref(out), 16, None) == 2
+    assert lib.moe_mma_peak(-1, 10, ctypes.byref(out), 16, None) == 2
     assert lib.moe_mma_peak(0, 0, ctypes.byref(out), 16, None) == 2
     assert lib.moe_mma_peak(1, 10, None, 16, None) == 1
