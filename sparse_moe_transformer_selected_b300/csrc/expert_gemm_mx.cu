@@ -23,7 +23,8 @@
 // Operands in shared memory, 128-byte swizzle, K-major:
 //   A  TMA with the 4-bit "16U4_ALIGN16B" type: every 16 packed codes (8 bytes)
 //      land in 16 bytes (8 bytes of codes, 8 bytes of padding), the layout
-//      the MMA reads E2M1 from.  A box is 128 codes x 64 or 128 rows.  The
+//      the MMA reads E2M1 from.  A box is 128 codes x 128 rows: gate_up's is
+//      3-D, 64 gate rows and the 64 up rows W below them; down's 2-D.  The
 //      type wants the tensor's row length a multiple of 128, so the map covers
 //      the first K - K % 128 codes of each row and a second map, whose base
 //      is the row's last 128 codes, serves the tail.
@@ -458,7 +459,7 @@ moe_expert_mx(const __grid_constant__ CUtensorMap map_wg,     // gate_up codes, 
         if (!wait_phase(&info_full[q & 1], (q >> 1) & 1, abort_flag, a.status, a.wait_ns, 0, 11)) { ok = false; break; }
         const UnitInfo& inf = info[q & 1];
         const bool gu = inf.gu != 0;
-        const int row_a = inf.row_a, row_b = inf.row_b, r0 = inf.r0;
+        const int row_a = inf.row_a, r0 = inf.r0;
         int tok[kNB];
 #pragma unroll
         for (int j = 0; j < kNB; ++j) tok[j] = inf.tok[j];
@@ -490,9 +491,8 @@ moe_expert_mx(const __grid_constant__ CUtensorMap map_wg,     // gate_up codes, 
             const CUtensorMap* mwi = main_box ? mw : mwt;
             const int xa = main_box ? i * kBoxK : 0;
             const int xb = i * kBoxK;
-            ptx::tma_load_2d(dai, mwi, &full[st.slot], xa, row_a);
             if (gu) {
-              ptx::tma_load_2d(dai + (kMW / 2) * kBoxK, mwi, &full[st.slot], xa, row_b);
+              ptx::tma_load_3d(dai, mwi, &full[st.slot], xa, row_a, 0);   // gate and up rows
               for (int t = 0; t < MG.NT; ++t) {
                 const CUtensorMap* mb = t ? &map_x1 : &map_x0;
                 ptx::tma_gather4(dbi + t * MG.rpt * kBoxK, mb, &full[st.slot], xb, tok[0], tok[1],
@@ -501,6 +501,7 @@ moe_expert_mx(const __grid_constant__ CUtensorMap map_wg,     // gate_up codes, 
                                  tok[5], tok[6], tok[7]);
               }
             } else {
+              ptx::tma_load_2d(dai, mwi, &full[st.slot], xa, row_a);
               for (int t = 0; t < MD.NT; ++t)
                 ptx::tma_load_2d(dbi + t * MD.rpt * kBoxK, mh[t], &full[st.slot], xb, r0);
             }
@@ -755,19 +756,44 @@ int plan_stages(const GemmArgs& a) {
   return s < kMaxStages ? s : kMaxStages;
 }
 
+// gate_up's codes as a 3-D tensor [half][row][code] over the [E 2W, d] table:
+// the half dimension steps W rows, so one box at (x, row, 0) holds 64 gate rows
+// and the 64 up rows W below them, in that order (one TMA instead of two).
+cudaError_t make_gate_up_map(CUtensorMap* map, const void* base, long long rows, long long cols,
+                             long long row_bytes, long long half_bytes) {
+  auto enc = get_encode();
+  if (!enc) return cudaErrorNotSupported;
+  const cuuint64_t dims[3] = {cuuint64_t(cols), cuuint64_t(rows), 2};
+  const cuuint64_t strides[2] = {cuuint64_t(row_bytes), cuuint64_t(half_bytes)};
+  const cuuint32_t box[3] = {cuuint32_t(kBoxK), cuuint32_t(kMW / 2), 2};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3, const_cast<void*>(base), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 // The weight maps of one GEMM: the main map and the tail map.
 cudaError_t make_weight_maps(bool gu, const GemmArgs& a, CUtensorMap* mw, CUtensorMap* mwt) {
   const int K = gu ? a.d : a.W;
   const uint8_t* w = gu ? a.w_gu : a.w_dn;
   const long long rows = gu ? (long long)a.E * 2 * a.W : (long long)a.E * a.d;
-  const int box_rows = gu ? kMW / 2 : kMW;
   const int kmain = K / kBoxK * kBoxK;
+  if (gu) {
+    // the last 128 codes of each row: base at code K - 128 of row 0
+    const long long half = (long long)a.W * (K / 2);
+    cudaError_t e = make_gate_up_map(mw, w, rows, kmain, K / 2, half);
+    if (e != cudaSuccess) return e;
+    if (K % kBoxK) return make_gate_up_map(mwt, w + (K - kBoxK) / 2, rows, kBoxK, K / 2, half);
+    *mwt = *mw;
+    return cudaSuccess;
+  }
   cudaError_t e = make_map(mw, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w, rows, kmain, K / 2, kBoxK,
-                           box_rows);
+                           kMW);
   if (e != cudaSuccess) return e;
   if (K % kBoxK)       // the last 128 codes of each row: base at code K - 128 of row 0
     return make_map(mwt, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w + (K - kBoxK) / 2, rows, kBoxK,
-                    K / 2, kBoxK, box_rows);
+                    K / 2, kBoxK, kMW);
   *mwt = *mw;
   return cudaSuccess;
 }
