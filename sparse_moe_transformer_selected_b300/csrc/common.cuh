@@ -47,9 +47,9 @@ int device_sm_count();
 // Router tile: tokens per CTA of the router kernel.  Also the granularity of
 // the per-tile expert histogram the permutation is built from.
 constexpr int kRouterTile = 32;
-// Largest token chunk of the grouped GEMMs.  An expert's segment of the
-// permuted rows is cut into ceil(count / chunk) chunks, chunk <= kGemmBM (the
-// shared-memory-staged design always uses kGemmBM: its MMA M side).
+// Token chunk the routing-only call scans for, and the one the design checks
+// start from.  A grouped GEMM cuts each expert's segment of the permuted rows
+// into ceil(count / chunk) chunks of its own chunk size.
 constexpr int kGemmBM = 128;
 
 // Router work split.  A CTA of the logits kernel takes 32 tokens x a group of
@@ -98,7 +98,7 @@ struct Workspace {
   size_t tile_counts;  // int32[ntiles*E]  rows of expert e in router tile
   size_t tile_base;    // int32[ntiles*E]  first permuted row of (tile, e)
   size_t offsets;      // int32[E+1]
-  size_t mtile_off;    // int32[E+1]   prefix of ceil(count/chunk)
+  size_t mtile_off;    // int32[2(E+1)] prefixes of ceil(count/chunk), then of ceil(count/chunk2)
   size_t perm;         // int32[R]
   size_t inv;          // int32[R]
   size_t rowexp;       // int32[R]   e_t of the token of each permuted row
@@ -145,7 +145,7 @@ inline Workspace workspace_layout(int64_t T, int d, int W, int E, int k) {
   ws.tile_counts = take(size_t(ntiles) * E * 4);
   ws.tile_base = take(size_t(ntiles) * E * 4);
   ws.offsets = take(size_t(E + 1) * 4);
-  ws.mtile_off = take(size_t(E + 1) * 4);
+  ws.mtile_off = take(size_t(E + 1) * 8);
   ws.perm = take(size_t(R) * 4);
   ws.inv = take(size_t(R) * 4);
   ws.rowexp = take(size_t(R) * 4);
@@ -178,7 +178,8 @@ struct RouteArgs {
   const float* norm_w;         // [d]
   float eps;
   int T, d, E, k;
-  int chunk;                   // token chunk of the grouped GEMMs (for mtile_off)
+  int chunk;                   // token chunk of gate_up (for mtile_off[0..E])
+  int chunk2;                  // token chunk of down (for mtile_off[E+1..2E+1])
   float* logit_part;           // [splits, T, E]
   int32_t* topk_idx;           // [T, k]
   float* topk_w;               // [T, k]
@@ -186,7 +187,7 @@ struct RouteArgs {
   int32_t* tile_counts;        // [ntiles, E]
   int32_t* tile_base;          // [ntiles, E]
   int32_t* offsets;            // [E + 1]
-  int32_t* mtile_off;          // [E + 1]
+  int32_t* mtile_off;          // [2 (E + 1)]
   int32_t* status;             // status word (cleared by the first kernel)
   float* rnorm;                // [T] 1 / rms of each token, written with xn
   int32_t* cnt;                // combine counts, zeroed by the first kernel
@@ -227,7 +228,8 @@ __device__ __forceinline__ float rms_scaled_bf16(float x, float g, float r32, do
 // logits are those of RMSNorm(x) = x / sqrt(mean(x²) + eps) · norm_w.
 // When T has at most kFuseScanTiles tiles and tile_base is given, the last
 // top-k CTA also runs the expert scan (tile_base, offsets, mtile_off for
-// `chunk`) and, when r.perm is given, writes perm and inv; *scanned is set.
+// `chunk` and `chunk2`) and, when r.perm is given, writes perm and inv;
+// *scanned is set.
 // Otherwise the caller launches the scan and the scatter.  With r.xq_hi the
 // token tables of the block-scaled design are written too.
 cudaError_t launch_router_topk(const RouteArgs& r, bool* scanned, cudaStream_t s);
@@ -236,8 +238,9 @@ cudaError_t launch_router_topk(const RouteArgs& r, bool* scanned, cudaStream_t s
 int router_tc_splits(int64_t T, int d, int E, int* k_len);
 cudaError_t launch_router_logits_tc(const RouteArgs& r, int* nks, cudaStream_t s);
 
-// K2a: expert offsets, per-(tile, expert) bases, prefix of chunks of `chunk` rows.
-cudaError_t launch_route_scan(const int32_t* tile_counts, int ntiles, int E, int chunk,
+// K2a: expert offsets, per-(tile, expert) bases, prefixes of chunks of `chunk`
+// rows (mtile_off[0..E]) and of `chunk2` rows (mtile_off[E+1..2E+1]).
+cudaError_t launch_route_scan(const int32_t* tile_counts, int ntiles, int E, int chunk, int chunk2,
                               int32_t* tile_base, int32_t* offsets, int32_t* mtile_off,
                               cudaStream_t s);
 
@@ -253,7 +256,7 @@ cudaError_t launch_route_scatter(const __nv_bfloat16* x, int T, int d, int E, in
 
 struct GemmArgs {
   int R, d, W, E;
-  int nb;                     // token chunk (multiple of 16, <= kGemmBM)
+  int nb;                     // token chunk (TMEM design: multiple of 16, <= 192; block-scaled: 8)
   int stages_c, stages_b;     // ring depths of the TMEM design (set by its launcher)
   const int32_t* offsets;     // [E+1]
   const int32_t* mtile_off;   // [E+1] prefix of ceil(count / nb)
@@ -307,10 +310,11 @@ __device__ __forceinline__ unsigned long long global_ns() {
 // (expert_gemm_tmem.cu); usable when its shared-memory plan fits (the
 // reduction length sets the size of the per-unit scale buffers).
 bool expert_gemm_tmem_fits(const GemmArgs& a);
-// Token chunk of the TMEM design for R routed rows over E experts: small
-// chunks (N = 16) when experts get few tokens, so an activation stage is a
-// few KB and the ring can be deep; 128 when they get many.
-int expert_gemm_tmem_chunk(int64_t R, int E);
+// Token chunk of the TMEM design's gate_up (or down) for R routed rows over E
+// experts: small chunks (N = 16) when experts get few tokens, so an activation
+// stage is a few KB and the ring can be deep; 192 (down: 160) when they get
+// many, since each chunk costs one dequantisation of the expert's weights.
+int expert_gemm_tmem_chunk(int64_t R, int E, bool gate_up);
 // Whether the clamp bounds h well inside the f16 range, so the TMEM design
 // carries h as an f16 pair and runs the down GEMM in f16.
 bool hidden_fits_f16(float limit);

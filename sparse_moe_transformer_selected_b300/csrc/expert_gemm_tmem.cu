@@ -8,24 +8,26 @@
 //
 // The weights are the M side of the MMA and the tokens the N side:
 //   D[weight row, token] = Σ_k A[weight row, k] · B[token, k]
-// A (128 weight rows x 128 K per stage) is never written to shared memory: the
-// packed E2M1 codes arrive by TMA (128 rows x 256 K = 16 KB per code stage),
-// eight dequantiser warps convert them in registers and store them into TMEM
-// with tcgen05.st, and tcgen05.mma reads A from TMEM.  B (a chunk of nb tokens
-// x 64 K per stage, 128-byte swizzle) arrives by TMA.  The chunk nb is 16 when
-// experts get a few tokens each (a decode step: the kernel streams weights and
-// the activation ring is many small stages deep) and up to 128 when they get
-// many (prefill: experts are cut into 128-token chunks).
+// A (128 weight rows x 128 K per A stage) is never written to shared memory:
+// the packed E2M1 codes arrive by TMA (128 rows x 256 K = 16 KB per code
+// stage), sixteen dequantiser warps convert them in registers and store them
+// into TMEM with tcgen05.st, and tcgen05.mma reads A from TMEM.  B (a chunk of
+// nb tokens x 64 K per sub-tile, 128-byte swizzle) arrives by TMA.  The chunk
+// nb is 16 when experts get a few tokens each (a decode step: the kernel
+// streams weights and the activation ring is many small stages deep) and up to
+// 192 when they get many (prefill): every chunk costs one dequantisation of
+// the expert's weights, so the fewer chunks the better, up to the point where
+// two accumulators of nb columns leave tensor memory too few A stages.
 //
 // Persistent kernel, one CTA per SM, 24 warps:
 //   warp 0      producer: scales (1-D bulk copy) and codes (TMA)
 //   warp 1      MMA issuer (one elected thread)
-//   warp 2      TMEM allocator (512 columns: 2 accumulator buffers of 128,
-//               each 128/nb accumulators of nb columns; 4 A stages of 64)
+//   warp 2      TMEM allocator (512 columns: 2 accumulators of nb columns,
+//               then as many A stages of 64 columns as fit, at most 6)
 //   warp 3      producer: activations (TMA, one nb-row box per operand and stage)
 //   warps 4-7   epilogue, TMEM lane quarter = warp % 4
-//   warps 8-23  dequantisers, lane quarter = warp % 4, K quarter of the stage
-//               = (warp - 8) / 4
+//   warps 8-23  dequantisers, lane quarter = warp % 4, K quarter of each A
+//               stage = (warp - 8) / 4
 // Work unit = (token chunk of one expert, weight M tile), chunk-major so a
 // chunk's activations and an expert's weights stay in L2 while they are reused.
 //
@@ -61,21 +63,23 @@
 namespace moe {
 namespace {
 
-constexpr int kNBMax = kGemmBM;              // largest token chunk (MMA N)
+constexpr int kNBMax = 192;                  // largest token chunk (MMA N)
 constexpr int kMW = 128;                     // weight rows per unit (MMA M, TMEM lanes)
-constexpr int kSK = 256;                     // K per stage: 128 B of codes per row, 128 TMEM columns of A
-constexpr int kACols = kSK / 2;              // TMEM columns per A stage
+constexpr int kSK = 256;                     // K per code stage: 128 B of codes per row
+constexpr int kAK = 128;                     // K per A stage
+constexpr int kACols = kAK / 2;              // TMEM columns per A stage (f16 pairs)
 constexpr int kMaxC = 12;                    // code-ring depth, most
-constexpr int kMaxA = 3;                     // A-ring depth, most
+constexpr int kMaxA = 6;                     // A-ring depth, most
 constexpr int kMaxB = 16;                    // activation-ring depth, most
 constexpr int kRing = 4;                     // per-unit row-factor ring
 constexpr int kThreads = 768;
 constexpr int kWarpProd = 0, kWarpMMA = 1, kWarpTmem = 2, kWarpProdB = 3, kWarpEpi0 = 4,
               kWarpDq0 = 8;
 // 16 dequantiser warps: 4 per TMEM lane quarter, each converting a quarter
-// (64 K, 32 columns) of every 256-K stage for its 32 weight rows.  Four warps
-// per SM partition hide the latency of each warp's load -> convert -> store
-// chain, which two could not.
+// (32 K, 16 columns) of every 128-K A stage for its 32 weight rows, two A
+// stages per code stage.  Every warp takes part in every A stage, so each
+// follows the A ring slot by slot.  Four warps per SM partition hide the
+// latency of each warp's load -> convert -> store chain, which two could not.
 constexpr int kDqWarps = 16;
 constexpr int kTmemCols = 512;
 constexpr int kCodeStageBytes = kMW * kSK / 2;   // 16 KB
@@ -86,13 +90,13 @@ constexpr int kNumBars = 2 * kMaxC + 2 * kMaxA + 2 * kMaxB + 4 + 4 + 2 * kRing +
 constexpr long long kSpinLimit = 4000000000ll;   // clock cycles: the final drains
 constexpr int kMaxSmem = 232448;                 // 227 KB opt-in per CTA
 
-// K of one activation stage: 256 for small chunks (a stage is a few KB and
-// one wait covers a whole A stage); for large ones 128 with one operand
-// (gate_up: each stage wait and release then covers 8 MMAs; measured faster
-// than 64) and 64 with two (down: a 128-K stage of h hi and lo would leave
-// only two stages in the ring; measured slower).
+// K of one activation stage, at most one A stage: 128 for small chunks and
+// for one operand (gate_up: each stage wait and release then covers 8 MMAs;
+// measured faster than 64), 64 for large chunks with two operands (down: a
+// 128-K stage of h hi and lo would leave only two stages in the ring;
+// measured slower).
 __host__ __device__ inline int act_stage_k(int nb, int nops) {
-  return nb <= 32 ? 256 : (nops == 1 ? 128 : 64);
+  return (nb <= 32 || nops == 1) ? 128 : 64;
 }
 // A stages that fit in TMEM next to two accumulators of nb columns.
 __host__ __device__ inline int a_stages(int nb) {
@@ -138,7 +142,7 @@ __host__ __device__ inline Lay layout(int nsb, int nb, int nc, int nbs) {
   off += kNumBars * 8;
   l.misc = off;
   off += 16;                          // TMEM base, abort flag
-  off += (M == Mode::Down) ? combine_smem_bytes(kNBMax) : 0;   // combine lists
+  off += (M == Mode::Down) ? combine_smem_bytes(nb) : 0;   // combine lists
   l.total = off;
   return l;
 }
@@ -339,7 +343,8 @@ moe_expert_gemm_tmem(const __grid_constant__ CUtensorMap map_w,
 
   const int K = kGateUp ? a.d : a.W;                 // reduction length
   const int nsb = K / 32;                            // scale bytes per weight row
-  const int nS = (K + kSK - 1) / kSK;                // stages (code = A) per unit
+  const int nS = (K + kSK - 1) / kSK;                // code stages per unit
+  const int nA = (K + kAK - 1) / kAK;                // A stages per unit
   const int bk = act_stage_k(a.nb, NOPS);            // K per activation stage
   const int nKB = (K + bk - 1) / bk;                 // activation stages per unit
   const int rpe = kGateUp ? 2 * a.W : a.d;           // weight rows per expert
@@ -523,16 +528,16 @@ moe_expert_gemm_tmem(const __grid_constant__ CUtensorMap map_w,
         const uint32_t d_tmem = tmem_base + buf * a.nb;
         uint32_t accumulate = 0;
         int jb = 0;                                  // activation stage of the unit
-        for (int ja = 0; ja < nS && ok; ++ja) {
+        for (int ja = 0; ja < nA && ok; ++ja) {
           if (!wait_phase(&a_full[ar.slot], ar.phase, abort_flag, a.status, a.wait_ns)) { ok = false; break; }
           const uint32_t a_stage = tmem_base + a_col0 + ar.slot * kACols;
           // the activation stages inside this A stage
-          for (int kb = ja * kSK; kb < min(K, (ja + 1) * kSK); kb += bk, ++jb) {
+          for (int kb = ja * kAK; kb < min(K, (ja + 1) * kAK); kb += bk, ++jb) {
             if (!wait_phase(&b_full[br.slot], br.phase, abort_flag, a.status, a.wait_ns)) { ok = false; break; }
             ptx::tc_fence_after();
             const uint32_t bsm = ptx::smem_u32(bt + br.slot * L.bstage);
             const int nk = min(bk, K - kb) / 16;         // K16 steps in this stage
-            const uint32_t a_cols = a_stage + (kb - ja * kSK) / 2;
+            const uint32_t a_cols = a_stage + (kb - ja * kAK) / 2;
             for (int kk0 = 0; kk0 < nk; kk0 += 4) {      // one 64-K sub-tile at a time
               const uint32_t sub = bsm + uint32_t((kk0 / 4) * NOPS * a.nb * 128);
               const uint64_t bdesc0 = ptx::desc_kmajor_sw128(sub);
@@ -659,20 +664,20 @@ moe_expert_gemm_tmem(const __grid_constant__ CUtensorMap map_w,
       // K5: the weighted sum of each token whose k rows are now all stored
       // (after the accumulator is released, so the next unit's MMAs run meanwhile)
       if constexpr (!kGateUp)
-        combine_tile<2>(a, w.r0, w.n, w.mt, Ln, comb, kNBMax, 2);
+        combine_tile<2>(a, w.r0, w.n, w.mt, Ln, comb, a.nb, 2);
     }
   } else if (warp >= kWarpDq0) {
     // --------------------------------------------------------- dequantisers --
-    // Warp (quarter, part) converts K range [part*64, part*64+64) of every
-    // 256-K stage for its 32 weight rows: 64 codes -> 32 TMEM columns, one
-    // tcgen05.st.
+    // Warp (quarter, part) converts K range [part*32, part*32+32) of each
+    // 128-K half of every 256-K code stage for its 32 weight rows: 32 codes
+    // -> 16 TMEM columns of one A stage, one tcgen05.st per half.
     const int quarter = warp & 3;
     const int part = (warp - kWarpDq0) >> 2;
     const int Ln = quarter * 32 + lane;          // TMEM lane = weight row of the tile
     const int sr = kGateUp ? ((Ln & 1) ? kMW / 2 + (Ln >> 1) : (Ln >> 1)) : Ln;   // smem row
     const uint32_t lane_addr = uint32_t(quarter * 32) << 16;
-    const uint32_t choff0 = ptx::sw128_offset(sr, part * 2);      // this row's 2 chunks
-    const uint32_t choff1 = ptx::sw128_offset(sr, part * 2 + 1);
+    const uint32_t choff0 = ptx::sw128_offset(sr, part);          // K half 0: chunk part
+    const uint32_t choff1 = ptx::sw128_offset(sr, 4 + part);      // K half 1: chunk 4 + part
     Ring cr, ar;
     bool ok = true;
     int q = 0;
@@ -699,16 +704,10 @@ moe_expert_gemm_tmem(const __grid_constant__ CUtensorMap map_w,
         ok = __all_sync(0xffffffffu, wait_phase(&code_full[cr.slot], cr.phase, abort_flag, a.status, a.wait_ns, 32));
         if (!ok) break;
         const uint8_t* cst = codes + cr.slot * kCodeStageBytes;
-        // this thread's 2 scale blocks: one 16-bit read when the row starts at
-        // an even byte offset (K/32 odd makes every other row start odd)
-        const int b0 = cs * (kSK / 32) + part * 2;
-        uint32_t s01 = 0;
-        if (valid && b0 < nsb) {
-          const uint8_t* sp = srow + b0;
-          if (b0 + 1 >= nsb) s01 = sp[0];
-          else if ((reinterpret_cast<uintptr_t>(sp) & 1u) == 0) s01 = *reinterpret_cast<const uint16_t*>(sp);
-          else s01 = uint32_t(sp[0]) | (uint32_t(sp[1]) << 8);
-        }
+        // this thread's scale blocks: one per K half
+        const int b0 = cs * (kSK / 32) + part, b1 = b0 + 4;
+        const bool v0 = valid && b0 < nsb, v1 = valid && b1 < nsb;
+        const uint32_t s01 = (v0 ? uint32_t(srow[b0]) : 0u) | (v1 ? uint32_t(srow[b1]) << 8 : 0u);
         uint32_t f0, f1;
         if (F16) {
           // 2^(s - r_n) as f16x2 for both blocks at once: byte-wise
@@ -716,15 +715,13 @@ moe_expert_gemm_tmem(const __grid_constant__ CUtensorMap map_w,
           // scale byte; clamped at 0 below the f16 normal range, where the
           // factor becomes 0), moved into both halves' exponent fields
           const uint32_t e2 = __vsubus4(0x0F0Fu, __vsubus4(rnb, s01)) & 0x1F1Fu;
-          f0 = (__byte_perm(e2, 0, 0x4040) << 10);
-          f1 = (__byte_perm(e2, 0, 0x4141) << 10);
-          if (!(valid && b0 < nsb)) f0 = 0u;
-          if (!(valid && b0 + 1 < nsb)) f1 = 0u;
+          f0 = v0 ? (__byte_perm(e2, 0, 0x4040) << 10) : 0u;
+          f1 = v1 ? (__byte_perm(e2, 0, 0x4141) << 10) : 0u;
         } else {
-          f0 = (valid && b0 < nsb) ? Dequant<DQ>::factor(int(s01 & 0xFF), rn) : 0u;
-          f1 = (valid && b0 + 1 < nsb) ? Dequant<DQ>::factor(int(s01 >> 8), rn) : 0u;
+          f0 = v0 ? Dequant<DQ>::factor(int(s01 & 0xFF), rn) : 0u;
+          f1 = v1 ? Dequant<DQ>::factor(int(s01 >> 8), rn) : 0u;
         }
-        // 64 codes: 2 x 16 bytes of the 128-byte swizzled row
+        // 2 x 32 codes: one 16-byte chunk of the 128-byte swizzled row per half
         const uint4 x0 = *reinterpret_cast<const uint4*>(cst + choff0);
         const uint4 x1 = *reinterpret_cast<const uint4*>(cst + choff1);
         // the code stage has been read
@@ -740,14 +737,20 @@ moe_expert_gemm_tmem(const __grid_constant__ CUtensorMap map_w,
         Dequant<DQ>::convert(x1.y, f1, &r[20]);
         Dequant<DQ>::convert(x1.z, f1, &r[24]);
         Dequant<DQ>::convert(x1.w, f1, &r[28]);
-        ok = __all_sync(0xffffffffu, wait_phase(&a_empty[ar.slot], ar.phase ^ 1, abort_flag, a.status, a.wait_ns, 32));
+        // the code stage's two A stages (the second only while it holds K)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          if (2 * cs + h >= nA) break;
+          ok = __all_sync(0xffffffffu, wait_phase(&a_empty[ar.slot], ar.phase ^ 1, abort_flag, a.status, a.wait_ns, 32));
+          if (!ok) break;
+          ptx::tmem_st_32x32b_x16(tmem_base + lane_addr + a_col0 + ar.slot * kACols + part * 16, &r[16 * h]);
+          ptx::tmem_st_wait();
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(&a_full[ar.slot]);
+          ar.next(NAS);
+        }
         if (!ok) break;
-        ptx::tmem_st_32x32b_x32(tmem_base + lane_addr + a_col0 + ar.slot * kACols + part * 32, r);
-        ptx::tmem_st_wait();
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&a_full[ar.slot]);
-        ar.next(NAS);
       }
       if (!ok) break;
       __syncwarp();
@@ -890,15 +893,19 @@ cudaError_t launch(const GemmArgs& args, cudaStream_t s) {
 
 }  // namespace
 
-int expert_gemm_tmem_chunk(int64_t R, int E) {
+// Down takes smaller large chunks than gate_up: its activation stages carry
+// two operands (h hi and lo), and at 192 tokens only two of them fit in
+// shared memory beside the code ring (measured: 160 best for down, 192 for
+// gate_up).
+int expert_gemm_tmem_chunk(int64_t R, int E, bool gate_up) {
   const int64_t avg = R / (E > 0 ? E : 1);
-  return avg <= 8 ? 16 : avg <= 16 ? 32 : avg <= 32 ? 64 : 128;
+  return avg <= 8 ? 16 : avg <= 16 ? 32 : avg <= 32 ? 64 : (gate_up ? 192 : 160);
 }
 
 bool expert_gemm_tmem_fits(const GemmArgs& args) {
-  GemmArgs a = args;
-  a.nb = expert_gemm_tmem_chunk(a.R, a.E);
-  GemmArgs g = a, d = a;
+  GemmArgs g = args, d = args;
+  g.nb = expert_gemm_tmem_chunk(args.R, args.E, true);
+  d.nb = expert_gemm_tmem_chunk(args.R, args.E, false);
   plan<Mode::GateUp>(g);
   plan<Mode::Down>(d);
   return g.stages_b >= 2 && d.stages_b >= 2 && g.stages_c >= 2 && d.stages_c >= 2 &&

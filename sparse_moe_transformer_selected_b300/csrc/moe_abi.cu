@@ -120,7 +120,7 @@ T* at(void* base, size_t off) {
 // read its normalised copy, written by K1 at the start of the y region.
 moe::RouteArgs route_args(void* ws, const moe::Workspace& L, const void* x, int64_t T, int d,
                           const float* rw, const float* rb, const float* norm_w, float eps,
-                          int E, int k, int chunk) {
+                          int E, int k, int chunk, int chunk2) {
   moe::RouteArgs r{};
   r.router_w = rw;
   r.router_b = rb;
@@ -138,6 +138,7 @@ moe::RouteArgs route_args(void* ws, const moe::Workspace& L, const void* x, int6
   r.E = E;
   r.k = k;
   r.chunk = chunk;
+  r.chunk2 = chunk2;
   r.logit_part = at<float>(ws, L.logit_part);
   r.topk_idx = at<int32_t>(ws, L.topk_idx);
   r.topk_w = at<float>(ws, L.topk_w);
@@ -168,8 +169,8 @@ moe_status run_route(const moe::RouteArgs& r, int32_t* rowexp, void* x_perm, cud
   if (e != cudaSuccess) return cuda_fail(e, "router_topk launch");
   if ((e = trace(1, s)) != cudaSuccess) return cuda_fail(e, "trace event");
   if (!scanned) {
-    e = moe::launch_route_scan(r.tile_counts, ntiles, r.E, r.chunk, r.tile_base, r.offsets,
-                               r.mtile_off, s);
+    e = moe::launch_route_scan(r.tile_counts, ntiles, r.E, r.chunk, r.chunk2, r.tile_base,
+                               r.offsets, r.mtile_off, s);
     if (e != cudaSuccess) return cuda_fail(e, "route_scan launch");
   }
   if ((e = trace(2, s)) != cudaSuccess) return cuda_fail(e, "trace event");
@@ -229,9 +230,12 @@ moe_status forward_impl(const void* x_bf16, int64_t T, int d, int W, const float
   if (design == Design::None)
     return fail(MOE_ERR_UNSUPPORTED, "no grouped-GEMM design fits d = %d, W = %d", d, W);
   const bool mx = design == Design::Mx;
-  a.nb = mx ? moe::mx_chunk(a.R, E) : moe::expert_gemm_tmem_chunk(a.R, E);
+  // token chunks: one for both GEMMs in the block-scaled design; the TMEM
+  // design's gate_up and down take their own (the scan writes both prefixes)
+  a.nb = mx ? moe::mx_chunk(a.R, E) : moe::expert_gemm_tmem_chunk(a.R, E, true);
+  const int nb_dn = mx ? a.nb : moe::expert_gemm_tmem_chunk(a.R, E, false);
   moe::RouteArgs r = route_args(workspace, L, x_bf16, T, d, router_w, router_b, norm_w, eps, E,
-                                k, a.nb);
+                                k, a.nb, nb_dn);
   // the block-scaled design's per-chunk counts follow the combine counts and
   // are zeroed with them
   if (mx) r.ncnt += moe::mx_chunk_bound(a.R, E);
@@ -296,8 +300,11 @@ moe_status forward_impl(const void* x_bf16, int64_t T, int d, int W, const float
     e = moe::launch_gateup_tmem(a, s);
     if (e != cudaSuccess) return cuda_fail(e, "gate_up launch");
     if ((e = trace(4, s)) != cudaSuccess) return cuda_fail(e, "trace event");
-    // K4 with K5 in its epilogue
-    e = moe::launch_down_tmem(a, s);
+    // K4 with K5 in its epilogue, over chunks of nb_dn rows
+    moe::GemmArgs ad = a;
+    ad.nb = nb_dn;
+    ad.mtile_off = r.mtile_off + E + 1;
+    e = moe::launch_down_tmem(ad, s);
     if (e != cudaSuccess) return cuda_fail(e, "down launch");
   }
   if ((e = trace(5, s)) != cudaSuccess) return cuda_fail(e, "trace event");
@@ -426,7 +433,7 @@ moe_status moe_route(const void* x_bf16, int64_t T, int d, const float* router_w
   if (st != MOE_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   moe::RouteArgs r = route_args(workspace, L, x_bf16, T, d, router_w, router_b, nullptr, 0.f, E,
-                                k, moe::kGemmBM);
+                                k, moe::kGemmBM, moe::kGemmBM);
   r.ncnt = 0;                                  // no combine follows
   st = run_route(r, nullptr, nullptr, s);
   if (st != MOE_OK) return st;

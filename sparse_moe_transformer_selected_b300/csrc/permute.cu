@@ -22,14 +22,14 @@ constexpr int kScanThreads = 1024;
 // then the partial sums are scanned in tile order and in expert order.
 __global__ void __launch_bounds__(kScanThreads)
 route_scan_kernel(const int32_t* __restrict__ tile_counts, int ntiles, int E, int chunk,
-                  int32_t* __restrict__ tile_base, int32_t* __restrict__ offsets,
+                  int chunk2, int32_t* __restrict__ tile_base, int32_t* __restrict__ offsets,
                   int32_t* __restrict__ mtile_off) {
   __shared__ int32_t part[kScanThreads];
   __shared__ int32_t total[257];
   __shared__ int32_t off[257];
   pdl_wait();
-  scan_tiles<kScanThreads>(tile_counts, ntiles, E, chunk, tile_base, offsets, mtile_off, part, total,
-                           off);
+  scan_tiles<kScanThreads>(tile_counts, ntiles, E, chunk, chunk2, tile_base, offsets, mtile_off, part,
+                           total, off);
 }
 
 // One warp per routed row (t, j): write perm / inv and copy x[t] to its row,
@@ -124,11 +124,11 @@ route_scatter_kernel(const __nv_bfloat16* __restrict__ x, int T, int d, int E, i
 
 }  // namespace
 
-cudaError_t launch_route_scan(const int32_t* tile_counts, int ntiles, int E, int chunk,
+cudaError_t launch_route_scan(const int32_t* tile_counts, int ntiles, int E, int chunk, int chunk2,
                               int32_t* tile_base, int32_t* offsets, int32_t* mtile_off,
                               cudaStream_t s) {
   return launch_pdl(route_scan_kernel, dim3(1), dim3(kScanThreads), 0, s, tile_counts, ntiles, E,
-                    chunk, tile_base, offsets, mtile_off);
+                    chunk, chunk2, tile_base, offsets, mtile_off);
 }
 
 cudaError_t launch_route_scatter(const __nv_bfloat16* x, int T, int d, int E, int k,

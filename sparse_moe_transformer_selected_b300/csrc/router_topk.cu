@@ -333,6 +333,7 @@ router_topk_kernel(const RouteArgs r, int nks, bool quantize, int32_t* __restric
   __shared__ uint32_t mask[kMaxE];       // bit t: token t of this tile picked e
   __shared__ int32_t sel[kTT][8];
   __shared__ int32_t scan_part[kTopkThreads], scan_total[257], scan_off[257];
+  static_assert(kTopkThreads >= 24, "the one-tile scan keeps 3 x 8 warp totals in scan_part");
   __shared__ int last_cta;
 
   const float* __restrict__ part = r.logit_part;
@@ -433,26 +434,34 @@ router_topk_kernel(const RouteArgs r, int nks, bool quantize, int32_t* __restric
     const int lane_e = tid & 31, wid = tid >> 5;
     const int32_t v = tid < E ? __popc(mask[tid]) : 0;
     const int32_t c = tid < E ? (v + r.chunk - 1) / r.chunk : 0;
-    int32_t iv = v, ic = c;                      // inclusive scans inside each warp
+    const int32_t c2 = tid < E ? (v + r.chunk2 - 1) / r.chunk2 : 0;
+    int32_t iv = v, ic = c, ic2 = c2;            // inclusive scans inside each warp
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int32_t pv = __shfl_up_sync(0xffffffffu, iv, o);
       const int32_t pc = __shfl_up_sync(0xffffffffu, ic, o);
-      if (lane_e >= o) { iv += pv; ic += pc; }
+      const int32_t pc2 = __shfl_up_sync(0xffffffffu, ic2, o);
+      if (lane_e >= o) { iv += pv; ic += pc; ic2 += pc2; }
     }
-    if (lane_e == 31 && wid < 8) { scan_part[wid] = iv; scan_part[8 + wid] = ic; }
+    if (lane_e == 31 && wid < 8) { scan_part[wid] = iv; scan_part[8 + wid] = ic; scan_part[16 + wid] = ic2; }
     __syncthreads();
     if (tid < E) {
-      int32_t bv = 0, bc = 0;                    // the earlier warps' totals, in order
-      for (int w2 = 0; w2 < wid; ++w2) { bv += scan_part[w2]; bc += scan_part[8 + w2]; }
-      const int32_t ev = bv + iv - v, ec = bc + ic - c;
+      int32_t bv = 0, bc = 0, bc2 = 0;           // the earlier warps' totals, in order
+      for (int w2 = 0; w2 < wid; ++w2) {
+        bv += scan_part[w2];
+        bc += scan_part[8 + w2];
+        bc2 += scan_part[16 + w2];
+      }
+      const int32_t ev = bv + iv - v, ec = bc + ic - c, ec2 = bc2 + ic2 - c2;
       scan_off[tid] = ev;
       r.offsets[tid] = ev;
       r.tile_base[tid] = ev;
       r.mtile_off[tid] = ec;
+      r.mtile_off[E + 1 + tid] = ec2;
       if (tid == E - 1) {
         r.offsets[E] = ev + v;
         r.mtile_off[E] = ec + c;
+        r.mtile_off[2 * E + 1] = ec2 + c2;
       }
     }
     __syncthreads();
@@ -474,8 +483,8 @@ router_topk_kernel(const RouteArgs r, int nks, bool quantize, int32_t* __restric
     __syncthreads();
     if (last_cta) {
       __threadfence();
-      scan_tiles<kTopkThreads>(tile_counts, int(gridDim.x), E, r.chunk, r.tile_base, r.offsets,
-                           r.mtile_off, scan_part, scan_total, scan_off);
+      scan_tiles<kTopkThreads>(tile_counts, int(gridDim.x), E, r.chunk, r.chunk2, r.tile_base,
+                               r.offsets, r.mtile_off, scan_part, scan_total, scan_off);
       if (r.perm) {
         // every routed row's place: the (tile, expert) base this CTA just
         // wrote plus the row's rank in its tile (other CTAs wrote those)
