@@ -51,16 +51,19 @@ OTHER_WORKLOADS = ["gptoss20b_prefill", "gptoss120b_prefill", "gptoss120b_skew16
 SUSTAINED_AFTER_MS = 1000.0
 
 
-def kernels_per_step(T: int, block_scaled: bool) -> int:
+def kernels_per_step(T: int, d: int, E: int, block_scaled: bool) -> int:
     """Kernels one moe_forward launches: router logits, router top-k, then
     gate_up and down with the combine (the block-scaled design runs the three
     in one kernel); plus the scan and the scatter when T has more than 8
     router tiles (else the last top-k CTA runs them), and the scatter whenever
-    the TMEM design needs its gathered f16 rows."""
+    the TMEM design needs its gathered f16 rows.  Above 8 router tiles with d a
+    multiple of 64 (and E <= 256) the logits run on the tensor cores, after a
+    kernel that splits the router weights into bf16 terms."""
     tiles = (T + 31) // 32
     experts = 1 if block_scaled else 2
     if tiles > FUSE_SCAN_TILES:
-        return 4 + experts
+        tc_split = 1 if (d % 64 == 0 and 1 <= E <= 256) else 0
+        return 4 + experts + tc_split
     return 2 + experts + (0 if block_scaled else 1)
 
 
@@ -488,7 +491,8 @@ def run_ours(args, wl):
                 "steps": args.other_steps, "design": "block-scaled" if r["mx"] else "tmem f16",
                 "roofline": {k_: oroof[k_] for k_ in ("bound", "kernel", "achieved", "unit",
                                                       "peak", "frac", "peak_source",
-                                                      "form_peak_tflops", "frac_of_form_peak")
+                                                      "form_peak_tflops", "frac_of_form_peak",
+                                                      "traffic", "frac_of_8tbs")
                              if k_ in oroof},
                 "stages_ms": {k_: round(v, 5) for k_, v in r["stage_ms"].items() if k_ != "_end"},
                 "active_experts": oact}
@@ -514,7 +518,7 @@ def run_ours(args, wl):
                 "h2d_bytes_per_step": main["h2d"], "d2h_bytes_per_step": main["d2h"],
                 "call": "moe_forward through the C ABI every step",
                 "graph_replay_value": whole_job_tokens_per_s(wl.T, world, e2e_graph)},
-        "gpu_launches": kernels_per_step(wl.T, mx) * args.steps,
+        "gpu_launches": kernels_per_step(wl.T, wl.d, wl.E, mx) * args.steps,
         "roofline": roof,
         "stages_ms": {k_: round(v, 5) for k_, v in main["stage_ms"].items() if k_ != "_end"},
         "active_experts": active,
