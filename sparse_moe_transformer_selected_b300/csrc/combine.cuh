@@ -22,9 +22,10 @@
 
 namespace moe {
 
-// Shared memory of combine_tile for chunks of up to `nb` rows.
-__host__ __device__ constexpr int combine_smem_bytes(int nb) {
-  return 16 + nb * 4 + nb * 8 * 4 * 2;   // count, token list, rows and weights (k <= 8)
+// Shared memory of combine_tile for chunks of up to `nb` rows and k <= 8
+// experts per token: count, token list, then k rows and k weights per token.
+__host__ __device__ constexpr int combine_smem_bytes(int nb, int k) {
+  return 16 + nb * 4 + nb * k * 4 * 2;
 }
 
 // Tokens i = i0, i0 + 4, ... < m of the list, columns c .. c + 3: a batch of B
@@ -44,7 +45,7 @@ __device__ __forceinline__ void combine_batches(const GemmArgs& a, int m, int c,
       for (int s = 0; s < KMAX; ++s) {
         const int i = ib + 4 * u;
         v[u][s] = (i < m && s < k)
-                      ? __ldcg(reinterpret_cast<const float4*>(y + size_t(rows[i * 8 + s]) * a.d + c))
+                      ? __ldcg(reinterpret_cast<const float4*>(y + size_t(rows[i * k + s]) * a.d + c))
                       : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
@@ -55,7 +56,7 @@ __device__ __forceinline__ void combine_batches(const GemmArgs& a, int m, int c,
 #pragma unroll
       for (int s = 0; s < KMAX; ++s) {             // slot order
         if (s < k) {
-          const float w = wts[i * 8 + s];
+          const float w = wts[i * k + s];
           acc.x = fmaf(w, v[u][s].x, acc.x);
           acc.y = fmaf(w, v[u][s].y, acc.y);
           acc.z = fmaf(w, v[u][s].z, acc.z);
@@ -82,8 +83,8 @@ __device__ __forceinline__ void combine_batches(const GemmArgs& a, int m, int c,
 
 // Called by the 128 epilogue threads of a CTA (tid 0..127) after each has
 // stored its y values of rows r0 .. r0 + n - 1 (n <= nb), output columns
-// [mt·128, mt·128 + 128).  `sm` is combine_smem_bytes(nb) of shared
-// memory; `bar_id` a named barrier free for these 128 threads.
+// [mt·128, mt·128 + 128).  `sm` is combine_smem_bytes(nb, a.k) bytes of
+// shared memory; `bar_id` a named barrier free for these 128 threads.
 //
 // The tokens this unit completes are listed first, with their k rows and
 // weights, by one thread per token; then each warp takes a quarter of them,
@@ -94,11 +95,11 @@ __device__ __forceinline__ void combine_batches(const GemmArgs& a, int m, int c,
 template <int B>
 __device__ __forceinline__ void combine_tile(const GemmArgs& a, int r0, int n, int mt, int tid,
                                              uint8_t* sm, int nb, uint32_t bar_id) {
+  const int k = a.k;
   int* nlast = reinterpret_cast<int*>(sm);
   int* tok = reinterpret_cast<int*>(sm + 16);
-  int* rows = tok + nb;                            // [nb][8]
-  float* wts = reinterpret_cast<float*>(rows + nb * 8);
-  const int k = a.k;
+  int* rows = tok + nb;                            // [nb][k]
+  float* wts = reinterpret_cast<float*>(rows + nb * k);
   if (tid == 0) *nlast = 0;
   __threadfence();                                 // this thread's y stores, before the count
   ptx::named_barrier(bar_id, 128);
@@ -115,8 +116,8 @@ __device__ __forceinline__ void combine_tile(const GemmArgs& a, int r0, int n, i
           row = 0;
           w = 0.f;
         }
-        rows[i * 8 + s] = row;
-        wts[i * 8 + s] = w;
+        rows[i * k + s] = row;
+        wts[i * k + s] = w;
       }
     }
   }

@@ -15,7 +15,7 @@ constexpr int kChunk = 16;
 // One CTA of 128 threads per (chunk of 16 permuted rows, output column tile),
 // all resident at once or not: the counts decide which CTA sums a token.
 __global__ void __launch_bounds__(128) combine_check_kernel(const GemmArgs a) {
-  __shared__ __align__(16) uint8_t sm[combine_smem_bytes(kChunk)];
+  __shared__ __align__(16) uint8_t sm[combine_smem_bytes(kChunk, 8)];
   const int r0 = blockIdx.x * kChunk;
   const int n = min(kChunk, a.R - r0);
   combine_tile<4>(a, r0, n, blockIdx.y, threadIdx.x, sm, kChunk, 1);

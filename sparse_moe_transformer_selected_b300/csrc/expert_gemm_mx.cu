@@ -218,7 +218,7 @@ __host__ __device__ inline Geo geometry(int d, int W, int stages) {
   g.off_bars = off;
   off += kNumBars * 8 + 16;           // barriers, TMEM base, abort flag
   g.off_comb = off;
-  off += combine_smem_bytes(kNB);
+  off += combine_smem_bytes(kNB, 8);
   off = (off + 15) & ~15;
   g.off_info = off;
   off += 2 * int(sizeof(UnitInfo));

@@ -122,9 +122,10 @@ struct Lay {
 };
 
 // Shared-memory plan for reduction length K (nsb = K/32 scale bytes per row),
-// token chunk nb and ring depths nc (codes) and nbs (activations).
+// token chunk nb, k experts per token and ring depths nc (codes) and nbs
+// (activations).
 template <Mode M>
-__host__ __device__ inline Lay layout(int nsb, int nb, int nc, int nbs) {
+__host__ __device__ inline Lay layout(int nsb, int nb, int k, int nc, int nbs) {
   Lay l{};
   int off = 0;
   l.codes = off;
@@ -142,7 +143,7 @@ __host__ __device__ inline Lay layout(int nsb, int nb, int nc, int nbs) {
   off += kNumBars * 8;
   l.misc = off;
   off += 16;                          // TMEM base, abort flag
-  off += (M == Mode::Down) ? combine_smem_bytes(nb) : 0;   // combine lists
+  off += (M == Mode::Down) ? combine_smem_bytes(nb, k) : 0;   // combine lists
   l.total = off;
   return l;
 }
@@ -354,7 +355,7 @@ moe_expert_gemm_tmem(const __grid_constant__ CUtensorMap map_w,
   const int NC = a.stages_c, NBS = a.stages_b;
   const int NAS = a_stages(a.nb);
   const int a_col0 = 2 * a.nb;                       // TMEM: accumulators first, then A
-  const Lay L = layout<M>(nsb, a.nb, NC, NBS);
+  const Lay L = layout<M>(nsb, a.nb, a.k, NC, NBS);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -805,24 +806,27 @@ cudaError_t make_map(CUtensorMap* map, CUtensorMapDataType dt, int esize, const 
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-// Ring depths for one launch.  The weight codes stream from HBM, whose
-// latency under load is several microseconds, so after a modest activation
-// ring (the activations are L2-resident) every remaining byte of shared memory
-// holds code stages in flight: about 10 x 16 KB at decode.
+// Ring depths for one launch.  Small chunks (decode-sized loads): a modest
+// activation ring, then every remaining byte of shared memory holds code
+// stages in flight (the weights stream from HBM, whose latency under load is
+// several microseconds): about 10 x 16 KB.  Large chunks: as many activation
+// stages as fit beside 3 code stages (gate_up) or 2 (down, whose stages carry
+// h hi and lo: 4 stages of 64 K at 160 tokens with 2 code stages measured 5-9%
+// faster than 3 with 4), then the rest as code stages.
 template <Mode M>
 void plan(GemmArgs& a) {
   const int K = (M == Mode::GateUp) ? a.d : a.W;
-  const int per_b = layout<M>(K / 32, a.nb, 0, 1).bstage;
+  const int per_b = layout<M>(K / 32, a.nb, a.k, 0, 1).bstage;
   int nbs;
   if (a.nb <= 32) {
     nbs = (48 * 1024) / per_b;                              // ~48 KB of activations
   } else {
-    const Lay base = layout<M>(K / 32, a.nb, 3, 0);         // keep 3 code stages
+    const Lay base = layout<M>(K / 32, a.nb, a.k, M == Mode::Down ? 2 : 3, 0);
     nbs = (kMaxSmem - 1024 - base.total) / per_b;
   }
   nbs = nbs < 2 ? 2 : nbs;
   nbs = nbs < kMaxB ? nbs : kMaxB;
-  const Lay base1 = layout<M>(K / 32, a.nb, 0, nbs);
+  const Lay base1 = layout<M>(K / 32, a.nb, a.k, 0, nbs);
   int nc = (kMaxSmem - 1024 - base1.total) / kCodeStageBytes;
   nc = nc < kMaxC ? nc : kMaxC;
   a.stages_b = nbs;
@@ -832,7 +836,7 @@ void plan(GemmArgs& a) {
 template <Mode M>
 size_t smem_bytes(const GemmArgs& a) {
   const int K = (M == Mode::GateUp) ? a.d : a.W;
-  return size_t(layout<M>(K / 32, a.nb, a.stages_c, a.stages_b).total) + 1024;
+  return size_t(layout<M>(K / 32, a.nb, a.k, a.stages_c, a.stages_b).total) + 1024;
 }
 
 template <Mode M, bool F16>

@@ -177,6 +177,26 @@ def test_all_tokens_one_expert():
     _check_full(dev, out, ref, 1)
 
 
+@pytest.mark.parametrize("n0,n1", [(192, 160), (193, 161), (384, 1)])
+def test_chunk_boundaries(n0, n1):
+    """Two experts take exactly n0 and n1 rows, so the TMEM design's token
+    chunks (192 rows for gate_up, 160 for down, above 32 rows per expert)
+    end exactly at an expert's last row, or one row before it; the tokens of
+    the two experts are interleaved at random."""
+    wl = gen.Workload("split", T=n0 + n1, d=256, W=256, E=2, k=1, seed=16)
+    inp = gen.make_inputs(wl)
+    # route on the sign of feature 0 alone: +1 -> expert 0, -1 -> expert 1
+    sign = np.ones(wl.T, dtype=np.float32)
+    sign[np.random.default_rng(17).permutation(wl.T)[:n1]] = -1.0
+    inp.x[:, 0] = gen.f32_to_bf16_bits(sign)
+    inp.router_w[:] = 0.0
+    inp.router_w[0, 0], inp.router_w[1, 0] = 10.0, -10.0
+    inp.router_b[:] = 0.0
+    dev, out, ref = _run(inp)
+    assert np.bincount(ref["topk_idx"].ravel(), minlength=2).tolist() == [n0, n1]
+    _check_full(dev, out, ref, 1)
+
+
 def test_identical_experts_give_router_independent_output():
     wl = gen.Workload("same", T=64, d=128, W=128, E=8, router_bias="normal", seed=14)
     inp = gen.make_inputs(wl)
