@@ -226,8 +226,9 @@ def roofline(wl, counts, stage_ms, step_ms, mx, peaks, peak_src, mma_peaks=None)
     roof["frac"] = roof["achieved"] / roof["peak"]
     if roof["bound"] == "tensor" and not mx and mma_peaks and mma_peaks.get("f16_tmem_a_n128"):
         # the rate of the instruction form the TMEM design issues (kind::f16,
-        # A in tensor memory, N = 128) on this GPU: down issues two MMAs (h hi,
-        # h lo) per K step, gate_up one
+        # A in tensor memory; its chunks are up to 192 tokens, and N = 128 and
+        # N = 256 measure the same rate) on this GPU: down issues two MMAs
+        # (h hi, h lo) per K step, gate_up one
         issued = roof["achieved"] * (2.0 if top == "down_combine" else 1.0)
         roof["form_peak_tflops"] = mma_peaks["f16_tmem_a_n128"]
         roof["frac_of_form_peak"] = issued / mma_peaks["f16_tmem_a_n128"]

@@ -271,7 +271,7 @@ moe_status moe_debug_combine(const float* y, const int32_t* perm, const int32_t*
  *            scales, operands in shared memory, N = 256 (the block-scaled
  *            design's kind)
  *   kind 2   kind::f16 with A read from tensor memory, N = 128 (the TMEM
- *            design's form at 128-token chunks)
+ *            design's form; its chunks are up to 192 tokens)
  *   kind 3   kind::f16 with A read from tensor memory, N = 256
  * One CTA per SM issues iters x 4 MMAs back to back; the launch is timed with
  * CUDA events on `stream` (synchronises it).  workspace: 4 bytes of device
