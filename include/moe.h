@@ -282,7 +282,7 @@ moe_status moe_mma_peak(int kind, int iters, double* tflops, void* workspace, vo
 
 /*
  * Size of the scratch array built into the library for moe_forward_noalloc:
- * 16 MiB, enough for about 128 tokens at d = W = 2880 with k = 4.
+ * 16 MiB, enough for up to 144 tokens at d = W = 2880 with k = 4 (E <= 128).
  */
 #define MOE_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
 

@@ -10,7 +10,7 @@
 // array below.  It is a convenience wrapper with no counterpart on the pages
 // the block follows.
 //
-// The array is sized for decode-sized batches (about 128 tokens at
+// The array is sized for decode-sized batches (up to 144 tokens at
 // d = W = 2880, top-4); every GPU that loads the library holds it until the
 // process exits.  Every call shares it: calls that overlap on the GPU (on two
 // streams, or from two threads) race on the same scratch and must not be
@@ -100,7 +100,7 @@ moe_status moe_forward_noalloc(const void* x_bf16, int64_t T, int d, int W,
     moe::set_last_error("moe_forward_noalloc: this shape needs " + std::to_string(need) +
                         " bytes of scratch but the built-in array holds " +
                         std::to_string(kScratchBytes) +
-                        " (about 128 tokens at d = W = 2880, k = 4); use moe_forward with a"
+                        " (up to 144 tokens at d = W = 2880, k = 4); use moe_forward with a"
                         " workspace");
     return MOE_ERR_WORKSPACE;
   }

@@ -37,6 +37,15 @@ def test_oversize_shape_is_rejected_before_any_gpu_work():
                                    v[7], v[8], 32, 4, 7.0, 1.702, v[9], None) == 2
 
 
+def test_scratch_fits_the_stated_decode_sizes():
+    """The header's size statement: the built-in scratch holds the workspace of
+    up to 144 tokens at d = W = 2880, k = 4, for 32 and for 128 experts."""
+    moe.load()
+    for E in (32, 128):
+        assert moe.moe_workspace_bytes(144, 2880, 2880, E, 4) <= moe.NOALLOC_SCRATCH_BYTES
+        assert moe.moe_workspace_bytes(145, 2880, 2880, E, 4) > moe.NOALLOC_SCRATCH_BYTES
+
+
 def test_zero_tokens_gets_the_same_argument_checks():
     """With T = 0 the call enqueues nothing but still rejects what moe_forward
     rejects (the fake addresses are never used)."""
