@@ -32,10 +32,12 @@ route_scan_kernel(const int32_t* __restrict__ tile_counts, int ntiles, int E, in
                            total, off);
 }
 
-// One warp per routed row (t, j): write perm / inv and copy x[t] to its row,
-// converted to f16 after an exact power-of-two scaling by 2^e_t (e_t puts the
-// token's largest |x| in [2^14, 2^15), so every bf16 value is held exactly).
-__global__ void __launch_bounds__(256)
+// One warp per token t: for each of its k routed rows (t, j) write perm / inv
+// and copy x[t] to the row, converted to f16 after an exact power-of-two
+// scaling by 2^e_t (e_t puts the token's largest |x| in [2^14, 2^15), so every
+// bf16 value is held exactly).  The token is read and converted once for its
+// k rows.  A slot whose expert or row is out of range is skipped and recorded.
+__global__ void __launch_bounds__(256, 2)
 route_scatter_kernel(const __nv_bfloat16* __restrict__ x, int T, int d, int E, int k,
                      const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ rank,
                      const int32_t* __restrict__ tile_base,
@@ -43,80 +45,96 @@ route_scatter_kernel(const __nv_bfloat16* __restrict__ x, int T, int d, int E, i
                      __half* __restrict__ x_perm, int32_t* __restrict__ rowexp,
                      int32_t* __restrict__ status) {
   const int64_t R = (int64_t)T * k;
-  const int64_t q = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   pdl_wait();
-  if (q >= R) return;
-  const int t = (int)(q / k);
-  const int e = topk_idx[q];
-  if (e < 0 || e >= E) {
-    if (lane == 0) atomicMax(status, kStatusBounds);
-    return;
-  }
-  const int64_t row = (int64_t)tile_base[(size_t)(t / kRouterTile) * E + e] + rank[q];
-  if (row < 0 || row >= R) {
-    if (lane == 0) atomicMax(status, kStatusBounds);
-    return;
-  }
-  if (lane == 0) {
-    if (perm) perm[row] = (int32_t)q;
-    if (inv) inv[q] = (int32_t)row;
-  }
-  if (x_perm) {
-    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * d);
-    uint4* dst = reinterpret_cast<uint4*>(x_perm + (size_t)row * d);
-    const int n16 = d / 8;
-    auto absmax8 = [](const uint4& v, float m) {
-      const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+  if (t >= T) return;
+  // the token's rows (-1: a slot left out); k <= 8, loops unrolled so the
+  // rows stay in registers
+  int64_t rows[8];
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
-        m = fmaxf(m, fmaxf(fabsf(__uint_as_float(in[c] << 16)), fabsf(__uint_as_float(in[c] & 0xFFFF0000u))));
-      return m;
-    };
-    auto to_f16 = [](const uint4& v, float f) {
-      const uint32_t in[4] = {v.x, v.y, v.z, v.w};
-      uint32_t o[4];
+  for (int j = 0; j < 8; ++j) {
+    rows[j] = -1;
+    if (j >= k) continue;
+    const int64_t q = t * k + j;
+    const int e = topk_idx[q];
+    int64_t row = -1;
+    if (e >= 0 && e < E) row = (int64_t)tile_base[(size_t)(t / kRouterTile) * E + e] + rank[q];
+    if (row < 0 || row >= R) {
+      if (lane == 0) atomicMax(status, kStatusBounds);
+      row = -1;
+    } else if (lane == 0) {
+      if (perm) perm[row] = (int32_t)q;
+      if (inv) inv[q] = (int32_t)row;
+    }
+    rows[j] = row;
+  }
+  if (!x_perm) return;
+  const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * d);
+  const int n16 = d / 8;
+  auto absmax8 = [](const uint4& v, float m) {
+    const uint32_t in[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const float lo = __uint_as_float(in[c] << 16) * f;
-        const float hi = __uint_as_float(in[c] & 0xFFFF0000u) * f;
-        const __half2 h = __floats2half2_rn(lo, hi);
-        o[c] = *reinterpret_cast<const uint32_t*>(&h);
-      }
-      return make_uint4(o[0], o[1], o[2], o[3]);
-    };
-    auto exponent = [&](float xmax) {
+    for (int c = 0; c < 4; ++c)
+      m = fmaxf(m, fmaxf(fabsf(__uint_as_float(in[c] << 16)), fabsf(__uint_as_float(in[c] & 0xFFFF0000u))));
+    return m;
+  };
+  auto to_f16 = [](const uint4& v, float f) {
+    const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) xmax = fmaxf(xmax, __shfl_xor_sync(0xffffffffu, xmax, off));
-      return (xmax > 0.f && isfinite(xmax)) ? max(-126, min(126, 14 - ilogbf(xmax))) : 0;
-    };
-    // A row of up to 32 x kRowRegs 16-byte pieces (d <= 3072) is read once into
-    // registers, all loads in flight together; longer rows take two passes.
-    constexpr int kRowRegs = 12;
-    if (n16 <= 32 * kRowRegs) {
-      uint4 v[kRowRegs];
-      float xmax = 0.f;                                  // largest |x| of the token
+    for (int c = 0; c < 4; ++c) {
+      const float lo = __uint_as_float(in[c] << 16) * f;
+      const float hi = __uint_as_float(in[c] & 0xFFFF0000u) * f;
+      const __half2 h = __floats2half2_rn(lo, hi);
+      o[c] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+  };
+  auto exponent = [&](float xmax) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) xmax = fmaxf(xmax, __shfl_xor_sync(0xffffffffu, xmax, off));
+    return (xmax > 0.f && isfinite(xmax)) ? max(-126, min(126, 14 - ilogbf(xmax))) : 0;
+  };
+  // A row of up to 32 x kRowRegs 16-byte pieces (d <= 3072) is read once into
+  // registers, all loads in flight together, and converted once; longer rows
+  // take a pass for the maximum and one per routed row.
+  constexpr int kRowRegs = 12;
+  if (n16 <= 32 * kRowRegs) {
+    uint4 v[kRowRegs];
+    float xmax = 0.f;                                  // largest |x| of the token
+#pragma unroll
+    for (int j = 0; j < kRowRegs; ++j) {
+      const int i = lane + 32 * j;
+      v[j] = i < n16 ? src[i] : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int j = 0; j < kRowRegs; ++j) xmax = absmax8(v[j], xmax);
+    const int et = exponent(xmax);
+    const float f = __int_as_float((et + 127) << 23);  // 2^e_t, |e_t| <= 126
+#pragma unroll
+    for (int j = 0; j < kRowRegs; ++j) v[j] = to_f16(v[j], f);
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      if (rows[s] < 0) continue;
+      if (lane == 0) rowexp[rows[s]] = et;
+      uint4* dst = reinterpret_cast<uint4*>(x_perm + (size_t)rows[s] * d);
 #pragma unroll
       for (int j = 0; j < kRowRegs; ++j) {
         const int i = lane + 32 * j;
-        v[j] = i < n16 ? src[i] : make_uint4(0, 0, 0, 0);
+        if (i < n16) dst[i] = v[j];
       }
+    }
+  } else {
+    float xmax = 0.f;
+    for (int i = lane; i < n16; i += 32) xmax = absmax8(src[i], xmax);
+    const int et = exponent(xmax);
+    const float f = __int_as_float((et + 127) << 23);
 #pragma unroll
-      for (int j = 0; j < kRowRegs; ++j) xmax = absmax8(v[j], xmax);
-      const int et = exponent(xmax);
-      if (lane == 0) rowexp[row] = et;
-      const float f = __int_as_float((et + 127) << 23);  // 2^e_t, |e_t| <= 126
-#pragma unroll
-      for (int j = 0; j < kRowRegs; ++j) {
-        const int i = lane + 32 * j;
-        if (i < n16) dst[i] = to_f16(v[j], f);
-      }
-    } else {
-      float xmax = 0.f;
-      for (int i = lane; i < n16; i += 32) xmax = absmax8(src[i], xmax);
-      const int et = exponent(xmax);
-      if (lane == 0) rowexp[row] = et;
-      const float f = __int_as_float((et + 127) << 23);
+    for (int s = 0; s < 8; ++s) {
+      if (rows[s] < 0) continue;
+      if (lane == 0) rowexp[rows[s]] = et;
+      uint4* dst = reinterpret_cast<uint4*>(x_perm + (size_t)rows[s] * d);
       for (int i = lane; i < n16; i += 32) dst[i] = to_f16(src[i], f);
     }
   }
@@ -136,9 +154,8 @@ cudaError_t launch_route_scatter(const __nv_bfloat16* x, int T, int d, int E, in
                                  const int32_t* tile_base, int32_t* perm, int32_t* inv,
                                  void* x_perm, int32_t* rowexp, int32_t* status,
                                  cudaStream_t s) {
-  const int64_t R = (int64_t)T * k;
   const int warps_per_block = 8;
-  const int64_t grid = (R + warps_per_block - 1) / warps_per_block;
+  const int64_t grid = ((int64_t)T + warps_per_block - 1) / warps_per_block;
   return launch_pdl(route_scatter_kernel, dim3((unsigned)grid), dim3(warps_per_block * 32), 0, s,
                     x, T, d, E, k, topk_idx, rank, tile_base, perm, inv,
                     static_cast<__half*>(x_perm), rowexp, status);
