@@ -60,24 +60,24 @@ bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) !
 // sm_103 check, once per device.
 moe_status check_device() {
   static std::mutex mu;
-  static int verdict[64];  // 0 unknown, 1 ok, 2 unsupported
+  static int arch_ok[64];  // 0 unknown, 1 ok, 2 unsupported
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   if (dev < 0 || dev >= 64) return fail(MOE_ERR_UNSUPPORTED, "device ordinal %d", dev);
   std::lock_guard<std::mutex> lock(mu);
-  if (verdict[dev] == 0) {
+  if (arch_ok[dev] == 0) {
     int major = 0, minor = 0;
     e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
-    verdict[dev] = (major == 10 && minor == 3) ? 1 : 2;
-    if (verdict[dev] == 2) {
+    arch_ok[dev] = (major == 10 && minor == 3) ? 1 : 2;
+    if (arch_ok[dev] == 2) {
       g_last_error = "device is sm_" + std::to_string(major) + std::to_string(minor) +
                      "; this library is built for sm_103a only";
     }
   }
-  if (verdict[dev] != 1) return fail(MOE_ERR_UNSUPPORTED, "device is not sm_103 (B300)");
+  if (arch_ok[dev] != 1) return fail(MOE_ERR_UNSUPPORTED, "device is not sm_103 (B300)");
   return MOE_OK;
 }
 
