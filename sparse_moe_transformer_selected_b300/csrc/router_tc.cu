@@ -243,7 +243,9 @@ int router_tc_e_pad(int E) { return (E + kM - 1) / kM * kM; }
 
 int router_tc_splits(int64_t T, int d, int E, int* k_len) {
   const int64_t tiles = ((T + kN - 1) / kN) * (router_tc_e_pad(E) / kM);
-  int64_t want = (int64_t(device_sm_count()) + tiles - 1) / tiles;
+  // as many d ranges as keep the CTAs within one wave (a CTA per SM): a
+  // partial second wave of these short, latency-bound CTAs costs a whole CTA time
+  int64_t want = int64_t(device_sm_count()) / tiles;
   const int64_t stages = d / kK;
   if (want > stages) want = stages;
   if (want > kRouterTcMaxSplits) want = kRouterTcMaxSplits;
