@@ -154,6 +154,7 @@ cudaError_t launch_route_scatter(const __nv_bfloat16* x, int T, int d, int E, in
                                  const int32_t* tile_base, int32_t* perm, int32_t* inv,
                                  void* x_perm, int32_t* rowexp, int32_t* status,
                                  cudaStream_t s) {
+  if (k < 1 || k > 8) return cudaErrorInvalidValue;   // a warp keeps at most 8 rows of its token
   const int warps_per_block = 8;
   const int64_t grid = ((int64_t)T + warps_per_block - 1) / warps_per_block;
   return launch_pdl(route_scatter_kernel, dim3((unsigned)grid), dim3(warps_per_block * 32), 0, s,
